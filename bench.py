@@ -1,0 +1,374 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV hot path on GB300.
+
+One step = one pass of the whole hot path over one batch: paged_kv_write of
+the batch's new K/V rows, then paged_attention_forward over the block pool.
+Default workload: the decode batch (64 sequences, contexts U[512, 4096], one
+query token each, 32 q / 8 kv heads, head_dim 128, block_size 16, bf16, a
+20000-block pool, seeded random block permutation).  Also measured (extra
+keys): the mixed continuous batch (8 prefill chunks of 512 tokens + 120
+decodes) as query tokens/s.
+
+Metric: algorithmic bytes of a step (unique K/V bytes read + q read + output
+written + the write path's read and write of the new rows + block-table
+entries used) / step time, in GB/s.  Inputs sit in HBM before the timed
+region; L2 (129 MB) is flushed between steps by writing a 512 MB buffer
+outside the timed events.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+instead, on a bounded sample of the same workload, on the host cores.
+Multi-GPU (torchrun): independent replicas, one per rank (the path needs no
+exchange); value = all ranks' bytes / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn decode KV GB/s (% HBM peak); mixed-batch query tokens/s"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1950.7)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic_bytes(w) -> dict:
+    """Bytes a perfect implementation must move for one step of workload w."""
+    st = w.step
+    es = 2 if w.dtype == "bf16" else 4
+    Hkv, D, Hq = w.num_kv_heads, w.head_dim, w.num_q_heads
+    L = st.context_lens.astype(np.int64)
+    shared = int(w.meta.get("shared_prefix_tokens", 0))
+    # unique KV tokens: a shared prefix is read from HBM once
+    uniq_tokens = int(L.sum()) - (shared * (len(L) - 1) if shared else 0)
+    kv = uniq_tokens * Hkv * D * es * 2
+    T = st.num_tokens
+    qo = 2 * T * Hq * D * es
+    write = 4 * T * Hkv * D * es + 8 * T
+    bt = int(((L + w.block_size - 1) // w.block_size).sum()) * 4 + 8 * len(L) + 4
+    attn = kv + qo
+    return {"step": attn + write + bt, "attn_kernel": kv + qo, "kv": kv, "write": write}
+
+
+def mma_flops(w) -> float:
+    """Unmasked QK^T and PV flops of the multi-token sequences."""
+    st = w.step
+    tot = 0.0
+    for s in range(st.num_seqs):
+        n, L = int(st.q_lens[s]), int(st.context_lens[s])
+        if n * (w.num_q_heads // w.num_kv_heads) <= 4:
+            continue
+        pairs = sum(L - n + i + 1 for i in range(n)) if w.causal else n * L
+        tot += 4.0 * w.head_dim * w.num_q_heads * pairs
+    return tot
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.lines = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "20"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _gpu_id(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[dev.index or 0] if vis else str(dev.index or 0)
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_236_gb300 as pkv
+    import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    hbm_peak, bf16_peak, peak_kind = _peaks()
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    def prepare(w):
+        st = w.step
+        return dict(kc=to_dev(w.k_cache), vc=to_dev(w.v_cache), q=to_dev(st.q), k=to_dev(st.k_new),
+                    v=to_dev(st.v_new), slots=torch.from_numpy(st.slot_mapping).to(dev),
+                    bt=torch.from_numpy(st.block_tables).to(dev), ctx=torch.from_numpy(st.context_lens).to(dev),
+                    qsl=torch.from_numpy(st.query_start_loc).to(dev), mql=int(st.q_lens.max(initial=0)))
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(w, t, steps, warmup):
+        out = torch.empty_like(t["q"])
+        ws = torch.empty(pkv.workspace_size(w.step.num_seqs, w.step.num_tokens, w.num_q_heads, w.num_kv_heads,
+                                            w.head_dim), dtype=torch.uint8, device=dev)
+
+        def one():
+            pkv.paged_kv_write(t["k"], t["v"], t["slots"], t["kc"], t["vc"])
+            pkv.paged_attention_forward(t["q"], t["kc"], t["vc"], t["bt"], t["ctx"], t["qsl"], w.scale, w.causal,
+                                        out=out, workspace=ws, max_query_len=t["mql"])
+
+        for _ in range(warmup):
+            flush.fill_(1)
+            one()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e in ev:  # torch creates CUDA events lazily: create them before the library records them
+            e[2].record()
+            e[3].record()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        for e in ev:
+            flush.fill_(1)
+            pkv.set_profile_events(e[2], e[3])
+            e[0].record()
+            one()
+            e[1].record()
+        pkv.set_profile_events(None, None)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
+        kern_ms = [pkv.profile_elapsed_ms(c, d) for _, _, c, d in ev]
+        return step_ms, kern_ms, out
+
+    # ---------------- headline: decode batch ----------------
+    w = wl.decode_batch(seed=1002 + rank)
+    t = prepare(w)
+    sampler = ClockSampler(_gpu_id(torch, dev))
+    time.sleep(0.3)
+    step_ms, kern_ms, out = timed(w, t, args.steps, args.warmup)
+    clocks = sampler.stop()
+    flags = pkv.device_errors()
+    if flags:
+        raise SystemExit(f"device error word set: {flags:#x}")
+    ab = algorithmic_bytes(w)
+    tot_ms = sum(step_ms)
+    if world > 1:
+        tt = torch.tensor([tot_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        tot_ms = float(tt.item())
+    value = ab["step"] * args.steps * world / (tot_ms * 1e-3) / 1e9
+    kern_avg_ms = sum(kern_ms) / len(kern_ms)
+    achieved = ab["attn_kernel"] / (kern_avg_ms * 1e-3) / 1e9
+
+    # ---------------- e2e through the public API, host buffers ----------------
+    st = w.step
+    pin = lambda a: (torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+                     if a.dtype == np.uint16 else torch.from_numpy(np.ascontiguousarray(a))).pin_memory()
+    host_in = dict(q=pin(st.q), k=pin(st.k_new), v=pin(st.v_new), slots=pin(st.slot_mapping),
+                   bt=pin(st.block_tables), ctx=pin(st.context_lens), qsl=pin(st.query_start_loc))
+    host_out = torch.empty(tuple(st.q.shape), dtype=t["q"].dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    ws = torch.empty(pkv.workspace_size(st.num_seqs, st.num_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim),
+                     dtype=torch.uint8, device=dev)
+    e2e_ms = []
+    for it in range(args.warmup + args.steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        d = {k2: x.to(dev, non_blocking=True) for k2, x in host_in.items()}
+        pkv.paged_kv_write(d["k"], d["v"], d["slots"], t["kc"], t["vc"])
+        o = pkv.paged_attention_forward(d["q"], t["kc"], t["vc"], d["bt"], d["ctx"], d["qsl"], w.scale, w.causal,
+                                        workspace=ws, max_query_len=1)
+        host_out.copy_(o, non_blocking=True)
+        b.record()
+        b.synchronize()
+        if it >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_tot = sum(e2e_ms)
+    if world > 1:
+        tt = torch.tensor([e2e_tot], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_tot = float(tt.item())
+    e2e_value = ab["step"] * args.steps * world / (e2e_tot * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tot_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode batch: 64 seqs, context U[512,4096], 1 query token, 32q/8kv heads, "
+                               "head_dim 128, block_size 16, 20000-block pool, random block permutation, bf16; "
+                               "step = paged_kv_write + paged_attention_forward",
+                   "l2": "flushed between steps (512 MB write outside the timed events)",
+                   "bytes_per_step": ab["step"], "kv_bytes": ab["kv"],
+                   "parallelism": f"replicas x{world}"},
+        "hbm_frac": round(value / hbm_peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel (attention kernels, per launch)",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
+                     "traffic": None, "kernel_ms": round(kern_avg_ms, 5),
+                     "algorithmic_bytes_per_launch": ab["attn_kernel"]},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_tot / args.steps, 5)},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+
+    # ---------------- mixed continuous batch (query tokens/s) ----------------
+    if args.mixed:
+        wm = wl.mixed_batch(seed=1003 + rank)
+        tm = prepare(wm)
+        ms_m, kern_m, _ = timed(wm, tm, max(3, args.steps // 2), args.warmup)
+        avg = sum(ms_m) / len(ms_m)
+        fl = mma_flops(wm)
+        result["mixed_batch"] = {
+            "value": round(wm.step.num_tokens / (avg * 1e-3), 1), "unit": "query tokens/s",
+            "ms_per_step": round(avg, 5), "attn_kernels_ms": round(sum(kern_m) / len(kern_m), 5),
+            "bytes_per_step": algorithmic_bytes(wm)["step"],
+            "hbm_frac": round(algorithmic_bytes(wm)["step"] / (avg * 1e-3) / 1e9 / hbm_peak, 4),
+            "prefill_unmasked_tflop": round(fl / 1e12, 4)}
+        result["gpu_launches"] += 4 * len(ms_m)
+        del tm
+
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    return result
+
+
+def cpu_baseline(w, budget_s: float = 15.0) -> dict:
+    """The fp64 oracle, as it stands, on sequences of the same workload until
+    the time budget is spent; GB/s over the algorithmic bytes of the rows it
+    produced."""
+    import workloads as wl
+    from oracle import paged_oracle as po
+    st = w.step
+    es = 2 if w.dtype == "bf16" else 4
+    kc, vc = w.k_cache, w.v_cache
+    done, nbytes = 0, 0
+    t0 = time.perf_counter()
+    for s in range(st.num_seqs):
+        a, b = int(st.query_start_loc[s]), int(st.query_start_loc[s + 1])
+        L = int(st.context_lens[s])
+        K = wl.to_f64(po.gather(kc, st.block_tables[s], L), w.dtype)
+        V = wl.to_f64(po.gather(vc, st.block_tables[s], L), w.dtype)
+        po.attend(wl.to_f64(st.q[a:b], w.dtype), K, V, w.scale, w.causal)
+        done += 1
+        nbytes += L * w.num_kv_heads * w.head_dim * es * 2 + 2 * (b - a) * w.num_q_heads * w.head_dim * es
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {done} of {st.num_seqs} sequences of the decode batch (gather + fp64 attention, "
+                      f"numpy BLAS threads default), {dt:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step one bounded sample (the
+    oracle on sequences of the decode batch for ~budget seconds)."""
+    import workloads as wl
+    w = wl.decode_batch()
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(w, budget_s=max(1.0, args.cpu_seconds / max(1, args.steps)))
+        if i >= args.warmup:
+            vals.append(r)
+    value = statistics.median(v["value"] for v in vals)
+    cb = dict(vals[-1], value=value)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode batch: 64 seqs, context U[512,4096], 1 query token, 32q/8kv heads, "
+                                   "head_dim 128, block_size 16, bf16 inputs widened to fp64 by the oracle"},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-mixed", dest="mixed", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

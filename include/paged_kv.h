@@ -1,0 +1,192 @@
+/*
+ * paged_kv.h - C ABI of a GB300 (sm_103a) library for attention over a
+ * block-paged KV cache.
+ *
+ * The operations follow the source pages:
+ *   - "ADR 004: Paged Attention Serving Integration" (Decision 4): the model
+ *     writes each layer's K/V rows into a block allocator and reads them back
+ *     through paged_attention_forward; prefill chunks and decode steps share
+ *     one call (Consequences).
+ *   - "Paged Attention 基础 - 原理与实现进度", section 2: a sequence's
+ *     logical positions map to physical blocks through a block table; a
+ *     query gathers its keys block by block, applies the causal mask and
+ *     computes softmax(QK^T)V; several tables may name the same physical
+ *     block (prefix sharing).  Section 3.2 names the metadata: block_tables,
+ *     slot_mapping, context_lens.
+ *   - Dao-AILab/flash-attention issue #660: several query tokens per
+ *     sequence (speculative decoding) next to single-token decode; the caller
+ *     owns the cache manager and calls kernels only.
+ *
+ * Layouts (row-major, innermost dimension contiguous):
+ *   block pool, per layer   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim]
+ *   new K/V rows            k, v              [num_tokens, num_kv_heads, head_dim]
+ *                                             (token stride may exceed num_kv_heads*head_dim)
+ *   queries / output        q, out            [num_tokens, num_q_heads, head_dim]
+ *   slot_mapping            int64  [num_tokens]; slot = block * block_size + offset; < 0 skips
+ *   block_tables            int32  [num_seqs, max_blocks_per_seq]; entries past a sequence's
+ *                                  last block are ignored (may be -1)
+ *   context_lens            int32  [num_seqs]; tokens in the cache AFTER this step's write,
+ *                                  the sequence's new (query) tokens included
+ *   query_start_loc         int32  [num_seqs + 1]; query rows of sequence s are
+ *                                  q[query_start_loc[s] : query_start_loc[s+1]]
+ *
+ * Semantics: query i of a sequence with n queries and L tokens sits at
+ * position L - n + i; with causal != 0 it attends keys 0 .. L-n+i, otherwise
+ * all L keys.  Query head h reads kv head h / (num_q_heads / num_kv_heads).
+ * The result is softmax(scale * q k^T) v accumulated in fp32 and cast to the
+ * dtype of q (round to nearest even).
+ *
+ * Ownership: every buffer is the caller's (device memory unless stated);
+ * the library allocates no device memory and keeps no state across calls
+ * except the cached driver entry point and the sticky device error word.
+ * Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).  Pointers must be 16-byte aligned.
+ *
+ * Errors: host-checkable problems return a status before any launch and set a
+ * thread-local message (pkv_last_error).  Metadata that only the device sees
+ * (a block id outside [0, num_blocks), a slot outside the pool, a sequence
+ * with more queries than tokens or a non-monotone query_start_loc, a context
+ * longer than its table) never faults: the offending access is skipped (or
+ * read as zeros), the sequence's output rows are zero, and a bit is set in
+ * the sticky device error word that pkv_device_errors reads.
+ */
+#ifndef PAGED_KV_H_
+#define PAGED_KV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or shape */
+  PKV_ERR_UNSUPPORTED = 2,  /* valid but not implemented (dtype, head_dim, block_size, GPU) */
+  PKV_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a launch failed */
+  PKV_ERR_WORKSPACE = 4     /* workspace missing or smaller than required */
+} pkv_status;
+
+typedef enum {
+  PKV_DTYPE_F32 = 0,
+  PKV_DTYPE_BF16 = 1
+} pkv_dtype;
+
+/* Device error word bits (pkv_device_errors). */
+#define PKV_DEVERR_SLOT_OUT_OF_RANGE 0x1   /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_DEVERR_BLOCK_OUT_OF_RANGE 0x2  /* block table entry outside [0, num_blocks) */
+#define PKV_DEVERR_BAD_SEQUENCE 0x4        /* q_len < 0, q_len > context_len, context too long */
+#define PKV_DEVERR_TIMEOUT 0x8             /* a bounded in-kernel wait gave up */
+#define PKV_DEVERR_PLAN_OVERFLOW 0x10      /* work list did not fit the workspace */
+
+/*
+ * paged_kv_write - scatter new K/V rows into the block pool.
+ *
+ * For every t < num_tokens with s = slot_mapping[t] >= 0:
+ *   k_cache[s / block_size][s % block_size][:][:] = k[t][:][:]   (and v likewise)
+ * A bit-exact copy in `dtype`.  ("ADR 004", Decision 4; "Paged Attention 基础",
+ * section 2: token position -> physical block and slot.)
+ *
+ *   k, v            device, [num_tokens, num_kv_heads, head_dim], token stride
+ *                   k_token_stride / v_token_stride ELEMENTS (>= num_kv_heads*head_dim;
+ *                   0 means dense)
+ *   slot_mapping    device int64 [num_tokens]
+ *   k_cache,v_cache device [num_blocks, block_size, num_kv_heads, head_dim]
+ * Two tokens with the same non-negative slot in one call: which one lands is
+ * unspecified.  Writes into a block shared by several tables are the
+ * caller's responsibility (copy-on-write belongs to the cache manager).
+ * num_tokens == 0 is a no-op.
+ */
+pkv_status paged_kv_write(const void* k, const void* v, const int64_t* slot_mapping,
+                          void* k_cache, void* v_cache,
+                          int64_t num_tokens, int64_t num_blocks, int32_t block_size,
+                          int32_t num_kv_heads, int32_t head_dim,
+                          int64_t k_token_stride, int64_t v_token_stride,
+                          pkv_dtype dtype, void* stream);
+
+/*
+ * paged_attention_workspace_size - bytes of device workspace that
+ * paged_attention_forward wants for a batch of this shape (an upper bound
+ * of what it uses; any smaller size >= paged_attention_workspace_min also
+ * works, with fewer KV splits).  Pure host arithmetic.
+ */
+size_t paged_attention_workspace_size(int32_t num_seqs, int64_t num_tokens, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim);
+
+/* Smallest workspace paged_attention_forward accepts for this shape. */
+size_t paged_attention_workspace_min(int32_t num_seqs, int64_t num_tokens, int32_t num_q_heads,
+                                     int32_t num_kv_heads, int32_t head_dim);
+
+/*
+ * paged_attention_forward - varlen attention through per-sequence block
+ * tables.  One call serves prefill chunks, single-token decode and
+ * multi-token speculative verification ("ADR 004", Consequences;
+ * flash-attention issue #660), with GQA/MQA (num_q_heads a multiple of
+ * num_kv_heads) and physically shared blocks.
+ *
+ *   q               device [num_tokens, num_q_heads, head_dim], dtype
+ *   k_cache,v_cache device [num_blocks, block_size, num_kv_heads, head_dim], dtype
+ *   block_tables    device int32 [num_seqs, max_blocks_per_seq]
+ *   context_lens    device int32 [num_seqs]
+ *   query_start_loc device int32 [num_seqs + 1], query_start_loc[num_seqs] == num_tokens
+ *   out             device [num_tokens, num_q_heads, head_dim], dtype; every row of
+ *                   every sequence is written
+ *   max_query_len   host hint: an upper bound of every sequence's query count, or
+ *                   0 if unknown (only used to skip launching kernels with no work)
+ *   scale           logit scale (e.g. 1/sqrt(head_dim))
+ *   causal          non-zero: bottom-right aligned causal mask
+ *   workspace       device scratch of workspace_bytes (>= paged_attention_workspace_min),
+ *                   256-byte aligned; overwritten by the call; must not be shared by
+ *                   calls that may run concurrently
+ * Supported: dtype bf16 or f32; head_dim 64 or 128; block_size 8, 16, 32 or 64;
+ * num_q_heads / num_kv_heads <= 128.
+ * Rows of a sequence whose metadata is invalid (see the error notes above)
+ * are written as zeros.
+ */
+pkv_status paged_attention_forward(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, const int32_t* context_lens,
+                                   const int32_t* query_start_loc, void* out,
+                                   int32_t num_seqs, int64_t num_tokens, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                                   int32_t block_size, int32_t max_blocks_per_seq,
+                                   int32_t max_query_len, float scale, int32_t causal,
+                                   void* workspace, size_t workspace_bytes, pkv_dtype dtype,
+                                   void* stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* pkv_last_error(void);
+
+/*
+ * pkv_device_errors - read (and with clear != 0, reset) the sticky device
+ * error word of the current device (PKV_DEVERR_* bits).  Synchronises the
+ * device.  Returns PKV_OK and stores the word in *flags.
+ */
+pkv_status pkv_device_errors(int32_t* flags, int32_t clear);
+
+/*
+ * pkv_set_profile_events - instrumentation for benchmarks.  With both
+ * arguments non-NULL (cudaEvent_t handles), later paged_attention_forward
+ * calls made on this thread record `start` on their stream right before the
+ * first attention kernel (after the planner) and `stop` right after the last
+ * one (before the split merge), so the attention kernels can be timed alone
+ * with cudaEventElapsedTime.  NULL, NULL turns it off.  The events stay the
+ * caller's.
+ */
+void pkv_set_profile_events(void* start, void* stop);
+
+/*
+ * pkv_event_elapsed_ms - milliseconds between two recorded events
+ * (cudaEventElapsedTime), for events recorded by this library.  Returns
+ * PKV_ERR_CUDA if either has not completed.
+ */
+pkv_status pkv_event_elapsed_ms(void* start, void* stop, float* ms);
+
+/* Library version string, e.g. "paged_kv 0.1.0 sm_103a". */
+const char* pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_H_ */

@@ -1,0 +1,231 @@
+"""Attention over a block-paged KV cache on GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI of ``libpaged_kv.so`` (declared in
+``include/paged_kv.h``): argument marshalling only - every step of the path
+runs in the library's CUDA kernels.  PyTorch supplies device memory and the
+current stream.  There is no CPU fallback: if the library is missing or the
+tensors are not on a CUDA device, the calls raise.
+
+    paged_kv_write(k, v, slot_mapping, k_cache, v_cache)
+    paged_attention_forward(q, k_cache, v_cache, block_tables, context_lens,
+                            query_start_loc, scale, causal)
+
+Block pool per layer: ``[num_blocks, block_size, num_kv_heads, head_dim]``
+("ADR 004: Paged Attention Serving Integration", Decision 4 - a per-layer
+cache tensor; "Paged Attention 基础", section 2 - fixed-size physical
+blocks named by block tables).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "paged_kv_write", "paged_attention_forward", "workspace_size", "workspace_min",
+    "device_errors", "set_profile_events", "profile_elapsed_ms", "lib", "LibraryError", "DEVERR",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpaged_kv.so")
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_WORKSPACE = range(5)
+DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+DEVERR = {
+    "slot_out_of_range": 0x1,
+    "block_out_of_range": 0x2,
+    "bad_sequence": 0x4,
+    "timeout": 0x8,
+    "plan_overflow": 0x10,
+}
+
+
+class LibraryError(RuntimeError):
+    """A non-OK status from the C ABI."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"paged_kv status {status}: {message}")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+c_vp, c_i32, c_i64, c_sz, c_f = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with `python -m paged_kv_cache_236_gb300.build` "
+                    "(there is no CPU fallback)")
+            L = ctypes.CDLL(LIB_PATH)
+            L.paged_kv_write.restype = c_i32
+            L.paged_kv_write.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i32, c_i32, c_i32,
+                                         c_i64, c_i64, c_i32, c_vp]
+            L.paged_attention_workspace_size.restype = c_sz
+            L.paged_attention_workspace_size.argtypes = [c_i32, c_i64, c_i32, c_i32, c_i32]
+            L.paged_attention_workspace_min.restype = c_sz
+            L.paged_attention_workspace_min.argtypes = [c_i32, c_i64, c_i32, c_i32, c_i32]
+            L.paged_attention_forward.restype = c_i32
+            L.paged_attention_forward.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i64, c_i32,
+                                                  c_i32, c_i32, c_i64, c_i32, c_i32, c_i32, c_f, c_i32, c_vp,
+                                                  c_sz, c_i32, c_vp]
+            L.pkv_last_error.restype = ctypes.c_char_p
+            L.pkv_last_error.argtypes = []
+            L.pkv_device_errors.restype = c_i32
+            L.pkv_device_errors.argtypes = [ctypes.POINTER(c_i32), c_i32]
+            L.pkv_set_profile_events.restype = None
+            L.pkv_set_profile_events.argtypes = [c_vp, c_vp]
+            L.pkv_event_elapsed_ms.restype = c_i32
+            L.pkv_event_elapsed_ms.argtypes = [c_vp, c_vp, ctypes.POINTER(c_f)]
+            L.pkv_version.restype = ctypes.c_char_p
+            L.pkv_version.argtypes = []
+            _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != PKV_OK:
+        raise LibraryError(status, lib().pkv_last_error().decode(errors="replace"))
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need_cuda(*tensors: torch.Tensor) -> torch.device:
+    dev = tensors[0].device
+    for t in tensors:
+        if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+            raise ValueError("all tensors must be CUDA tensors (no CPU path)")
+        if t.device != dev:
+            raise ValueError("all tensors must be on the same device")
+    return dev
+
+
+def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                   v_cache: torch.Tensor) -> None:
+    """Scatter ``k, v [T, Hkv, D]`` into ``k_cache, v_cache [NB, bs, Hkv, D]``
+    at ``slot_mapping [T]`` (int64; slot = block * bs + offset; < 0 skips)."""
+    dev = _need_cuda(k, v, slot_mapping, k_cache, v_cache)
+    if k_cache.dtype not in DTYPE or k.dtype != k_cache.dtype or v.dtype != k_cache.dtype or \
+            v_cache.dtype != k_cache.dtype:
+        raise ValueError("k, v, k_cache, v_cache must share dtype bfloat16 or float32")
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape or not k_cache.is_contiguous() or \
+            not v_cache.is_contiguous():
+        raise ValueError("caches must be contiguous [num_blocks, block_size, num_kv_heads, head_dim]")
+    NB, bs, Hkv, D = k_cache.shape
+    T = k.shape[0]
+    for name, t in (("k", k), ("v", v)):
+        if t.dim() != 3 or tuple(t.shape[1:]) != (Hkv, D) or t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError(f"{name} must be [T, {Hkv}, {D}] with contiguous heads")
+    if v.shape[0] != T or slot_mapping.shape != (T,) or slot_mapping.dtype != torch.int64 or \
+            not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous int64 [T]")
+    with torch.cuda.device(dev):
+        _check(lib().paged_kv_write(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), k_cache.data_ptr(),
+                                    v_cache.data_ptr(), T, NB, bs, Hkv, D, k.stride(0) if T else 0,
+                                    v.stride(0) if T else 0, DTYPE[k_cache.dtype], _stream(dev)))
+
+
+def workspace_size(num_seqs: int, num_tokens: int, num_q_heads: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(lib().paged_attention_workspace_size(num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim))
+
+
+def workspace_min(num_seqs: int, num_tokens: int, num_q_heads: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(lib().paged_attention_workspace_min(num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim))
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(dev: torch.device, nbytes: int) -> torch.Tensor:
+    key = (dev.index, torch.cuda.current_stream(dev).cuda_stream)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+        _ws_cache[key] = ws
+    return ws
+
+
+def paged_attention_forward(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor,
+                            query_start_loc: torch.Tensor, scale: float, causal: bool = True, *,
+                            out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                            max_query_len: int = 0) -> torch.Tensor:
+    """Varlen attention of ``q [T, Hq, D]`` through per-sequence block tables.
+
+    ``context_lens[s]`` counts sequence s's tokens after this step's write
+    (its query tokens included); query i of n sits at position L - n + i.
+    ``workspace`` (uint8, >= ``workspace_min``) defaults to a cached buffer
+    per (device, stream).  ``max_query_len`` is an optional host hint.
+    """
+    dev = _need_cuda(q, k_cache, v_cache, block_tables, context_lens, query_start_loc)
+    if q.dtype not in DTYPE or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise ValueError("q, k_cache, v_cache must share dtype bfloat16 or float32")
+    if q.dim() != 3 or not q.is_contiguous():
+        raise ValueError("q must be contiguous [T, Hq, D]")
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape or not k_cache.is_contiguous() or \
+            not v_cache.is_contiguous():
+        raise ValueError("caches must be contiguous [num_blocks, block_size, num_kv_heads, head_dim]")
+    T, Hq, D = q.shape
+    NB, bs, Hkv, Dk = k_cache.shape
+    if Dk != D:
+        raise ValueError("head_dim of q and the caches differ")
+    B = context_lens.shape[0]
+    for name, t, shape in (("block_tables", block_tables, None), ("context_lens", context_lens, (B,)),
+                           ("query_start_loc", query_start_loc, (B + 1,))):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous int32")
+        if shape is not None and tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or (B > 0 and block_tables.shape[1] == 0):
+        raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq] with max_blocks_per_seq > 0")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.device != dev:
+        raise ValueError("out must match q")
+    with torch.cuda.device(dev):
+        need = workspace_min(B, T, Hq, Hkv, D)
+        if workspace is None:
+            workspace = _workspace(dev, workspace_size(B, T, Hq, Hkv, D))
+        if workspace.dtype != torch.uint8 or workspace.device != dev or workspace.numel() < need:
+            raise ValueError(f"workspace must be a uint8 CUDA tensor of at least {need} bytes")
+        _check(lib().paged_attention_forward(
+            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+            context_lens.data_ptr(), query_start_loc.data_ptr(), out.data_ptr(), B, T, Hq, Hkv, D, NB, bs,
+            max(1, block_tables.shape[1]), int(max_query_len), float(scale), 1 if causal else 0,
+            workspace.data_ptr(), workspace.numel(), DTYPE[q.dtype], _stream(dev)))
+    return out
+
+
+def set_profile_events(start, stop) -> None:
+    """Record ``start``/``stop`` (torch.cuda.Event) around the attention
+    kernels of later forward calls on this thread; ``None, None`` stops."""
+    if start is None or stop is None:
+        lib().pkv_set_profile_events(None, None)
+    else:
+        lib().pkv_set_profile_events(start.cuda_event, stop.cuda_event)
+
+
+def profile_elapsed_ms(start, stop) -> float:
+    """Milliseconds between two events recorded through ``set_profile_events``."""
+    ms = c_f(0.0)
+    _check(lib().pkv_event_elapsed_ms(start.cuda_event, stop.cuda_event, ctypes.byref(ms)))
+    return float(ms.value)
+
+
+def device_errors(clear: bool = True) -> int:
+    """Sticky device error bits (``DEVERR``) of the current device; synchronises."""
+    flags = c_i32(0)
+    _check(lib().pkv_device_errors(ctypes.byref(flags), 1 if clear else 0))
+    return int(flags.value)

@@ -1,0 +1,395 @@
+// Host side of the C ABI declared in include/paged_kv.h: argument checks,
+// tensor-map encoding, workspace layout and the launch sequence
+//   planner -> tensor-core kernel (multi-token rows) -> CUDA-core kernel
+//   (decode-shaped rows) -> split merge
+// all on the caller's stream, with no host synchronisation.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <math.h>
+#include <mutex>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "paged_kv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+
+pkv_status fail(pkv_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Sticky device error word: one per device (a __device__ variable exists on
+// every device that loads this library).
+__device__ int g_device_error;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int major = 0, minor = 0;
+  int* err = nullptr;  // device address of g_device_error
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+pkv_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (!(d.major == 10 && d.minor == 3))
+      return fail(PKV_ERR_UNSUPPORTED, "this library is built for sm_103a; device %d is sm_%d%d", dev, d.major,
+                  d.minor);
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_device_error)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    d.err = static_cast<int*>(p);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return PKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(pkv_dtype dt) { return dt == PKV_DTYPE_BF16 ? 2 : 4; }
+
+// 4-D map of a block pool [NB, bs, Hkv, D] with a box of one block of one kv head.
+pkv_status encode_pool_map(CUtensorMap* map, const void* base, pkv_dtype dt, int64_t NB, int bs, int Hkv, int D,
+                           int box_d, CUtensorMapSwizzle swz) {
+  const int es = elem_bytes(dt);
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)bs, (cuuint64_t)NB};
+  cuuint64_t strides[3] = {(cuuint64_t)D * es, (cuuint64_t)Hkv * D * es, (cuuint64_t)bs * Hkv * D * es};
+  cuuint32_t box[4] = {(cuuint32_t)box_d, 1, (cuuint32_t)bs, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, dt == PKV_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                        4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (pool) failed: %d", (int)r);
+  return PKV_OK;
+}
+
+// 3-D map of q [T, Hq, D] with a box of {box_d, G heads, tokens}.
+pkv_status encode_q_map(CUtensorMap* map, const void* base, int64_t T, int Hq, int D, int box_d, int G, int tokens) {
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)(T > 0 ? T : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+  cuuint32_t box[3] = {(cuuint32_t)box_d, (cuuint32_t)G, (cuuint32_t)tokens};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed: %d", (int)r);
+  return PKV_OK;
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Item-count targets used for capacity sizing (device-independent upper
+// bounds of the per-device targets below).
+constexpr int kCapTargetDec = 4096;
+constexpr int kCapTargetMma = 2048;
+constexpr int kDefaultPartRows = 32768;
+
+}  // namespace
+
+namespace pkv {
+
+WorkspaceLayout workspace_layout(int B, int64_t T, int Hq, int Hkv, int D, size_t bytes_available, int /*num_sms*/,
+                                 bool want_default_parts) {
+  WorkspaceLayout L{};
+  const int G = Hq / Hkv;
+  const int64_t rows = T * (int64_t)G;
+  const int64_t dec_units = (int64_t)Hkv * ((rows + kDecRows - 1) / kDecRows + B);
+  const int64_t mma_units = (int64_t)Hkv * ((rows + kMmaRows - 1) / kMmaRows + B);
+  const int64_t dec_cap = kCapTargetDec + dec_units;
+  const int64_t mma_cap = kCapTargetMma + mma_units;
+  const int64_t merge_cap = dec_cap + mma_cap;
+  size_t off = 0;
+  L.header_off = off;
+  off = align_up(off + sizeof(PlanHeader));
+  L.dec_off = off;
+  off = align_up(off + (size_t)dec_cap * sizeof(WorkItem));
+  L.mma_off = off;
+  off = align_up(off + (size_t)mma_cap * sizeof(WorkItem));
+  L.merge_off = off;
+  off = align_up(off + (size_t)merge_cap * sizeof(MergeGroup));
+  const size_t fixed = off;
+  const size_t per_row = sizeof(float2) + (size_t)D * sizeof(float);
+  int64_t part_cap = 0;
+  if (want_default_parts) {
+    part_cap = kDefaultPartRows;
+  } else if (bytes_available > fixed + 2 * kAlign) {
+    part_cap = (int64_t)((bytes_available - fixed - 2 * kAlign) / per_row);
+    if (part_cap > (int64_t)1 << 30) part_cap = (int64_t)1 << 30;
+  }
+  L.ml_off = off;
+  off = align_up(off + (size_t)part_cap * sizeof(float2));
+  L.acc_off = off;
+  off = align_up(off + (size_t)part_cap * D * sizeof(float));
+  L.total = part_cap > 0 ? off : fixed;
+  L.dec_cap = (int)dec_cap;
+  L.mma_cap = (int)mma_cap;
+  L.merge_cap = (int)merge_cap;
+  L.part_cap = (int)part_cap;
+  return L;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_last_error(void) { return g_msg; }
+
+const char* pkv_version(void) { return "paged_kv 0.1.0 sm_103a"; }
+
+void pkv_set_profile_events(void* start, void* stop) {
+  g_prof_start = static_cast<cudaEvent_t>(start);
+  g_prof_stop = static_cast<cudaEvent_t>(stop);
+  if (!g_prof_start || !g_prof_stop) g_prof_start = g_prof_stop = nullptr;
+}
+
+pkv_status pkv_event_elapsed_ms(void* start, void* stop, float* ms) {
+  if (!start || !stop || !ms) return fail(PKV_ERR_INVALID_ARG, "null argument");
+  cudaError_t e = cudaEventElapsedTime(ms, static_cast<cudaEvent_t>(start), static_cast<cudaEvent_t>(stop));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+  return PKV_OK;
+}
+
+pkv_status pkv_device_errors(int32_t* flags, int32_t clear) {
+  if (!flags) return fail(PKV_ERR_INVALID_ARG, "flags is NULL");
+  DeviceInfo* d = nullptr;
+  pkv_status st = device_info(&d);
+  if (st != PKV_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  int v = 0;
+  if ((e = cudaMemcpy(&v, d->err, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "read device error word");
+  if (clear) {
+    const int z = 0;
+    if ((e = cudaMemcpy(d->err, &z, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "clear device error word");
+  }
+  *flags = v;
+  return PKV_OK;
+}
+
+pkv_status paged_kv_write(const void* k, const void* v, const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                          int64_t num_tokens, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                          int32_t head_dim, int64_t k_token_stride, int64_t v_token_stride, pkv_dtype dtype,
+                          void* stream) {
+  g_msg[0] = 0;
+  if (dtype != PKV_DTYPE_BF16 && dtype != PKV_DTYPE_F32) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", (int)dtype);
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "sizes must be positive (num_tokens >= 0)");
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  if (row > (1 << 24)) return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads * head_dim too large");
+  if (k_token_stride == 0) k_token_stride = row;
+  if (v_token_stride == 0) v_token_stride = row;
+  if (k_token_stride < row || v_token_stride < row)
+    return fail(PKV_ERR_INVALID_ARG, "token stride smaller than num_kv_heads * head_dim");
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return fail(PKV_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+  DeviceInfo* d = nullptr;
+  pkv_status st = device_info(&d);
+  if (st != PKV_OK) return st;
+  cudaError_t e = launch_kv_write(k, v, slot_mapping, k_cache, v_cache, num_tokens, num_blocks * block_size,
+                                  (int)row, elem_bytes(dtype), k_token_stride, v_token_stride, d->err,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "paged_kv_write launch");
+  return PKV_OK;
+}
+
+size_t paged_attention_workspace_size(int32_t num_seqs, int64_t num_tokens, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim) {
+  if (num_seqs < 0 || num_tokens < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+  return workspace_layout(num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, 0, 0, true).total;
+}
+
+size_t paged_attention_workspace_min(int32_t num_seqs, int64_t num_tokens, int32_t num_q_heads,
+                                     int32_t num_kv_heads, int32_t head_dim) {
+  if (num_seqs < 0 || num_tokens < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+  return workspace_layout(num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, 0, 0, false).total;
+}
+
+pkv_status paged_attention_forward(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, const int32_t* context_lens,
+                                   const int32_t* query_start_loc, void* out, int32_t num_seqs, int64_t num_tokens,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                                   int32_t block_size, int32_t max_blocks_per_seq, int32_t max_query_len,
+                                   float scale, int32_t causal, void* workspace, size_t workspace_bytes,
+                                   pkv_dtype dtype, void* stream) {
+  g_msg[0] = 0;
+  const int B = num_seqs, Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim, bs = block_size;
+  const int64_t T = num_tokens;
+  if (dtype != PKV_DTYPE_BF16 && dtype != PKV_DTYPE_F32) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", (int)dtype);
+  if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_blocks <= 0 || bs <= 0 || max_blocks_per_seq <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "sizes must be positive (num_seqs, num_tokens >= 0)");
+  if (Hq % Hkv != 0) return fail(PKV_ERR_INVALID_ARG, "num_q_heads (%d) %% num_kv_heads (%d) != 0", Hq, Hkv);
+  if (Hq / Hkv > 128) return fail(PKV_ERR_UNSUPPORTED, "more than 128 q heads per kv head");
+  if (D != 64 && D != 128) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", D);
+  if (bs != 8 && bs != 16 && bs != 32 && bs != 64)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32, 64)", bs);
+  if (!(scale > 0.f) || !isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale must be positive and finite");
+  if ((int64_t)max_blocks_per_seq * bs > (int64_t)1 << 30) return fail(PKV_ERR_UNSUPPORTED, "context too long");
+  if (T > ((int64_t)1 << 31) / ((int64_t)Hq * D)) return fail(PKV_ERR_UNSUPPORTED, "num_tokens too large");
+  if (B == 0 || T == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start_loc || !out)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PKV_ERR_INVALID_ARG, "q, out and the caches must be 16-byte aligned");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+    return fail(PKV_ERR_WORKSPACE, "workspace missing or not 256-byte aligned");
+  const WorkspaceLayout lay = workspace_layout(B, T, Hq, Hkv, D, workspace_bytes, 0, false);
+  if (workspace_bytes < lay.total)
+    return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < minimum %zu", workspace_bytes, lay.total);
+
+  DeviceInfo* dev = nullptr;
+  pkv_status st = device_info(&dev);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool bf16 = dtype == PKV_DTYPE_BF16;
+  const int G = Hq / Hkv;
+
+  int dec_ctas = 1;
+  cudaError_t e = decode_ctas_per_sm(bf16, D, &dec_ctas);
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel set-up");
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  PlanHeader* header = reinterpret_cast<PlanHeader*>(ws + lay.header_off);
+  WorkItem* dec_items = reinterpret_cast<WorkItem*>(ws + lay.dec_off);
+  WorkItem* mma_items = reinterpret_cast<WorkItem*>(ws + lay.mma_off);
+  MergeGroup* merges = reinterpret_cast<MergeGroup*>(ws + lay.merge_off);
+  float2* part_ml = reinterpret_cast<float2*>(ws + lay.ml_off);
+  float* part_acc = reinterpret_cast<float*>(ws + lay.acc_off);
+
+  // tensor-core path: bf16, head_dim 128, G a power of two (a 128-row tile is
+  // 128/G whole tokens)
+  const bool mma_ok = bf16 && D == 128 && (G & (G - 1)) == 0 && G <= 128;
+  // with a host hint that no sequence has more than kDecRows rows, skip the launch
+  const bool mma_launch = mma_ok && !(max_query_len > 0 && (int64_t)max_query_len * G <= kDecRows);
+  const int dec_grid = dev->sms * dec_ctas;
+
+  PlanParams pp{};
+  pp.context_lens = context_lens;
+  pp.query_start_loc = query_start_loc;
+  pp.B = B;
+  pp.T = T;
+  pp.G = G;
+  pp.Hkv = Hkv;
+  pp.bs = bs;
+  pp.max_blocks = max_blocks_per_seq;
+  pp.causal = causal ? 1 : 0;
+  pp.mma_ok = mma_launch ? 1 : 0;
+  pp.dec_rows_max = kDecRows;
+  pp.target_dec = dec_grid * 4;
+  pp.target_mma = dev->sms * 4;
+  pp.min_chunk_dec = 256;
+  pp.min_chunk_mma = 512;
+  pp.dec_cap = lay.dec_cap;
+  pp.mma_cap = lay.mma_cap;
+  pp.merge_cap = lay.merge_cap;
+  pp.part_cap = lay.part_cap;
+  pp.header = header;
+  pp.dec_items = dec_items;
+  pp.mma_items = mma_items;
+  pp.merges = merges;
+  pp.out = out;
+  pp.out_row_bytes = Hq * D * elem_bytes(dtype);
+  pp.err = dev->err;
+  if ((e = launch_planner(pp, s)) != cudaSuccess) return cuda_fail(e, "planner launch");
+
+  CUtensorMap kmap, vmap;
+  if ((st = encode_pool_map(&kmap, k_cache, dtype, num_blocks, bs, Hkv, D, D, CU_TENSOR_MAP_SWIZZLE_NONE)) != PKV_OK)
+    return st;
+  if ((st = encode_pool_map(&vmap, v_cache, dtype, num_blocks, bs, Hkv, D, D, CU_TENSOR_MAP_SWIZZLE_NONE)) != PKV_OK)
+    return st;
+
+  AttnParams ap{};
+  ap.q = q;
+  ap.out = out;
+  ap.block_tables = block_tables;
+  ap.context_lens = context_lens;
+  ap.query_start_loc = query_start_loc;
+  ap.header = header;
+  ap.part_ml = part_ml;
+  ap.part_acc = part_acc;
+  ap.Hq = Hq;
+  ap.Hkv = Hkv;
+  ap.G = G;
+  ap.D = D;
+  ap.bs = bs;
+  ap.max_blocks = max_blocks_per_seq;
+  ap.num_blocks = num_blocks;
+  ap.scale_log2 = scale * 1.4426950408889634f;
+  ap.causal = causal ? 1 : 0;
+  ap.err = dev->err;
+
+  if (g_prof_start && (e = cudaEventRecord(g_prof_start, s)) != cudaSuccess) return cuda_fail(e, "profile event");
+  if (mma_launch) {
+    CUtensorMap qmap, kmap_sw, vmap_sw;
+    if ((st = encode_q_map(&qmap, q, T, Hq, D, 64, G, kMmaRows / G)) != PKV_OK) return st;
+    if ((st = encode_pool_map(&kmap_sw, k_cache, dtype, num_blocks, bs, Hkv, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        PKV_OK)
+      return st;
+    if ((st = encode_pool_map(&vmap_sw, v_cache, dtype, num_blocks, bs, Hkv, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        PKV_OK)
+      return st;
+    ap.counter = &header->mma_counter;
+    ap.items = mma_items;
+    if ((e = launch_mma(ap, qmap, kmap_sw, vmap_sw, dev->sms, s)) != cudaSuccess) return cuda_fail(e, "mma launch");
+  }
+  ap.counter = &header->dec_counter;
+  ap.items = dec_items;
+  if ((e = launch_decode(ap, kmap, vmap, bf16, dec_grid, s)) != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (g_prof_stop && (e = cudaEventRecord(g_prof_stop, s)) != cudaSuccess) return cuda_fail(e, "profile event");
+
+  MergeParams mp{};
+  mp.out = out;
+  mp.query_start_loc = query_start_loc;
+  mp.header = header;
+  mp.groups = merges;
+  mp.part_ml = part_ml;
+  mp.part_acc = part_acc;
+  mp.Hq = Hq;
+  mp.G = G;
+  mp.D = D;
+  if ((e = launch_merge(mp, bf16, dev->sms * 4, s)) != cudaSuccess) return cuda_fail(e, "merge launch");
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,126 @@
+// Host/device shared declarations: the work plan written to the workspace by
+// the planner kernel and read by the attention kernels, and the launch
+// functions each translation unit exports to the host API.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// Rows of one kv head of one sequence are (query token i, head-in-group g)
+// pairs, row = i * G + g.
+constexpr int kDecRows = 4;      // rows per CUDA-core work item
+constexpr int kDecTileKeys = 64;  // keys per CUDA-core pipeline stage
+constexpr int kMmaRows = 128;     // rows per tensor-core work item (M of the MMA)
+constexpr int kMmaTileKeys = 128;  // keys per tensor-core pipeline stage
+constexpr int kMaxSplits = 64;
+
+struct alignas(16) PlanHeader {
+  int n_dec;        // CUDA-core work items
+  int n_mma;        // tensor-core work items
+  int n_merge;      // merge groups
+  int chunk_dec;    // keys per split (CUDA-core path)
+  int chunk_mma;    // keys per split (tensor-core path)
+  int part_rows;    // partial rows used
+  int dec_counter;  // work counters (dynamic item fetch), zeroed by the planner
+  int mma_counter;
+  int merge_counter;
+  int pad[7];
+};
+
+// One unit of attention work: `nrows` rows of sequence `seq`, kv head `kvh`,
+// starting at row `row0`, over keys [kb, ke).  part < 0: normalise and write
+// the output rows; otherwise write partial (m, l, acc) rows part .. part+nrows-1.
+struct alignas(16) WorkItem {
+  int seq, kvh, row0, nrows;
+  int kb, ke, part, pad;
+};
+
+// Split-KV merge: rows row0 .. row0+nrows-1 of (seq, kvh) have nsplit
+// partial states at part_base + p * nrows + r.
+struct alignas(16) MergeGroup {
+  int seq, kvh, row0, nrows;
+  int nsplit, part_base, pad0, pad1;
+};
+
+struct WorkspaceLayout {
+  size_t header_off, dec_off, mma_off, merge_off, ml_off, acc_off, total;
+  int dec_cap, mma_cap, merge_cap, part_cap;
+};
+
+// Capacity arithmetic shared by the size queries and the forward call.
+WorkspaceLayout workspace_layout(int B, int64_t T, int Hq, int Hkv, int D, size_t bytes_available,
+                                 int num_sms, bool want_default_parts);
+
+struct PlanParams {
+  const int32_t* context_lens;
+  const int32_t* query_start_loc;
+  int B;
+  int64_t T;
+  int G;            // q heads per kv head
+  int Hkv;
+  int bs;
+  int max_blocks;   // block table row length
+  int causal;
+  int mma_ok;       // tensor-core path available for this call
+  int dec_rows_max;  // rows <= this go to the CUDA-core path when mma_ok
+  int target_dec, target_mma;  // desired item counts
+  int min_chunk_dec, min_chunk_mma;
+  int dec_cap, mma_cap, merge_cap, part_cap;
+  PlanHeader* header;
+  WorkItem* dec_items;
+  WorkItem* mma_items;
+  MergeGroup* merges;
+  void* out;        // rows of invalid sequences are zeroed
+  int out_row_bytes;  // bytes of one token's output row (Hq * D * elem)
+  int* err;
+};
+
+struct AttnParams {
+  const void* q;
+  void* out;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start_loc;
+  const PlanHeader* header;
+  int* counter;
+  const WorkItem* items;
+  float2* part_ml;   // (m, l) per partial row, m in log2 units
+  float* part_acc;   // [part_rows][D]
+  int Hq, Hkv, G, D, bs, max_blocks;
+  int64_t num_blocks;
+  float scale_log2;  // scale * log2(e)
+  int causal;
+  int* err;
+};
+
+struct MergeParams {
+  void* out;
+  const int32_t* query_start_loc;
+  const PlanHeader* header;
+  const MergeGroup* groups;
+  const float2* part_ml;
+  const float* part_acc;
+  int Hq, G, D;
+};
+
+// launchers (return cudaGetLastError after the launch)
+cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slots, void* kc, void* vc,
+                            int64_t T, int64_t num_slots, int row_elems, int elem_bytes,
+                            int64_t k_stride, int64_t v_stride, int* err, cudaStream_t s);
+cudaError_t launch_planner(const PlanParams& p, cudaStream_t s);
+cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          bool bf16, int grid, cudaStream_t s);
+cudaError_t launch_merge(const MergeParams& p, bool bf16, int grid, cudaStream_t s);
+cudaError_t launch_mma(const AttnParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                       const CUtensorMap& vmap, int grid, cudaStream_t s);
+
+// Shared-memory bytes of the CUDA-core kernel, and its resident CTAs per SM
+// (also sets the kernel's shared-memory opt-in on the current device).
+int decode_smem_bytes(int D, int elem_bytes);
+cudaError_t decode_ctas_per_sm(bool bf16, int D, int* ctas);
+
+}  // namespace pkv

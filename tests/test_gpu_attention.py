@@ -1,0 +1,158 @@
+"""paged_attention_forward on the GPU against the fp64 oracle: the pages'
+worked example (tiny fp32 config), ragged random batches over the supported
+shapes, edge cases and invalid metadata."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_236_gb300 as pkv
+import workloads as wl
+from gpu_util import DeviceWorkload, check_step, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("case", ["1", "1b"])
+def test_tiny_worked_example(case):
+    """Block tables [7, 3] and [7, 9, 12] sharing block 7; an 8-token causal
+    chunk, then (case 1) a 1-token decode into freshly allocated blocks."""
+    dw = DeviceWorkload(wl.tiny(case, poison=True))
+    for i in range(len(dw.w.steps)):
+        out = dw.run_step(i)
+        check_step(dw, out, i, what=f"tiny-{case} step {i}")
+    assert pkv.device_errors() == 0
+
+
+CASES = []
+for dtype in ("bf16", "f32"):
+    for D in (64, 128):
+        for bs in (8, 16, 32, 64):
+            for (hq, hkv) in ((8, 2), (4, 4), (8, 1), (16, 2)):
+                CASES.append((dtype, D, bs, hq, hkv))
+
+
+@pytest.mark.parametrize("dtype,D,bs,hq,hkv", CASES)
+def test_random_batches(dtype, D, bs, hq, hkv):
+    seed = 500 + CASES.index((dtype, D, bs, hq, hkv))
+    w = wl.random_small(seed, dtype=dtype, batch=5, max_ctx=300, max_q=12, num_q_heads=hq, num_kv_heads=hkv,
+                        head_dim=D, block_size=bs, poison=True)
+    dw = DeviceWorkload(w)
+    out = dw.run_step(0)
+    check_step(dw, out, what=f"{dtype} D{D} bs{bs} {hq}/{hkv}")
+    assert pkv.device_errors() == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_non_causal(dtype):
+    w = wl.random_small(77, dtype=dtype, batch=4, max_ctx=150, max_q=9, causal=False)
+    dw = DeviceWorkload(w)
+    check_step(dw, dw.run_step(0), what="non-causal")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_prefill_chunks_multi_tile(dtype):
+    """Longer causal chunks spanning many 128-row and 128-key tiles with a
+    ragged tail."""
+    w = wl.build("chunks", context_lens=[700, 333, 129, 1000], q_lens=[300, 333, 17, 1], num_blocks=200,
+                 block_size=16, num_q_heads=8, num_kv_heads=2, head_dim=128, dtype=dtype, seed=31, poison=True)
+    dw = DeviceWorkload(w)
+    check_step(dw, dw.run_step(0), what="chunks")
+
+
+def test_edge_cases_empty_and_single():
+    """Sequences with no queries, a single-token context, contexts ending
+    exactly on a block boundary, and a batch that is entirely empty."""
+    w = wl.build("edges", context_lens=[1, 16, 17, 32, 5, 64], q_lens=[1, 0, 3, 1, 0, 16], num_blocks=40,
+                 block_size=16, num_q_heads=8, num_kv_heads=2, head_dim=128, dtype="bf16", seed=3, poison=True)
+    dw = DeviceWorkload(w)
+    check_step(dw, dw.run_step(0), what="edges")
+    # T == 0: nothing to do, must not fail
+    q = torch.empty(0, 8, 128, dtype=torch.bfloat16, device="cuda")
+    out = pkv.paged_attention_forward(q, dw.kc, dw.vc, torch.zeros(2, 1, dtype=torch.int32, device="cuda"),
+                                      torch.zeros(2, dtype=torch.int32, device="cuda"),
+                                      torch.zeros(3, dtype=torch.int32, device="cuda"), 0.1, True)
+    assert out.shape == (0, 8, 128)
+    assert pkv.device_errors() == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_long_context_split_kv(dtype):
+    """One decode token over 20000 keys and a few short ones: the long one is
+    split across many CTAs and merged; a minimum workspace (no room for
+    partial rows, so no splits) gives the same rows within tolerance."""
+    w = wl.build("long", context_lens=[20000, 100, 3000], q_lens=[1, 1, 2], num_blocks=1600, block_size=16,
+                 num_q_heads=8, num_kv_heads=2, head_dim=128, dtype=dtype, seed=8, poison=True)
+    dw = DeviceWorkload(w)
+    out = dw.run_step(0)
+    check_step(dw, out, what="split")
+    st = w.step
+    t = dw.step_tensors(st)
+    ws = torch.empty(pkv.workspace_min(3, st.num_tokens, 8, 2, 128), dtype=torch.uint8, device="cuda")
+    out2 = pkv.paged_attention_forward(t["q"], dw.kc, dw.vc, t["bt"], t["ctx"], t["qsl"], w.scale, True,
+                                       workspace=ws)
+    check_step(dw, out2, what="no-split")
+
+
+def test_block_permutation_is_bit_identical():
+    """Relabelling physical blocks (moving pool rows accordingly) changes no
+    output bit: the kernels reduce in logical order."""
+    w = wl.random_small(12, dtype="bf16", batch=6, max_ctx=400, max_q=10, poison=True)
+    dw = DeviceWorkload(w)
+    out = dw.run_step(0)
+    perm = np.random.Generator(np.random.PCG64(4)).permutation(w.num_blocks)
+    kc = torch.empty_like(dw.kc)
+    vc = torch.empty_like(dw.vc)
+    pt = torch.from_numpy(perm).cuda()
+    kc[pt] = dw.kc
+    vc[pt] = dw.vc
+    st = w.step
+    bt = np.where(st.block_tables >= 0, perm[np.maximum(st.block_tables, 0)], -1).astype(np.int32)
+    t = dw.step_tensors(st)
+    out2 = pkv.paged_attention_forward(t["q"], kc, vc, torch.from_numpy(bt).cuda(), t["ctx"], t["qsl"], w.scale,
+                                       True)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+def test_invalid_metadata_is_flagged_and_zeroed():
+    """A sequence with more queries than tokens and one whose table names a
+    block outside the pool: no fault, the first's rows are zero, both raise
+    device error bits, the valid sequence is still right."""
+    w = wl.build("bad", context_lens=[40, 30, 50], q_lens=[2, 1, 1], num_blocks=12, block_size=16,
+                 num_q_heads=4, num_kv_heads=2, head_dim=128, dtype="bf16", seed=2, poison=False)
+    dw = DeviceWorkload(w)
+    st = w.step
+    t = dw.step_tensors(st)
+    pkv.paged_kv_write(t["k"], t["v"], t["slots"], dw.kc, dw.vc)
+    ctx = t["ctx"].clone()
+    ctx[0] = 1                       # 2 queries but 1 token
+    bt = t["bt"].clone()
+    bt[1, 1] = 10_000                # outside the pool
+    pkv.device_errors(clear=True)
+    out = pkv.paged_attention_forward(t["q"], dw.kc, dw.vc, bt, ctx, t["qsl"], w.scale, True)
+    flags = pkv.device_errors(clear=True)
+    assert flags & pkv.DEVERR["bad_sequence"] and flags & pkv.DEVERR["block_out_of_range"]
+    o = to_f64(out)
+    assert np.all(o[0:2] == 0)
+    assert np.all(np.isfinite(o))
+    from oracle import paged_oracle as po
+    po.kv_write(st.k_new, st.v_new, st.slot_mapping, dw.kc_host, dw.vc_host)
+    rows = dw.oracle_rows(0, [2])
+    a, b, ref = rows[2]
+    from gpu_util import check_close
+    check_close(o[a:b], ref, "bf16", "valid sequence next to bad ones")
+
+
+def test_host_side_errors():
+    q = torch.zeros(4, 6, 128, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(4, 16, 4, 128, dtype=torch.bfloat16, device="cuda")
+    i32 = lambda *s: torch.zeros(*s, dtype=torch.int32, device="cuda")
+    with pytest.raises(pkv.LibraryError) as e:
+        pkv.paged_attention_forward(q, kc, kc, i32(1, 1), i32(1), i32(2), 0.1, True)
+    assert "num_kv_heads" in str(e.value)
+    q = torch.zeros(4, 8, 96, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(4, 16, 4, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pkv.LibraryError) as e:
+        pkv.paged_attention_forward(q, kc, kc, i32(1, 1), i32(1), i32(2), 0.1, True)
+    assert e.value.status == 2
+    with pytest.raises(ValueError):
+        pkv.paged_attention_forward(q.cpu(), kc, kc, i32(1, 1), i32(1), i32(2), 0.1, True)
