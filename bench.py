@@ -36,6 +36,21 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged-attn decode KV GB/s (% HBM peak); mixed-batch query tokens/s"
+BASE_SEED = {"decode": 1002, "mixed": 1003, "prefill": 1003, "specverify": 1004, "prefix": 1005, "prefix-long": 1006}
+WORKLOAD_DESC = {
+    "decode": "decode batch: 64 seqs, context U[512,4096], 1 query token, 32q/8kv heads, head_dim 128, "
+              "block_size 16, 20000-block pool, random block permutation, bf16",
+    "mixed": "mixed continuous batch: 8 prefill chunks of 512 tokens on U[0,2048] cached + 120 decodes with "
+             "context U[256,8192], 32q/8kv heads, head_dim 128, block_size 16, 80000-block pool, bf16",
+    "prefill": "the mixed batch's 8 prefill chunks alone (512 tokens on U[0,2048] cached), 32q/8kv, head_dim 128, "
+               "block_size 16, bf16",
+    "specverify": "speculative verify: 32 seqs x 5 query tokens on 8192-token contexts, 64q/8kv heads, head_dim "
+                  "128, block_size 32, 10240-block pool, bf16",
+    "prefix": "prefix-shared decode: 256 seqs sharing a 2048-token prefix (128 blocks) + private U[128,1024] "
+              "suffixes, 1 query token, 32q/8kv, head_dim 128, block_size 16, bf16",
+    "prefix-long": "long-context prefix-shared decode: 4 seqs x 131072 tokens (2048 shared), 1 query token, "
+                   "32q/8kv, head_dim 128, block_size 16, bf16",
+}
 
 
 def _peaks():
@@ -75,6 +90,12 @@ def mma_flops(w) -> float:
         pairs = sum(L - n + i + 1 for i in range(n)) if w.causal else n * L
         tot += 4.0 * w.head_dim * w.num_q_heads * pairs
     return tot
+
+
+def launches_per_step(w, max_q_len: int) -> int:
+    """Our kernels per step: write, planner, [tensor-core kernel], CUDA-core kernel, merge."""
+    g = w.num_q_heads // w.num_kv_heads
+    return 4 + (1 if max_q_len * g > 4 else 0)
 
 
 class ClockSampler:
@@ -196,8 +217,8 @@ def run_gpu(args, rank, world, local_rank):
         kern_ms = [pkv.profile_elapsed_ms(c, d) for _, _, c, d in ev]
         return step_ms, kern_ms, out
 
-    # ---------------- headline: decode batch ----------------
-    w = wl.decode_batch(seed=1002 + rank)
+    # ---------------- headline workload ----------------
+    w = wl.CONFIGS[args.workload](seed=BASE_SEED[args.workload] + rank)
     t = prepare(w)
     sampler = ClockSampler(_gpu_id(torch, dev))
     time.sleep(0.3)
@@ -214,7 +235,21 @@ def run_gpu(args, rank, world, local_rank):
         tot_ms = float(tt.item())
     value = ab["step"] * args.steps * world / (tot_ms * 1e-3) / 1e9
     kern_avg_ms = sum(kern_ms) / len(kern_ms)
-    achieved = ab["attn_kernel"] / (kern_avg_ms * 1e-3) / 1e9
+    if args.workload == "prefill":
+        fl = mma_flops(w)
+        achieved = fl / (kern_avg_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "mma_attn_kernel (tcgen05, per launch)", "achieved": round(achieved, 1),
+                "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(achieved / bf16_peak, 4),
+                "peak_kind": peak_kind + " bf16 dense (burst)", "traffic": None,
+                "kernel_ms": round(kern_avg_ms, 5), "algorithmic_flops_per_launch": fl}
+    else:
+        achieved = ab["attn_kernel"] / (kern_avg_ms * 1e-3) / 1e9
+        kname = "mma_attn_kernel (tcgen05)" if args.workload == "specverify" else (
+            "mma_attn_kernel + decode_kernel" if args.workload == "mixed" else "decode_kernel")
+        roof = {"bound": "hbm", "kernel": kname + ", attention kernels per launch", "achieved": round(achieved, 1),
+                "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                "peak_kind": peak_kind + " HBM copy", "traffic": None, "kernel_ms": round(kern_avg_ms, 5),
+                "algorithmic_bytes_per_launch": ab["attn_kernel"]}
 
     # ---------------- e2e through the public API, host buffers ----------------
     st = w.step
@@ -235,7 +270,7 @@ def run_gpu(args, rank, world, local_rank):
         d = {k2: x.to(dev, non_blocking=True) for k2, x in host_in.items()}
         pkv.paged_kv_write(d["k"], d["v"], d["slots"], t["kc"], t["vc"])
         o = pkv.paged_attention_forward(d["q"], t["kc"], t["vc"], d["bt"], d["ctx"], d["qsl"], w.scale, w.causal,
-                                        workspace=ws, max_query_len=1)
+                                        workspace=ws, max_query_len=t["mql"])
         host_out.copy_(o, non_blocking=True)
         b.record()
         b.synchronize()
@@ -252,26 +287,22 @@ def run_gpu(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(tot_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "decode batch: 64 seqs, context U[512,4096], 1 query token, 32q/8kv heads, "
-                               "head_dim 128, block_size 16, 20000-block pool, random block permutation, bf16; "
-                               "step = paged_kv_write + paged_attention_forward",
+        "config": {"workload": WORKLOAD_DESC[args.workload],
+                   "step": "paged_kv_write of the batch's new K/V rows + paged_attention_forward",
                    "l2": "flushed between steps (512 MB write outside the timed events)",
-                   "bytes_per_step": ab["step"], "kv_bytes": ab["kv"],
+                   "bytes_per_step": ab["step"], "kv_bytes": ab["kv"], "query_tokens": w.step.num_tokens,
                    "parallelism": f"replicas x{world}"},
+        "query_tokens_per_s": round(w.step.num_tokens * args.steps * world / (tot_ms * 1e-3), 1),
         "hbm_frac": round(value / hbm_peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel (attention kernels, per launch)",
-                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
-                     "traffic": None, "kernel_ms": round(kern_avg_ms, 5),
-                     "algorithmic_bytes_per_launch": ab["attn_kernel"]},
+        "roofline": roof,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_tot / args.steps, 5)},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": launches_per_step(w, t["mql"]) * args.steps,
         "clocks": clocks,
     }
 
     # ---------------- mixed continuous batch (query tokens/s) ----------------
-    if args.mixed:
+    if args.mixed and args.workload != "mixed":
         wm = wl.mixed_batch(seed=1003 + rank)
         tm = prepare(wm)
         ms_m, kern_m, _ = timed(wm, tm, max(3, args.steps // 2), args.warmup)
@@ -283,7 +314,7 @@ def run_gpu(args, rank, world, local_rank):
             "bytes_per_step": algorithmic_bytes(wm)["step"],
             "hbm_frac": round(algorithmic_bytes(wm)["step"] / (avg * 1e-3) / 1e9 / hbm_peak, 4),
             "prefill_unmasked_tflop": round(fl / 1e12, 4)}
-        result["gpu_launches"] += 4 * len(ms_m)
+        result["gpu_launches"] += launches_per_step(wm, tm["mql"]) * len(ms_m)
         del tm
 
     if rank == 0 and not args.no_cpu_baseline:
@@ -315,27 +346,31 @@ def cpu_baseline(w, budget_s: float = 15.0) -> dict:
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0))
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"first {done} of {st.num_seqs} sequences of the decode batch (gather + fp64 attention, "
+            "sample": f"first {done} of {st.num_seqs} sequences of {w.name} (gather + fp64 attention, "
                       f"numpy BLAS threads default), {dt:.1f} s"}
 
 
 def run_reference(args):
-    """The oracle as the reference arm: each step one bounded sample (the
-    oracle on sequences of the decode batch for ~budget seconds)."""
+    """The oracle as the reference arm: each step one bounded sample of the
+    same workload (the oracle on its sequences for about a budget's worth of
+    seconds), timed on the host cores."""
     import workloads as wl
-    w = wl.decode_batch()
-    vals = []
+    w = wl.CONFIGS[args.workload](seed=BASE_SEED[args.workload])
+    vals, secs = [], []
     for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
         r = cpu_baseline(w, budget_s=max(1.0, args.cpu_seconds / max(1, args.steps)))
         if i >= args.warmup:
             vals.append(r)
-    value = statistics.median(v["value"] for v in vals)
+            secs.append(time.perf_counter() - t0)
+    value = round(statistics.median(v["value"] for v in vals), 4)
     cb = dict(vals[-1], value=value)
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "decode batch: 64 seqs, context U[512,4096], 1 query token, 32q/8kv heads, "
-                                   "head_dim 128, block_size 16, bf16 inputs widened to fp64 by the oracle"},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.median(secs), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC[args.workload] + "; bf16 inputs widened to fp64 by the oracle",
+                       "step": "the fp64 oracle (gather through block tables + masked softmax attention) on a "
+                               "bounded sample of the batch's sequences"},
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -346,6 +381,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(BASE_SEED), default="decode")
     ap.add_argument("--no-mixed", dest="mixed", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

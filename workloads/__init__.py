@@ -376,6 +376,17 @@ def mixed_batch(poison: bool = False, seed: int = 1003) -> Workload:
                  poison=poison, max_blocks_per_seq=512)
 
 
+def prefill_chunks(poison: bool = False, seed: int = 1003) -> Workload:
+    """The mixed batch's 8 prefill chunks alone (512 new tokens on U[0, 2048]
+    cached tokens each, the same draw as the mixed batch): the compute-bound
+    part of multi-token attention.  32 q / 8 kv heads, head_dim 128, bs 16."""
+    g = np.random.Generator(np.random.PCG64(seed + 7_000_000))
+    cached = g.integers(0, 2048, size=8, endpoint=True)
+    return build("prefill-8x512", context_lens=cached + 512, q_lens=np.full(8, 512), num_blocks=2048,
+                 block_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128, dtype="bf16", seed=seed,
+                 poison=poison, max_blocks_per_seq=512)
+
+
 def spec_verify(poison: bool = False, seed: int = 1004) -> Workload:
     """Speculative verification, bf16: 32 sequences of 8192 tokens whose last
     5 are draft tokens (causal among themselves); 64 q / 8 kv heads, head_dim
@@ -432,6 +443,7 @@ CONFIGS = {
     "decode": decode_batch,
     "mixed": mixed_batch,
     "specverify": spec_verify,
+    "prefill": prefill_chunks,
     "prefix": prefix_shared,
     "prefix-long": prefix_shared_long,
 }
