@@ -154,6 +154,39 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
                                    void* workspace, size_t workspace_bytes, pkv_dtype dtype,
                                    void* stream);
 
+/*
+ * paged_attention_forward_static_ws - paged_attention_forward for callers
+ * that cannot allocate device memory (no counterpart on the source pages).
+ *
+ * Same arguments and results as paged_attention_forward, without the
+ * workspace: the scratch is a static array compiled into the library
+ * (paged_attention_static_workspace_bytes(), 8 MiB), present on every GPU that
+ * loads the library until the process exits.  Meant for code that runs under
+ * an allocator which forbids new device allocations once started, or that
+ * can only pass through buffers someone else registered.  The call allocates
+ * nothing (no cudaMalloc / cudaFree, no allocating library routine).
+ *   - A batch whose paged_attention_workspace_min exceeds the static size is
+ *     rejected with PKV_ERR_WORKSPACE before any launch.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device uses the same array, which keeps the last call's
+ *     contents (each call rewrites what it reads).  Calls whose GPU work can
+ *     overlap (other streams, unordered host threads) race on it: serialise
+ *     them.
+ */
+pkv_status paged_attention_forward_static_ws(const void* q, const void* k_cache, const void* v_cache,
+                                             const int32_t* block_tables, const int32_t* context_lens,
+                                             const int32_t* query_start_loc, void* out,
+                                             int32_t num_seqs, int64_t num_tokens, int32_t num_q_heads,
+                                             int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                                             int32_t block_size, int32_t max_blocks_per_seq,
+                                             int32_t max_query_len, float scale, int32_t causal,
+                                             pkv_dtype dtype, void* stream);
+
+/* Bytes of the static scratch used by paged_attention_forward_static_ws. */
+size_t paged_attention_static_workspace_bytes(void);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* pkv_last_error(void);
 

@@ -125,6 +125,8 @@ constexpr int kDefaultPartRows = 32768;
 
 namespace pkv {
 
+void set_last_error(const char* msg) { snprintf(g_msg, sizeof(g_msg), "%s", msg); }
+
 WorkspaceLayout workspace_layout(int B, int64_t T, int Hq, int Hkv, int D, size_t bytes_available, int /*num_sms*/,
                                  bool want_default_parts) {
   WorkspaceLayout L{};

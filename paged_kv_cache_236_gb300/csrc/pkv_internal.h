@@ -118,6 +118,9 @@ cudaError_t launch_merge(const MergeParams& p, bool bf16, int grid, cudaStream_t
 cudaError_t launch_mma(const AttnParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
                        const CUtensorMap& vmap, int grid, cudaStream_t s);
 
+// Sets the thread-local message pkv_last_error returns.
+void set_last_error(const char* msg);
+
 // Shared-memory bytes of the CUDA-core kernel, and its resident CTAs per SM
 // (also sets the kernel's shared-memory opt-in on the current device).
 int decode_smem_bytes(int D, int elem_bytes);
