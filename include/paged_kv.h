@@ -79,6 +79,7 @@ typedef enum {
 #define PKV_DEVERR_BAD_SEQUENCE 0x4        /* q_len < 0, q_len > context_len, context too long */
 #define PKV_DEVERR_TIMEOUT 0x8             /* a bounded in-kernel wait gave up */
 #define PKV_DEVERR_PLAN_OVERFLOW 0x10      /* work list did not fit the workspace */
+#define PKV_DEVERR_INTERNAL 0x20           /* a kernel found its launch configuration unusable */
 
 /*
  * paged_kv_write - scatter new K/V rows into the block pool.

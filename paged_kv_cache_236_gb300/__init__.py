@@ -39,6 +39,7 @@ DEVERR = {
     "bad_sequence": 0x4,
     "timeout": 0x8,
     "plan_overflow": 0x10,
+    "internal": 0x20,
 }
 
 

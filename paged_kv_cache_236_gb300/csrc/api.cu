@@ -1,13 +1,15 @@
 // Host side of the C ABI declared in include/paged_kv.h: argument checks,
 // tensor-map encoding, workspace layout and the launch sequence
 //   planner -> tensor-core kernel (multi-token rows) -> CUDA-core kernel
-//   (decode-shaped rows) -> split merge
-// all on the caller's stream, with no host synchronisation.
+//   (decode-shaped rows)
+// all on the caller's stream, with no host synchronisation (split-KV partial
+// rows are merged inside the attention kernels by the last split to finish).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <math.h>
+#include <algorithm>
 #include <mutex>
 #include <stdarg.h>
 #include <stdio.h>
@@ -146,6 +148,8 @@ WorkspaceLayout workspace_layout(int B, int64_t T, int Hq, int Hkv, int D, size_
   off = align_up(off + (size_t)mma_cap * sizeof(WorkItem));
   L.merge_off = off;
   off = align_up(off + (size_t)merge_cap * sizeof(MergeGroup));
+  L.ticket_off = off;
+  off = align_up(off + (size_t)merge_cap * sizeof(int));
   const size_t fixed = off;
   const size_t per_row = sizeof(float2) + (size_t)D * sizeof(float);
   int64_t part_cap = 0;
@@ -296,14 +300,26 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   WorkItem* dec_items = reinterpret_cast<WorkItem*>(ws + lay.dec_off);
   WorkItem* mma_items = reinterpret_cast<WorkItem*>(ws + lay.mma_off);
   MergeGroup* merges = reinterpret_cast<MergeGroup*>(ws + lay.merge_off);
+  int* tickets = reinterpret_cast<int*>(ws + lay.ticket_off);
   float2* part_ml = reinterpret_cast<float2*>(ws + lay.ml_off);
   float* part_acc = reinterpret_cast<float*>(ws + lay.acc_off);
 
   // tensor-core path: bf16, head_dim 128, G a power of two (a 128-row tile is
   // 128/G whole tokens)
   const bool mma_ok = bf16 && D == 128 && (G & (G - 1)) == 0 && G <= 128;
-  // with a host hint that no sequence has more than kDecRows rows, skip the launch
-  const bool mma_launch = mma_ok && !(max_query_len > 0 && (int64_t)max_query_len * G <= kDecRows);
+  // decode-shaped rows: tensor-core kernel (keys on M, rows on N) for bf16,
+  // head_dim 128 and G dividing 16; the CUDA-core kernel otherwise
+  const bool dectc = mma_ok && G <= kTcDecRows;
+  const int dec_rows_max = dectc ? kTcDecRows : kDecRows;
+  // rows of softmax per key in that kernel: a power of two >= G (so items hold
+  // whole tokens) covering the hinted query length; 16 when there is no hint
+  int tc_rows = kTcDecRows;
+  if (dectc && max_query_len > 0) {
+    const int64_t want = std::max<int64_t>(G, (int64_t)max_query_len * G);
+    tc_rows = want <= 4 ? 4 : want <= 8 ? 8 : kTcDecRows;
+  }
+  // with a host hint that no sequence has more rows than that, skip the launch
+  const bool mma_launch = mma_ok && !(max_query_len > 0 && (int64_t)max_query_len * G <= dec_rows_max);
   const int dec_grid = dev->sms * dec_ctas;
 
   PlanParams pp{};
@@ -317,10 +333,12 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   pp.max_blocks = max_blocks_per_seq;
   pp.causal = causal ? 1 : 0;
   pp.mma_ok = mma_launch ? 1 : 0;
-  pp.dec_rows_max = kDecRows;
-  pp.target_dec = dec_grid * 4;
+  pp.dec_rows_max = dec_rows_max;
+  pp.dec_unit_rows = dectc ? tc_rows : kDecRows;
+  pp.dec_tile_keys = dectc ? kMmaTileKeys : kDecTileKeys;
+  pp.target_dec = dectc ? dev->sms * 6 : dec_grid * 4;
   pp.target_mma = dev->sms * 4;
-  pp.min_chunk_dec = 256;
+  pp.min_chunk_dec = dectc ? 512 : 256;
   pp.min_chunk_mma = 512;
   pp.dec_cap = lay.dec_cap;
   pp.mma_cap = lay.mma_cap;
@@ -330,6 +348,7 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   pp.dec_items = dec_items;
   pp.mma_items = mma_items;
   pp.merges = merges;
+  pp.tickets = tickets;
   pp.out = out;
   pp.out_row_bytes = Hq * D * elem_bytes(dtype);
   pp.err = dev->err;
@@ -350,6 +369,8 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   ap.header = header;
   ap.part_ml = part_ml;
   ap.part_acc = part_acc;
+  ap.groups = merges;
+  ap.tickets = tickets;
   ap.Hq = Hq;
   ap.Hkv = Hkv;
   ap.G = G;
@@ -377,20 +398,22 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   }
   ap.counter = &header->dec_counter;
   ap.items = dec_items;
-  if ((e = launch_decode(ap, kmap, vmap, bf16, dec_grid, s)) != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (dectc) {
+    CUtensorMap qmap16, kmap_sw, vmap_sw;
+    if ((st = encode_q_map(&qmap16, q, T, Hq, D, 64, G, kTcDecRows / G)) != PKV_OK) return st;
+    if ((st = encode_pool_map(&kmap_sw, k_cache, dtype, num_blocks, bs, Hkv, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        PKV_OK)
+      return st;
+    if ((st = encode_pool_map(&vmap_sw, v_cache, dtype, num_blocks, bs, Hkv, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        PKV_OK)
+      return st;
+    if ((e = launch_dectc(ap, tc_rows, qmap16, kmap_sw, vmap_sw, dev->sms, s)) != cudaSuccess)
+      return cuda_fail(e, "decode (tensor-core) launch");
+  } else if ((e = launch_decode(ap, kmap, vmap, bf16, dec_grid, s)) != cudaSuccess) {
+    return cuda_fail(e, "decode launch");
+  }
   if (g_prof_stop && (e = cudaEventRecord(g_prof_stop, s)) != cudaSuccess) return cuda_fail(e, "profile event");
 
-  MergeParams mp{};
-  mp.out = out;
-  mp.query_start_loc = query_start_loc;
-  mp.header = header;
-  mp.groups = merges;
-  mp.part_ml = part_ml;
-  mp.part_acc = part_acc;
-  mp.Hq = Hq;
-  mp.G = G;
-  mp.D = D;
-  if ((e = launch_merge(mp, bf16, dev->sms * 4, s)) != cudaSuccess) return cuda_fail(e, "merge launch");
   return PKV_OK;
 }
 

@@ -1,5 +1,4 @@
-// CUDA-core paged attention for few rows per kv head (decode), with split-KV,
-// plus the split merge.
+// CUDA-core paged attention for few rows per kv head (decode), with split-KV.
 //
 // What it computes ("Paged Attention 基础", section 2, steps 1-5): for each
 // work item - up to kDecRows rows (query token, head-in-group) of one
@@ -7,24 +6,29 @@
 // each key block, form scale * q.k, apply the causal mask at the query's
 // absolute position L - n + i, and accumulate softmax(.)V with a running
 // (max, sum) ("online softmax").  Items that cover a whole key range write
-// normalised output rows; split items write partial (m, l, acc) rows that
-// merge_kernel combines: m = max_p m_p, l = sum_p l_p 2^(m_p - m),
+// normalised output rows.  Split items write partial (m, l, acc) rows; the
+// last split of a merge group to finish (an atomic ticket, no waiting)
+// combines them: m = max_p m_p, l = sum_p l_p 2^(m_p - m),
 // O = sum_p acc_p 2^(m_p - m) / l (logits kept in log2 units).
 //
 // GB300 design:
-//  * persistent CTAs (2 per SM) fetch items from an atomic counter;
+//  * persistent CTAs (2 per SM) take items from an atomic counter, in the
+//    planner's largest-first order;
 //  * a producer warp streams each 64-key tile of K and V with TMA: one 4-D
 //    tensor-map box per physical block ({head_dim, 1 head, block_size, 1
 //    block} of the pool [num_blocks, block_size, num_kv_heads, head_dim]), so
 //    the block table is resolved by the box coordinate and blocks past a
 //    sequence's end (or invalid ids) are out-of-range boxes that read as
-//    zeros; a 3-stage mbarrier ring keeps ~64 KB per CTA in flight;
+//    zeros.  Block ids are loaded one tile ahead; an item's q rows arrive in
+//    the same stage as its first tile (bulk copies); the item's description
+//    travels in the stage's metadata, so consumers never wait on global
+//    memory.  A 3-stage mbarrier ring keeps ~64 KB per CTA in flight;
 //  * 4 consumer warps each own 16 keys of a tile: 8 lanes per key (16-byte
 //    shared loads, conflict-free), partial dot products for the 4 rows of 2
-//    keys reduced with a transposing butterfly (7 shuffles per 8 scores),
-//    warp-level online softmax, then P.V with each lane owning head_dim/32
-//    output columns of all 4 rows; the 4 warp states are merged at the end of
-//    an item through shared memory.
+//    keys in packed fp32x2 FMAs reduced with a transposing butterfly (7
+//    shuffles per 8 scores), warp-level online softmax, then P.V with each
+//    lane owning head_dim/32 output columns of all 4 rows (packed FMAs); the
+//    4 warp states are merged at the end of an item through shared memory.
 #include <math_constants.h>
 
 #include "pkv_device.cuh"
@@ -41,7 +45,7 @@ constexpr int kLPT = 8;                                   // lanes per key (QK)
 constexpr int kTPR = kLPT / kRP;                          // keys per lane group per round (2)
 constexpr int kKeysPerRound = (32 / kLPT) * kTPR;         // 8
 constexpr int kRounds = kWarpKeys / kKeysPerRound;        // 2
-constexpr int kMetaDone = 2, kMetaLast = 1;
+constexpr int kMetaDone = 2, kMetaLast = 1, kMetaFirst = 4;
 static_assert(kRP == 4 && kLPT == 8, "butterfly below is written for 8 partials per lane");
 
 template <typename T, int D>
@@ -54,95 +58,101 @@ struct Cfg {
   static constexpr int kEPL = kCPL * kEPC;     // q elements per lane
   static constexpr int kDPL = D / 32;          // output columns per lane
   static constexpr int kTileBytes = kDecTileKeys * kRowBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kStages = (98304 / kStageBytes) < 2 ? 2 : ((98304 / kStageBytes) > 4 ? 4 : (98304 / kStageBytes));
+  static constexpr int kQSlotOff = 2 * kTileBytes;  // an item's q rows, in its first tile's stage
+  static constexpr int kStageBytes = (2 * kTileBytes + kRP * kRowBytes + 1023) / 1024 * 1024;
+  static constexpr int kStages =
+      (98304 / kStageBytes) < 2 ? 2 : ((98304 / kStageBytes) > 4 ? 4 : (98304 / kStageBytes));
   // shared memory carve-up
   static constexpr int kPOff = kStages * kStageBytes;
-  static constexpr int kPBytes = kConsumerWarps * kWarpKeys * kRP * 4;
+  static constexpr int kPBytes = kConsumerWarps * kWarpKeys * kRP * 8;  // (p, p) pairs
   static constexpr int kAccOff = kPOff + kPBytes;
   static constexpr int kAccBytes = kConsumerWarps * kRP * D * 4;
   static constexpr int kMlOff = kAccOff + kAccBytes;
   static constexpr int kMlBytes = kConsumerWarps * kRP * 2 * 4;
   static constexpr int kMetaOff = kMlOff + kMlBytes;
-  static constexpr int kMetaBytes = kStages * 16;
+  static constexpr int kMetaBytes = kStages * 64;
   static constexpr int kBarOff = kMetaOff + kMetaBytes;
-  static constexpr int kSmem = kBarOff + 2 * kStages * 8 + 1024;  // + slack to align the base to 1 KB
+  static constexpr int kSmem = kBarOff + 2 * kStages * 8 + 16 + 1024;  // + slack to align the base to 1 KB
   static_assert(kCPL >= 1 && kChunks % kLPT == 0, "row must split into 8 lanes of 16-byte chunks");
 };
 
+// What a stage carries besides K and V: which item and key tile, and the
+// item's description (so consumers need no global loads).
 struct alignas(16) Meta {
-  int item, kbase, flags, pad;
+  int item, kbase, flags, seq;
+  int kvh, row0, nrows, ke;
+  int part, grp, L, n;
+  int qstart, pad0, pad1, pad2;
 };
+static_assert(sizeof(Meta) == 64, "meta slot");
 
-template <int kBytes>
-struct VecT;
-template <>
-struct VecT<4> {
-  using type = uint32_t;
-};
-template <>
-struct VecT<8> {
-  using type = uint2;
-};
-template <>
-struct VecT<16> {
-  using type = uint4;
-};
+// ---------------------------------------------------------------------------
+// packed fp32x2 arithmetic (two fp32 values in one 64-bit register pair)
+// ---------------------------------------------------------------------------
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 up2(f32x2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
-// Convert one 16-byte chunk of K into floats.
+// One 16-byte chunk of K or q as kEPC/2 fp32 pairs (elements 2j, 2j+1).
 template <typename T>
-__device__ __forceinline__ void chunk_to_float(const uint4 raw, float* f);
+__device__ __forceinline__ void chunk_to_pairs(const uint4 raw, f32x2* f);
 template <>
-__device__ __forceinline__ void chunk_to_float<__nv_bfloat16>(const uint4 raw, float* f) {
-  f[0] = bf16_lo(raw.x);
-  f[1] = bf16_hi(raw.x);
-  f[2] = bf16_lo(raw.y);
-  f[3] = bf16_hi(raw.y);
-  f[4] = bf16_lo(raw.z);
-  f[5] = bf16_hi(raw.z);
-  f[6] = bf16_lo(raw.w);
-  f[7] = bf16_hi(raw.w);
+__device__ __forceinline__ void chunk_to_pairs<__nv_bfloat16>(const uint4 raw, f32x2* f) {
+  f[0] = pk2(bf16_lo(raw.x), bf16_hi(raw.x));
+  f[1] = pk2(bf16_lo(raw.y), bf16_hi(raw.y));
+  f[2] = pk2(bf16_lo(raw.z), bf16_hi(raw.z));
+  f[3] = pk2(bf16_lo(raw.w), bf16_hi(raw.w));
 }
 template <>
-__device__ __forceinline__ void chunk_to_float<float>(const uint4 raw, float* f) {
-  f[0] = __uint_as_float(raw.x);
-  f[1] = __uint_as_float(raw.y);
-  f[2] = __uint_as_float(raw.z);
-  f[3] = __uint_as_float(raw.w);
+__device__ __forceinline__ void chunk_to_pairs<float>(const uint4 raw, f32x2* f) {
+  f[0] = pk2(__uint_as_float(raw.x), __uint_as_float(raw.y));
+  f[1] = pk2(__uint_as_float(raw.z), __uint_as_float(raw.w));
 }
 
-// Load this lane's kDPL V columns of one key row as floats.
+// This lane's kDPL V columns of one key row as fp32 pairs.
 template <typename T, int DPL>
-__device__ __forceinline__ void load_v(const uint8_t* p, float* f) {
+__device__ __forceinline__ void load_v_pairs(const uint8_t* p, f32x2* f) {
   if constexpr (sizeof(T) == 2) {
     if constexpr (DPL == 4) {
       const uint2 w = *reinterpret_cast<const uint2*>(p);
-      f[0] = bf16_lo(w.x);
-      f[1] = bf16_hi(w.x);
-      f[2] = bf16_lo(w.y);
-      f[3] = bf16_hi(w.y);
+      f[0] = pk2(bf16_lo(w.x), bf16_hi(w.x));
+      f[1] = pk2(bf16_lo(w.y), bf16_hi(w.y));
     } else {
       const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-      f[0] = bf16_lo(w);
-      f[1] = bf16_hi(w);
+      f[0] = pk2(bf16_lo(w), bf16_hi(w));
     }
   } else {
     if constexpr (DPL == 4) {
-      const float4 w = *reinterpret_cast<const float4*>(p);
-      f[0] = w.x;
-      f[1] = w.y;
-      f[2] = w.z;
-      f[3] = w.w;
+      const uint4 w = *reinterpret_cast<const uint4*>(p);
+      f[0] = pk2(__uint_as_float(w.x), __uint_as_float(w.y));
+      f[1] = pk2(__uint_as_float(w.z), __uint_as_float(w.w));
     } else {
-      const float2 w = *reinterpret_cast<const float2*>(p);
-      f[0] = w.x;
-      f[1] = w.y;
+      const uint2 w = *reinterpret_cast<const uint2*>(p);
+      f[0] = pk2(__uint_as_float(w.x), __uint_as_float(w.y));
     }
   }
 }
 
 // Sum v[i] over the 8 lanes of a lane group, transposing: afterwards lane
-// (lane & 7) == i holds the group total of v[i] in v[0].
+// (lane & 7) == i holds the group total of v[i].
 __device__ __forceinline__ float group_transpose_sum(float v[8], int lane) {
   const bool b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
 #pragma unroll
@@ -162,6 +172,13 @@ __device__ __forceinline__ float group_transpose_sum(float v[8], int lane) {
   return keep + __shfl_xor_sync(0xffffffffu, send, 1);
 }
 
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
                                                              const __grid_constant__ CUtensorMap kmap,
@@ -169,15 +186,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
   using C = Cfg<T, D>;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  float* pbuf = reinterpret_cast<float*>(smem + C::kPOff);
+  f32x2* pbuf = reinterpret_cast<f32x2*>(smem + C::kPOff);
   float* comb_acc = reinterpret_cast<float*>(smem + C::kAccOff);
   float* comb_ml = reinterpret_cast<float*>(smem + C::kMlOff);
   Meta* meta = reinterpret_cast<Meta*>(smem + C::kMetaOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* empty = full + C::kStages;
+  int* flag_last = reinterpret_cast<int*>(empty + C::kStages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_items = p.header->n_dec;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -186,6 +203,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();  // the plan and the K/V write are complete and visible from here on
+  const int n_items = p.header->n_dec;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -195,50 +214,82 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
     }
     const int nb_per_tile = kDecTileKeys / p.bs;
     int tile = 0;
+    int idx = 0;
+    if (lane == 0) idx = atomicAdd(p.counter, 1);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
     for (;;) {
-      int idx = 0;
-      if (lane == 0) idx = atomicAdd(p.counter, 1);
-      idx = __shfl_sync(0xffffffffu, idx, 0);
-      const int stage0 = tile % C::kStages;
       if (idx >= n_items) {
-        if (!mbar_wait(&empty[stage0], ((tile / C::kStages) & 1) ^ 1, p.err)) return;
+        const int stage = tile % C::kStages;
+        if (!mbar_wait(&empty[stage], ((tile / C::kStages) & 1) ^ 1, p.err)) return;
         if (lane == 0) {
-          meta[stage0].item = -1;
-          meta[stage0].flags = kMetaDone;
-          mbar_arrive(&full[stage0]);
+          meta[stage].item = -1;
+          meta[stage].flags = kMetaDone;
+          mbar_arrive(&full[stage]);
         }
         break;
       }
       const WorkItem it = p.items[idx];
+      // take the next item now; its index is only needed after this item's tiles
+      int next = 0;
+      if (lane == 0) next = atomicAdd(p.counter, 1);
       const int L = p.context_lens[it.seq];
+      const int qstart = p.query_start_loc[it.seq];
+      const int n = p.query_start_loc[it.seq + 1] - qstart;
       const int nblk = (L + p.bs - 1) / p.bs;
       const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
+      auto block_of = [&](int kbase) -> int {  // physical block for this lane in the tile at kbase
+        const int lb = kbase / p.bs + lane;
+        int phys = (int)p.num_blocks;  // out of range: the box reads as zeros
+        if (lane < nb_per_tile && lb < nblk) {
+          const int b = __ldg(bt + lb);
+          if (b >= 0 && (int64_t)b < p.num_blocks)
+            phys = b;
+          else
+            raise_error(p.err, PKV_DEVERR_BLOCK_OUT_OF_RANGE);
+        }
+        return phys;
+      };
+      int phys = block_of(it.kb);
       for (int kbase = it.kb; kbase < it.ke; kbase += kDecTileKeys) {
         const int stage = tile % C::kStages;
+        const bool first = kbase == it.kb;
+        const int next_phys = (kbase + kDecTileKeys < it.ke) ? block_of(kbase + kDecTileKeys) : 0;
         if (!mbar_wait(&empty[stage], ((tile / C::kStages) & 1) ^ 1, p.err)) return;
+        uint8_t* sbase = smem + stage * C::kStageBytes;
         if (lane == 0) {
-          meta[stage].item = idx;
-          meta[stage].kbase = kbase;
-          meta[stage].flags = (kbase + kDecTileKeys >= it.ke) ? kMetaLast : 0;
-          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+          Meta& m = meta[stage];
+          m.item = idx;
+          m.kbase = kbase;
+          m.flags = ((kbase + kDecTileKeys >= it.ke) ? kMetaLast : 0) | (first ? kMetaFirst : 0);
+          m.seq = it.seq;
+          m.kvh = it.kvh;
+          m.row0 = it.row0;
+          m.nrows = it.nrows;
+          m.ke = it.ke;
+          m.part = it.part;
+          m.grp = it.grp;
+          m.L = L;
+          m.n = n;
+          m.qstart = qstart;
+          mbar_arrive_expect_tx(&full[stage], 2 * C::kTileBytes + (first ? it.nrows * C::kRowBytes : 0));
         }
         __syncwarp();
         if (lane < nb_per_tile) {
-          const int lb = kbase / p.bs + lane;
-          int phys = (int)p.num_blocks;  // out of range: the box reads as zeros
-          if (lb < nblk) {
-            const int b = bt[lb];
-            if (b >= 0 && (int64_t)b < p.num_blocks)
-              phys = b;
-            else
-              raise_error(p.err, PKV_DEVERR_BLOCK_OUT_OF_RANGE);
-          }
-          uint8_t* kdst = smem + stage * C::kStageBytes + lane * p.bs * C::kRowBytes;
+          uint8_t* kdst = sbase + lane * p.bs * C::kRowBytes;
           tma_load_4d(kdst, &kmap, &full[stage], 0, it.kvh, 0, phys);
           tma_load_4d(kdst + C::kTileBytes, &vmap, &full[stage], 0, it.kvh, 0, phys);
         }
+        if (first && lane < it.nrows) {
+          const int row = it.row0 + lane;
+          const int tok = row / p.G, g = row - tok * p.G;
+          const T* qrow =
+              reinterpret_cast<const T*>(p.q) + ((int64_t)(qstart + tok) * p.Hq + (int64_t)it.kvh * p.G + g) * D;
+          bulk_load(sbase + C::kQSlotOff + lane * C::kRowBytes, qrow, C::kRowBytes, &full[stage]);
+        }
+        phys = next_phys;
         ++tile;
       }
+      idx = __shfl_sync(0xffffffffu, next, 0);
     }
     return;
   }
@@ -246,58 +297,46 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
   // -------------------------------------------------------------- consumers
   const int grp = lane >> 3, j = lane & 7;
   const int myrow = lane & (kRP - 1);  // row whose scores this lane holds
-  float* pw = pbuf + warp * kWarpKeys * kRP;
+  f32x2* pw = pbuf + warp * kWarpKeys * kRP;
 
-  float qf[kRP][C::kEPL];
-  float acc[kRP][C::kDPL];
+  f32x2 qf[kRP][C::kEPL / 2];
+  f32x2 acc[kRP][C::kDPL / 2];
   float m_row = -CUDART_INF_F, l_row = 0.f;
   int vis_row = 0;  // keys visible to row `myrow` (absolute key < vis_row)
-  WorkItem it = {0, 0, 0, 0, 0, 0, -1, 0};
-  int L = 0, n = 0, qstart = 0;
-  int cur = -1;
   int tile = 0;
   for (;;) {
     const int stage = tile % C::kStages;
     if (!mbar_wait(&full[stage], (tile / C::kStages) & 1, p.err)) break;
     const Meta mt = meta[stage];
     if (mt.flags & kMetaDone) break;
-    if (mt.item != cur) {
-      cur = mt.item;
-      it = p.items[cur];
-      L = p.context_lens[it.seq];
-      qstart = p.query_start_loc[it.seq];
-      n = p.query_start_loc[it.seq + 1] - qstart;
+    const uint8_t* sbase = smem + stage * C::kStageBytes;
+    if (mt.flags & kMetaFirst) {
       m_row = -CUDART_INF_F;
       l_row = 0.f;
+      const f32x2 sc2 = pk2(p.scale_log2, p.scale_log2);
 #pragma unroll
       for (int r = 0; r < kRP; ++r) {
 #pragma unroll
-        for (int e = 0; e < C::kDPL; ++e) acc[r][e] = 0.f;
-        const int row = it.row0 + r;
-        if (r < it.nrows) {
-          const int tok = row / p.G, g = row - tok * p.G;
-          const T* qrow = reinterpret_cast<const T*>(p.q) +
-                          ((int64_t)(qstart + tok) * p.Hq + (int64_t)it.kvh * p.G + g) * D;
+        for (int e = 0; e < C::kDPL / 2; ++e) acc[r][e] = 0ull;
+        if (r < mt.nrows) {
+          const uint8_t* qrow = sbase + C::kQSlotOff + r * C::kRowBytes;
 #pragma unroll
           for (int m = 0; m < C::kCPL; ++m) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(qrow + (j + 8 * m) * C::kEPC);
-            float f[C::kEPC];
-            chunk_to_float<T>(raw, f);
+            const uint4 raw = *reinterpret_cast<const uint4*>(qrow + (j + 8 * m) * 16);
+            f32x2 f[C::kEPC / 2];
+            chunk_to_pairs<T>(raw, f);
 #pragma unroll
-            for (int e = 0; e < C::kEPC; ++e) qf[r][m * C::kEPC + e] = f[e] * p.scale_log2;
+            for (int e = 0; e < C::kEPC / 2; ++e) qf[r][m * (C::kEPC / 2) + e] = mul2(f[e], sc2);
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < C::kEPL; ++e) qf[r][e] = 0.f;
+          for (int e = 0; e < C::kEPL / 2; ++e) qf[r][e] = 0ull;
         }
       }
-      {
-        const int row = it.row0 + myrow;
-        const int tok = row / p.G;
-        vis_row = myrow < it.nrows ? min(it.ke, p.causal ? L - n + tok + 1 : L) : 0;
-      }
+      const int tok = (mt.row0 + myrow) / p.G;
+      vis_row = myrow < mt.nrows ? min(mt.ke, p.causal ? mt.L - mt.n + tok + 1 : mt.L) : 0;
     }
-    const uint8_t* ks = smem + stage * C::kStageBytes + warp * kWarpKeys * C::kRowBytes;
+    const uint8_t* ks = sbase + warp * kWarpKeys * C::kRowBytes;
     const uint8_t* vs = ks + C::kTileBytes;
     const int wkb = mt.kbase + warp * kWarpKeys;  // absolute key of this warp's first key
 
@@ -305,9 +344,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
     float sc[kRounds];
 #pragma unroll
     for (int rnd = 0; rnd < kRounds; ++rnd) {
-      float part[kTPR * kRP];
+      f32x2 part2[kTPR * kRP];
 #pragma unroll
-      for (int i = 0; i < kTPR * kRP; ++i) part[i] = 0.f;
+      for (int i = 0; i < kTPR * kRP; ++i) part2[i] = 0ull;
 #pragma unroll
       for (int t = 0; t < kTPR; ++t) {
         const int kl = rnd * kKeysPerRound + grp * kTPR + t;
@@ -315,13 +354,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
 #pragma unroll
         for (int m = 0; m < C::kCPL; ++m) {
           const uint4 raw = *reinterpret_cast<const uint4*>(krow + (j + 8 * m) * 16);
-          float f[C::kEPC];
-          chunk_to_float<T>(raw, f);
+          f32x2 f[C::kEPC / 2];
+          chunk_to_pairs<T>(raw, f);
 #pragma unroll
           for (int r = 0; r < kRP; ++r)
 #pragma unroll
-            for (int e = 0; e < C::kEPC; ++e) part[t * kRP + r] = fmaf(qf[r][m * C::kEPC + e], f[e], part[t * kRP + r]);
+            for (int e = 0; e < C::kEPC / 2; ++e)
+              part2[t * kRP + r] = fma2(qf[r][m * (C::kEPC / 2) + e], f[e], part2[t * kRP + r]);
         }
+      }
+      float part[kTPR * kRP];
+#pragma unroll
+      for (int i = 0; i < kTPR * kRP; ++i) {
+        const float2 h = up2(part2[i]);
+        part[i] = h.x + h.y;
       }
       const float s = group_transpose_sum(part, lane);
       const int key = wkb + rnd * kKeysPerRound + grp * kTPR + (j / kRP);
@@ -343,37 +389,36 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
     for (int rnd = 0; rnd < kRounds; ++rnd) {
       const float pr = exp2f(sc[rnd] - m_use);
       psum += pr;
-      pw[(rnd * kKeysPerRound + grp * kTPR + (j / kRP)) * kRP + myrow] = pr;
+      pw[(rnd * kKeysPerRound + grp * kTPR + (j / kRP)) * kRP + myrow] = pk2(pr, pr);
     }
     psum += __shfl_xor_sync(0xffffffffu, psum, 4);
     psum += __shfl_xor_sync(0xffffffffu, psum, 8);
     psum += __shfl_xor_sync(0xffffffffu, psum, 16);
     l_row = l_row * alpha + psum;
     m_row = m_new;
-    float a[kRP];
 #pragma unroll
-    for (int r = 0; r < kRP; ++r) a[r] = __shfl_sync(0xffffffffu, alpha, r);
+    for (int r = 0; r < kRP; ++r) {
+      const float a = __shfl_sync(0xffffffffu, alpha, r);
+      const f32x2 a2 = pk2(a, a);
 #pragma unroll
-    for (int r = 0; r < kRP; ++r)
-#pragma unroll
-      for (int e = 0; e < C::kDPL; ++e) acc[r][e] *= a[r];
+      for (int e = 0; e < C::kDPL / 2; ++e) acc[r][e] = mul2(acc[r][e], a2);
+    }
     __syncwarp();
 
     // ---- acc += P V over this warp's keys that exist (keys >= ke may hold garbage)
-    const int kcount = max(0, min(kWarpKeys, it.ke - wkb));
+    const int kcount = max(0, min(kWarpKeys, mt.ke - wkb));
 #pragma unroll
     for (int kk = 0; kk < kWarpKeys; ++kk) {
       if (kk < kcount) {
-        const float4 pv = *reinterpret_cast<const float4*>(pw + kk * kRP);
-        float vf[C::kDPL];
-        load_v<T, C::kDPL>(vs + kk * C::kRowBytes + lane * C::kDPL * C::kEs, vf);
+        const ulonglong2 p01 = *reinterpret_cast<const ulonglong2*>(pw + kk * kRP);
+        const ulonglong2 p23 = *reinterpret_cast<const ulonglong2*>(pw + kk * kRP + 2);
+        const f32x2 pp[4] = {p01.x, p01.y, p23.x, p23.y};
+        f32x2 vf[C::kDPL / 2];
+        load_v_pairs<T, C::kDPL>(vs + kk * C::kRowBytes + lane * C::kDPL * C::kEs, vf);
 #pragma unroll
-        for (int e = 0; e < C::kDPL; ++e) {
-          acc[0][e] = fmaf(pv.x, vf[e], acc[0][e]);
-          acc[1][e] = fmaf(pv.y, vf[e], acc[1][e]);
-          acc[2][e] = fmaf(pv.z, vf[e], acc[2][e]);
-          acc[3][e] = fmaf(pv.w, vf[e], acc[3][e]);
-        }
+        for (int r = 0; r < kRP; ++r)
+#pragma unroll
+          for (int e = 0; e < C::kDPL / 2; ++e) acc[r][e] = fma2(pp[r], vf[e], acc[r][e]);
       }
     }
     __syncwarp();
@@ -389,11 +434,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
 #pragma unroll
       for (int r = 0; r < kRP; ++r)
 #pragma unroll
-        for (int e = 0; e < C::kDPL; ++e) comb_acc[(warp * kRP + r) * D + lane * C::kDPL + e] = acc[r][e];
+        for (int e = 0; e < C::kDPL / 2; ++e) {
+          const float2 h = up2(acc[r][e]);
+          comb_acc[(warp * kRP + r) * D + lane * C::kDPL + 2 * e] = h.x;
+          comb_acc[(warp * kRP + r) * D + lane * C::kDPL + 2 * e + 1] = h.y;
+        }
       named_barrier(1, kConsumerWarps * 32);
       for (int idx = threadIdx.x; idx < kRP * D; idx += kConsumerWarps * 32) {
         const int r = idx / D, d = idx - r * D;
-        if (r >= it.nrows) continue;
+        if (r >= mt.nrows) continue;
         float M = -CUDART_INF_F;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_ml[(w * kRP + r) * 2]);
@@ -405,49 +454,51 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
           lsum = fmaf(wt, comb_ml[(w * kRP + r) * 2 + 1], lsum);
           o = fmaf(wt, comb_acc[(w * kRP + r) * D + d], o);
         }
-        if (it.part < 0) {
-          const int row = it.row0 + r;
+        if (mt.part < 0) {
+          const int row = mt.row0 + r;
           const int tok = row / p.G, g = row - tok * p.G;
-          T* orow = reinterpret_cast<T*>(p.out) + ((int64_t)(qstart + tok) * p.Hq + (int64_t)it.kvh * p.G + g) * D;
+          T* orow =
+              reinterpret_cast<T*>(p.out) + ((int64_t)(mt.qstart + tok) * p.Hq + (int64_t)mt.kvh * p.G + g) * D;
           orow[d] = Elem<T>::to_out(o / lsum);
         } else {
-          p.part_acc[(int64_t)(it.part + r) * D + d] = o;
-          if (d == 0) p.part_ml[it.part + r] = make_float2(M, lsum);
+          p.part_acc[(int64_t)(mt.part + r) * D + d] = o;
+          if (d == 0) p.part_ml[mt.part + r] = make_float2(M, lsum);
+        }
+      }
+      if (mt.part >= 0) {
+        // the split that completes its merge group combines the group's partials
+        __threadfence();
+        named_barrier(1, kConsumerWarps * 32);
+        if (threadIdx.x == 0) *flag_last = atomicAdd(p.tickets + mt.grp, 1);
+        named_barrier(1, kConsumerWarps * 32);
+        const MergeGroup g = p.groups[mt.grp];
+        if (*flag_last == g.nsplit - 1) {
+          __threadfence();
+          for (int idx = threadIdx.x; idx < g.nrows * D; idx += kConsumerWarps * 32) {
+            const int r = idx / D, d = idx - r * D;
+            float M = -CUDART_INF_F;
+#pragma unroll 8
+            for (int sp = 0; sp < g.nsplit; ++sp)
+              M = fmaxf(M, __ldcg(&p.part_ml[g.part_base + sp * g.nrows + r]).x);
+            const float Mu = M == -CUDART_INF_F ? 0.f : M;
+            float lsum = 0.f, o = 0.f;
+#pragma unroll 8
+            for (int sp = 0; sp < g.nsplit; ++sp) {
+              const int slot = g.part_base + sp * g.nrows + r;
+              const float2 ml = __ldcg(&p.part_ml[slot]);
+              const float wt = exp2f(ml.x - Mu);
+              lsum = fmaf(wt, ml.y, lsum);
+              o = fmaf(wt, __ldcg(&p.part_acc[(int64_t)slot * D + d]), o);
+            }
+            const int row = g.row0 + r;
+            const int tok = row / p.G, gh = row - tok * p.G;
+            T* orow =
+                reinterpret_cast<T*>(p.out) + ((int64_t)(mt.qstart + tok) * p.Hq + (int64_t)g.kvh * p.G + gh) * D;
+            orow[d] = Elem<T>::to_out(o / lsum);
+          }
         }
       }
       named_barrier(1, kConsumerWarps * 32);
-    }
-  }
-}
-
-template <typename T, int D>
-__global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
-  const int n = p.header->n_merge;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int gi = blockIdx.x; gi < n; gi += gridDim.x) {
-    const MergeGroup g = p.groups[gi];
-    const int qstart = p.query_start_loc[g.seq];
-    for (int r = warp; r < g.nrows; r += 4) {
-      float M = -CUDART_INF_F;
-      for (int sp = 0; sp < g.nsplit; ++sp) M = fmaxf(M, p.part_ml[g.part_base + sp * g.nrows + r].x);
-      const float Mu = M == -CUDART_INF_F ? 0.f : M;
-      float lsum = 0.f;
-      for (int sp = 0; sp < g.nsplit; ++sp) {
-        const float2 ml = p.part_ml[g.part_base + sp * g.nrows + r];
-        lsum = fmaf(exp2f(ml.x - Mu), ml.y, lsum);
-      }
-      const float inv = 1.f / lsum;
-      const int row = g.row0 + r;
-      const int tok = row / p.G, gg = row - tok * p.G;
-      T* orow = reinterpret_cast<T*>(p.out) + ((int64_t)(qstart + tok) * p.Hq + (int64_t)g.kvh * p.G + gg) * D;
-      for (int d = lane; d < D; d += 32) {
-        float o = 0.f;
-        for (int sp = 0; sp < g.nsplit; ++sp) {
-          const int slot = g.part_base + sp * g.nrows + r;
-          o = fmaf(exp2f(p.part_ml[slot].x - Mu), p.part_acc[(int64_t)slot * D + d], o);
-        }
-        orow[d] = Elem<T>::to_out(o * inv);
-      }
     }
   }
 }
@@ -481,8 +532,8 @@ cudaError_t launch_decode_t(const AttnParams& p, const CUtensorMap& kmap, const 
   using C = Cfg<T, D>;
   cudaError_t e = prepare_decode<T, D>(nullptr);
   if (e != cudaSuccess) return e;
-  decode_kernel<T, D><<<grid, kThreads, C::kSmem, s>>>(p, kmap, vmap);
-  return cudaGetLastError();
+  e = launch_pdl(decode_kernel<T, D>, dim3(grid), dim3(kThreads), C::kSmem, s, p, kmap, vmap);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -505,21 +556,6 @@ cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kmap, const CU
   }
   return p.D == 128 ? launch_decode_t<float, 128>(p, kmap, vmap, grid, s)
                     : launch_decode_t<float, 64>(p, kmap, vmap, grid, s);
-}
-
-cudaError_t launch_merge(const MergeParams& p, bool bf16, int grid, cudaStream_t s) {
-  if (bf16) {
-    if (p.D == 128)
-      merge_kernel<__nv_bfloat16, 128><<<grid, 128, 0, s>>>(p);
-    else
-      merge_kernel<__nv_bfloat16, 64><<<grid, 128, 0, s>>>(p);
-  } else {
-    if (p.D == 128)
-      merge_kernel<float, 128><<<grid, 128, 0, s>>>(p);
-    else
-      merge_kernel<float, 64><<<grid, 128, 0, s>>>(p);
-  }
-  return cudaGetLastError();
 }
 
 }  // namespace pkv

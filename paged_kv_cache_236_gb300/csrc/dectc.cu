@@ -1,0 +1,605 @@
+// Tensor-core paged attention for few rows per kv head (decode, short
+// speculative windows): tcgen05.mma with the keys on the M axis.
+//
+// What it computes is the same as every other attention kernel here
+// ("Paged Attention 基础", section 2, steps 1-5; causal mask at each query's
+// absolute position L - n + i): for a work item of up to 16 rows (query
+// token, head-in-group) of one sequence and one kv head over keys [kb, ke),
+// softmax(scale * q k^T) v with a running (max, sum), normalised at the end,
+// or a partial (m, l, acc) row for split-KV; the last split of a merge group
+// to finish merges the group (atomic ticket, no waiting).
+//
+// Why tensor cores: decode reads every K/V byte once and does 4 FMAs per
+// byte pair per query row; on CUDA cores the conversions, reductions and
+// FMAs leave the SMs latency-bound below the HBM rate.  Here each 128-key
+// tile costs two small MMAs, with the rows on N:
+//   S^T [128 keys x 16 rows] = K [128 keys x 128 d] . Q^T        (A K-major, B K-major)
+//   O^T [128 d x 16 rows]   += V^T [128 d x 128 keys] . P^T      (A MN-major, B K-major)
+// so one thread per key does the softmax arithmetic for its key (16 values)
+// and one thread per output column writes the result, coalesced.
+//
+// Roles (320 threads, one CTA per SM, persistent, items from an atomic
+// counter in the planner's largest-first order):
+//   warp 0    TMA producer: per 128-key tile one {64, 1, block_size, 1} box
+//             per physical block and 64-column half of K and V (128-byte
+//             swizzle; out-of-range boxes for blocks past the end read as
+//             zeros), and an item's Q tile ({64, G, 16/G} box of q) with its
+//             first tile; item descriptions travel in per-stage metadata;
+//   warp 1    TMEM allocation and the single thread issuing the MMAs; the
+//             P.V of tile g is issued after the S of tile g+1;
+//   warps 2-5 softmax (thread = key = TMEM lane) and epilogue (thread =
+//             output column = TMEM lane of O^T).
+// Shared memory: 3 stages of K+V (192 KB), 2 Q tiles and 2 P tiles (4 KB
+// each).  TMEM: S^T double-buffered in columns [0,32), O^T in [32,48).
+#include <math_constants.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+#include "pkv_tc.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kStages = 3;
+constexpr int kKeys = kMmaTileKeys;            // 128 keys per tile
+constexpr int kN = kTcDecRows;                 // 16 rows (MMA N)
+constexpr int kTileBytes = kKeys * 128 * 2;    // one of K or V: 32 KB
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kQHalf = kN * 128;               // one 64-column half of the Q / P tiles (2 KB)
+constexpr int kQOff = kStages * kStageBytes;
+constexpr int kPOff = kQOff + 2 * 2 * kQHalf;
+constexpr int kMetaOff = kPOff + 2 * 2 * kQHalf;
+constexpr int kRedOff = kMetaOff + kStages * 64;
+constexpr int kSlotOff = kRedOff + 2 * 4 * kN * 4;
+constexpr int kBarOff = kSlotOff + 2 * 256;
+constexpr int kNumBars = 3 * kStages + 2 * 8;
+constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
+constexpr uint32_t kTmemCols = 64;
+constexpr uint32_t kSCol = 0, kOCol = 32;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kMetaDone = 2, kMetaLast = 1, kMetaFirst = 4;
+
+constexpr uint32_t kIdescS = idesc_bf16(128, kN, false, false);
+constexpr uint32_t kIdescO = idesc_bf16(128, kN, true, false);
+
+struct alignas(16) Meta {
+  int item, kbase, flags, seq;
+  int kvh, row0, nrows, ke;
+  int part, grp, L, n;
+  int qstart, pad0, pad1, pad2;
+};
+static_assert(sizeof(Meta) == 64, "meta slot");
+
+struct Bars {
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  uint64_t o_full[2], o_empty[2], ml_full[2], ml_empty[2];
+};
+
+// What the softmax warps hand the epilogue at an item's end.
+struct alignas(16) EpSlot {
+  Meta mt;
+  float m[kN], l[kN];
+  int done;
+  int pad[15];
+};
+static_assert(sizeof(EpSlot) == 256, "epilogue slot");
+static_assert(sizeof(Bars) == kNumBars * 8, "barrier block");
+
+// All 128 softmax threads (warps 2-5) wait for the same phase; exit together.
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* err) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+}
+
+// Reduce NR values per lane over the 32 lanes of a warp with `op`,
+// transposing: the result returned by lane l is the reduction of value
+// row_of(l) = l >> (5 - log2 NR), so NR values cost NR - 1 + 5 - log2 NR shuffles.
+template <int NR, typename Op>
+__device__ __forceinline__ float xreduce(float (&a)[NR], int lane, Op op) {
+  constexpr int kLog = NR == 1 ? 0 : NR == 2 ? 1 : NR == 4 ? 2 : NR == 8 ? 3 : 4;
+#pragma unroll
+  for (int lvl = 0; lvl < kLog; ++lvl) {
+    const int off = 16 >> lvl;
+    const int half = NR >> (lvl + 1);
+    const bool up = lane & off;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? a[i] : a[i + half];
+      const float keep = up ? a[i + half] : a[i];
+      a[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, off));
+    }
+  }
+  float x = a[0];
+#pragma unroll
+  for (int off = 16 >> kLog; off > 0; off >>= 1) x = op(x, __shfl_xor_sync(0xffffffffu, x, off));
+  return x;
+}
+
+template <int NR>
+__device__ __forceinline__ void tmem_ld_rows(uint32_t taddr, uint32_t (&v)[NR]) {
+  if constexpr (NR == 4) tmem_ld4(taddr, v);
+  else if constexpr (NR == 8) tmem_ld8(taddr, v);
+  else tmem_ld16(taddr, v);
+}
+template <int NR>
+__device__ __forceinline__ void tmem_st_rows(uint32_t taddr, const uint32_t (&v)[NR]) {
+  if constexpr (NR == 4) tmem_st4(taddr, v);
+  else if constexpr (NR == 8) tmem_st8(taddr, v);
+  else tmem_st16(taddr, v);
+}
+
+struct MaxOp {
+  __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+struct AddOp {
+  __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
+};
+
+// NR: rows per item (4, 8 or 16; the MMA's N stays 16, extra columns unused).
+template <int NR>
+__global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
+                                                            const __grid_constant__ CUtensorMap qmap,
+                                                            const __grid_constant__ CUtensorMap kmap,
+                                                            const __grid_constant__ CUtensorMap vmap) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNumBars * 8);
+  int* flag_last = reinterpret_cast<int*>(tmem_slot + 1);
+  Meta* meta = reinterpret_cast<Meta*>(smem + kMetaOff);
+  float* red = reinterpret_cast<float*>(smem + kRedOff);  // [2][4 warps][NR rows]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->s_free[b], 128);
+      mbar_init(&bars->p_full[b], 128);
+      mbar_init(&bars->pv_done[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->o_full[b], 1);
+      mbar_init(&bars->o_empty[b], 128);
+      mbar_init(&bars->ml_full[b], 128);
+      mbar_init(&bars->ml_empty[b], 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();  // the plan and the K/V write are complete and visible from here on
+  const int n_items = p.header->n_dec;
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0) {
+    // ================================================================ producer
+    if (lane == 0) {
+      prefetch_tensormap(&qmap);
+      prefetch_tensormap(&kmap);
+      prefetch_tensormap(&vmap);
+    }
+    const int nb_per_tile = kKeys / p.bs;
+    int g = 0, it_cnt = 0;
+    int idx = 0;
+    if (lane == 0) idx = atomicAdd(p.counter, 1);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
+    for (;;) {
+      if (idx >= n_items) {
+        const int st = g % kStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->kv_empty[st], ((g / kStages) & 1) ^ 1, p.err))) break;
+        if (lane == 0) {
+          meta[st].item = -1;
+          meta[st].flags = kMetaDone;
+          mbar_arrive(&bars->k_full[st]);
+        }
+        break;
+      }
+      const WorkItem it = p.items[idx];
+      int next = 0;
+      if (lane == 0) next = atomicAdd(p.counter, 1);  // consumed after this item's tiles
+      const int L = p.context_lens[it.seq];
+      const int qstart = p.query_start_loc[it.seq];
+      const int n = p.query_start_loc[it.seq + 1] - qstart;
+      const int nblk = (L + p.bs - 1) / p.bs;
+      const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
+      auto block_of = [&](int kbase) -> int {  // physical block of this lane's block in the tile
+        const int lb = kbase / p.bs + lane;
+        int phys = (int)p.num_blocks;  // out of range: the box reads as zeros
+        if (lane < nb_per_tile && lb < nblk) {
+          const int b = __ldg(bt + lb);
+          if (b >= 0 && (int64_t)b < p.num_blocks)
+            phys = b;
+          else
+            raise_error(p.err, PKV_DEVERR_BLOCK_OUT_OF_RANGE);
+        }
+        return phys;
+      };
+      int phys = block_of(it.kb);
+      bool ok = true;
+      for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
+        const int st = g % kStages;
+        const bool first = kbase == it.kb;
+        const int next_phys = (kbase + kKeys < it.ke) ? block_of(kbase + kKeys) : 0;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->kv_empty[st], ((g / kStages) & 1) ^ 1, p.err))) {
+          ok = false;
+          break;
+        }
+        uint8_t* kd = smem + st * kStageBytes;
+        uint8_t* vd = kd + kTileBytes;
+        if (lane == 0) {
+          Meta& m = meta[st];
+          m.item = idx;
+          m.kbase = kbase;
+          m.flags = ((kbase + kKeys >= it.ke) ? kMetaLast : 0) | (first ? kMetaFirst : 0);
+          m.seq = it.seq;
+          m.kvh = it.kvh;
+          m.row0 = it.row0;
+          m.nrows = it.nrows;
+          m.ke = it.ke;
+          m.part = it.part;
+          m.grp = it.grp;
+          m.L = L;
+          m.n = n;
+          m.qstart = qstart;
+          mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes + (first ? 2 * kQHalf : 0));
+          mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
+          if (first) {
+            // this item's Q rows: tokens row0/G .. of the item, G heads each
+            uint8_t* qd = smem + kQOff + (it_cnt & 1) * 2 * kQHalf;
+            const int tok0 = qstart + it.row0 / p.G;
+            tma_load_3d(qd, &qmap, &bars->k_full[st], 0, it.kvh * p.G, tok0);
+            tma_load_3d(qd + kQHalf, &qmap, &bars->k_full[st], 64, it.kvh * p.G, tok0);
+          }
+        }
+        __syncwarp();
+        if (lane < nb_per_tile) {
+          const int row_off = lane * p.bs * 128;
+          tma_load_4d(kd + row_off, &kmap, &bars->k_full[st], 0, it.kvh, 0, phys);
+          tma_load_4d(kd + kHalf + row_off, &kmap, &bars->k_full[st], 64, it.kvh, 0, phys);
+          tma_load_4d(vd + row_off, &vmap, &bars->v_full[st], 0, it.kvh, 0, phys);
+          tma_load_4d(vd + kHalf + row_off, &vmap, &bars->v_full[st], 64, it.kvh, 0, phys);
+        }
+        phys = next_phys;
+      }
+      if (!ok) break;
+      ++it_cnt;
+      idx = __shfl_sync(0xffffffffu, next, 0);
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      int g = 0, it_cnt = -1;
+      int pend = -1, pend_item = 0;  // tile whose P.V is still to be issued, and its item count
+      bool pend_first = false, pend_last = false;
+      auto issue_pv = [&]() -> bool {
+        const int b = pend & 1, st = pend % kStages, ob = pend_item & 1;
+        if (pend_first) {
+          // O^T[ob] is about to be overwritten: the epilogue of item pend_item-2 must have read it
+          if (!mbar_wait(&bars->o_empty[ob], ((pend_item >> 1) & 1) ^ 1, p.err)) return false;
+        }
+        if (!mbar_wait(&bars->p_full[b], (pend >> 1) & 1, p.err)) return false;
+        if (!mbar_wait(&bars->v_full[st], (pend / kStages) & 1, p.err)) return false;
+        tc_fence_after();
+        const uint32_t vbase = smem_base + st * kStageBytes + kTileBytes;
+        const uint32_t pbase = smem_base + kPOff + b * 2 * kQHalf;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint64_t a = desc_mn(vbase + kk * 2048);
+          const uint64_t bd = desc_k(pbase + (kk >> 2) * kQHalf + (kk & 3) * 32);
+          umma_bf16(tmem + kOCol + ob * kN, a, bd, kIdescO, (pend_first && kk == 0) ? 0u : 1u);
+        }
+        umma_commit(&bars->pv_done[b]);
+        umma_commit(&bars->kv_empty[st]);
+        if (pend_last) umma_commit(&bars->o_full[ob]);
+        pend = -1;
+        return true;
+      };
+      for (;; ++g) {
+        const int st = g % kStages;
+        if (!mbar_wait(&bars->k_full[st], (g / kStages) & 1, p.err)) break;
+        const int flags = meta[st].flags;
+        if (flags & kMetaDone) {
+          if (pend >= 0) issue_pv();
+          break;
+        }
+        if (flags & kMetaFirst) ++it_cnt;
+        const int b = g & 1;
+        if (!mbar_wait(&bars->s_free[b], ((g >> 1) & 1) ^ 1, p.err)) break;
+        tc_fence_after();
+        const uint32_t kbase = smem_base + st * kStageBytes;
+        const uint32_t qbase = smem_base + kQOff + (it_cnt & 1) * 2 * kQHalf;
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk) {
+          const uint64_t a = desc_k(kbase + (kk >> 2) * kHalf + (kk & 3) * 32);
+          const uint64_t bd = desc_k(qbase + (kk >> 2) * kQHalf + (kk & 3) * 32);
+          umma_bf16(tmem + kSCol + b * kN, a, bd, kIdescS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars->s_full[b]);
+        if (pend >= 0 && !issue_pv()) break;
+        pend = g;
+        pend_item = it_cnt;
+        pend_first = (flags & kMetaFirst) != 0;
+        pend_last = (flags & kMetaLast) != 0;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ softmax / epilogue
+    constexpr int kLog = NR == 4 ? 2 : NR == 8 ? 3 : 4;
+    const int q4 = warp & 3;
+    const int t = q4 * 32 + lane;  // key of the tile (S^T lane) / output column (O^T lane)
+    const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+    EpSlot* slots = reinterpret_cast<EpSlot*>(smem + kSlotOff);
+    if (warp < 6) {
+      // ---------------------------------------------------------- softmax
+      const int my_row = lane >> (5 - kLog);  // row this lane holds after a reduction
+      const bool row_writer = (lane & ((1 << (5 - kLog)) - 1)) == 0;
+      float m_ref[NR], lsum[NR];
+      int vis[NR];
+      Meta mt;
+      int g = 0, it_cnt = -1;
+      for (;; ++g) {
+        const int st = g % kStages;
+        if (!wait_all(&bars->k_full[st], (g / kStages) & 1, p.err)) break;
+        const int flags = meta[st].flags;
+        if (flags & kMetaDone) {
+          // tell the epilogue warps there are no more items
+          const int ob = (it_cnt + 1) & 1;
+          if (wait_all(&bars->ml_empty[ob], (((it_cnt + 1) >> 1) & 1) ^ 1, p.err)) {
+            if (t == 0) slots[ob].done = 1;
+            mbar_arrive(&bars->ml_full[ob]);
+          }
+          break;
+        }
+        if (flags & kMetaFirst) {
+          mt = meta[st];
+          ++it_cnt;
+#pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            m_ref[r] = -CUDART_INF_F;
+            lsum[r] = 0.f;
+            const int tok = (mt.row0 + r) / p.G;
+            vis[r] = r < mt.nrows ? min(mt.ke, p.causal ? mt.L - mt.n + tok + 1 : mt.L) : 0;
+          }
+        }
+        const int kbase = meta[st].kbase;
+        const int b = g & 1;
+        float* redb = red + b * 4 * NR;  // [4 warps][NR], double-buffered by tile
+        if (!wait_all(&bars->s_full[b], (g >> 1) & 1, p.err)) break;
+        tc_fence_after();
+        uint32_t sraw[NR];
+        tmem_ld_rows<NR>(lane_base + kSCol + b * kN, sraw);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars->s_free[b]);
+
+        // ---- masked logits of this thread's key; row maxima over the tile
+        const int key = kbase + t;
+        float v[NR], a[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          v[r] = key < vis[r] ? __uint_as_float(sraw[r]) : -CUDART_INF_F;
+          a[r] = v[r];
+        }
+        const float wmax = xreduce<NR>(a, lane, MaxOp());
+        if (row_writer) redb[q4 * NR + my_row] = wmax;
+        named_barrier(1, 128);
+        float alpha[NR], m_use[NR];
+        bool any_rescale = false;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          const float mx =
+              fmaxf(fmaxf(redb[r], redb[NR + r]), fmaxf(redb[2 * NR + r], redb[3 * NR + r])) * p.scale_log2;
+          alpha[r] = 1.f;
+          if (mx > m_ref[r] + kRescaleThreshold) {  // false while both are -inf
+            alpha[r] = fast_exp2(m_ref[r] - mx);    // 0 when m_ref is -inf
+            any_rescale |= m_ref[r] != -CUDART_INF_F;
+            m_ref[r] = mx;
+          }
+          m_use[r] = m_ref[r] == -CUDART_INF_F ? 0.f : m_ref[r];
+        }
+        any_rescale = any_rescale && !(flags & kMetaFirst);
+
+        // ---- P (bf16) into this tile's P buffer: row r, column t, 128-byte swizzle
+        if (!wait_all(&bars->pv_done[b], ((g >> 1) & 1) ^ 1, p.err)) break;  // P.V of tile g-2 is done
+        uint8_t* pbuf = smem + kPOff + b * 2 * kQHalf + (t >> 6) * kQHalf;
+        const int pchunk = (t & 63) >> 3, pbyte = (t & 7) * 2;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          const float e = fast_exp2(fmaf(v[r], p.scale_log2, -m_use[r]));
+          lsum[r] = fmaf(lsum[r], alpha[r], e);
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + r * 128 + ((pchunk ^ (r & 7)) << 4) + pbyte) =
+              __float2bfloat16_rn(e);
+        }
+        if (any_rescale) {
+          // O^T must hold every earlier tile's P.V before it is scaled; thread t
+          // owns O^T row t (output column t), whose column r belongs to row r
+          if (!wait_all(&bars->pv_done[b ^ 1], ((g - 1) >> 1) & 1, p.err)) break;
+          tc_fence_after();
+          const uint32_t ocol = lane_base + kOCol + (it_cnt & 1) * kN;
+          uint32_t o[NR];
+          tmem_ld_rows<NR>(ocol, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int r = 0; r < NR; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+          tmem_st_rows<NR>(ocol, o);
+          tmem_wait_st();
+        }
+        if (kbase + kKeys > mt.L) {
+          // keys at or past the sequence's end hold arbitrary bits: zero their V
+          // rows (after the tile has landed) so that 0 * V stays 0
+          if (!wait_all(&bars->v_full[st], (g / kStages) & 1, p.err)) break;
+          if (key >= mt.L) {
+            uint4* v0 = reinterpret_cast<uint4*>(smem + st * kStageBytes + kTileBytes + t * 128);
+            uint4* v1 = reinterpret_cast<uint4*>(smem + st * kStageBytes + kTileBytes + kHalf + t * 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) v0[c] = v1[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[b]);
+
+        if (!(flags & kMetaLast)) continue;
+        // ---- item end: row sums over the 128 key-threads, handed to the epilogue
+        float* reds = red + (b ^ 1) * 4 * NR;  // the other buffer of this tile pair
+        {
+          float c[NR];
+#pragma unroll
+          for (int r = 0; r < NR; ++r) c[r] = lsum[r];
+          const float wsum = xreduce<NR>(c, lane, AddOp());
+          if (row_writer) reds[q4 * NR + my_row] = wsum;
+        }
+        named_barrier(1, 128);
+        const int ob = it_cnt & 1;
+        if (!wait_all(&bars->ml_empty[ob], ((it_cnt >> 1) & 1) ^ 1, p.err)) break;
+        EpSlot& es = slots[ob];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          if (t == r) {
+            es.m[r] = m_ref[r];
+            es.l[r] = (reds[r] + reds[NR + r]) + (reds[2 * NR + r] + reds[3 * NR + r]);
+          }
+        }
+        if (t == 0) {
+          es.mt = mt;
+          es.done = 0;
+        }
+        named_barrier(1, 128);  // reds[] is rewritten two tiles from now; the slot is complete
+        mbar_arrive(&bars->ml_full[ob]);
+      }
+    } else {
+      // ---------------------------------------------------------- epilogue
+      const int d = t;
+      int* flag_last = reinterpret_cast<int*>(tmem_slot + 1);
+      for (int it_cnt = 0;; ++it_cnt) {
+        const int ob = it_cnt & 1;
+        if (!wait_all(&bars->ml_full[ob], (it_cnt >> 1) & 1, p.err)) break;
+        const EpSlot& es = slots[ob];
+        if (es.done) break;
+        const Meta mt = es.mt;
+        float mrow[NR], lrow[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          mrow[r] = es.m[r];
+          lrow[r] = r < mt.nrows ? es.l[r] : 1.f;
+        }
+        mbar_arrive(&bars->ml_empty[ob]);
+        if (!wait_all(&bars->o_full[ob], (it_cnt >> 1) & 1, p.err)) break;
+        tc_fence_after();
+        uint32_t o[NR];
+        tmem_ld_rows<NR>(lane_base + kOCol + ob * kN, o);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars->o_empty[ob]);
+        const int nr = mt.nrows;
+        if (mt.part < 0) {
+#pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            if (r < nr) {
+              const int row = mt.row0 + r;
+              const int tok = row / p.G, gh = row - tok * p.G;
+              __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                    ((int64_t)(mt.qstart + tok) * p.Hq + (int64_t)mt.kvh * p.G + gh) * 128;
+              orow[d] = __float2bfloat16_rn(__uint_as_float(o[r]) / lrow[r]);
+            }
+          }
+          continue;
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          if (r < nr) {
+            p.part_acc[(int64_t)(mt.part + r) * 128 + d] = __uint_as_float(o[r]);
+            if (d == r) p.part_ml[mt.part + r] = make_float2(mrow[r], lrow[r]);
+          }
+        }
+        // The split that completes its merge group combines the group's
+        // partial rows: m = max m_p, l = sum l_p 2^(m_p - m), O = sum acc_p 2^(m_p - m) / l.
+        // Release: the barrier orders every thread's partial writes before
+        // thread 0's fence and ticket; acquire: thread 0's fence after the
+        // ticket, then the barrier, before anyone reads other splits' rows.
+        named_barrier(2, 128);
+        if (d == 0) {
+          __threadfence();
+          *flag_last = atomicAdd(p.tickets + mt.grp, 1);
+        }
+        named_barrier(2, 128);
+        const MergeGroup gr = p.groups[mt.grp];
+        if (*flag_last == gr.nsplit - 1) {
+          if (d == 0) __threadfence();
+          named_barrier(2, 128);
+#pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            if (r < gr.nrows) {
+              float M = -CUDART_INF_F;
+#pragma unroll 8
+              for (int sp = 0; sp < gr.nsplit; ++sp)
+                M = fmaxf(M, __ldcg(&p.part_ml[gr.part_base + sp * gr.nrows + r]).x);
+              const float Mu = M == -CUDART_INF_F ? 0.f : M;
+              float lt = 0.f, acc = 0.f;
+#pragma unroll 8
+              for (int sp = 0; sp < gr.nsplit; ++sp) {
+                const int slot = gr.part_base + sp * gr.nrows + r;
+                const float2 ml = __ldcg(&p.part_ml[slot]);
+                const float wt = fast_exp2(ml.x - Mu);
+                lt = fmaf(wt, ml.y, lt);
+                acc = fmaf(wt, __ldcg(&p.part_acc[(int64_t)slot * 128 + d]), acc);
+              }
+              const int row = gr.row0 + r;
+              const int tok = row / p.G, gh = row - tok * p.G;
+              __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                    ((int64_t)(mt.qstart + tok) * p.Hq + (int64_t)gr.kvh * p.G + gh) * 128;
+              orow[d] = __float2bfloat16_rn(acc / lt);
+            }
+          }
+        }
+        named_barrier(2, 128);  // the flag is rewritten by the next split item
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int NR>
+cudaError_t launch_dectc_t(const AttnParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, int grid, cudaStream_t s) {
+  static unsigned long long done_mask = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+    e = cudaFuncSetAttribute(dectc_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    __atomic_fetch_or(&done_mask, 1ull << dev, __ATOMIC_RELEASE);
+  }
+  e = launch_pdl(dectc_kernel<NR>, dim3(grid), dim3(kThreads), kSmem, s, p, qmap, kmap, vmap);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dectc(const AttnParams& p, int rows, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                         const CUtensorMap& vmap, int grid, cudaStream_t s) {
+  if (rows <= 4) return launch_dectc_t<4>(p, qmap, kmap, vmap, grid, s);
+  if (rows <= 8) return launch_dectc_t<8>(p, qmap, kmap, vmap, grid, s);
+  return launch_dectc_t<16>(p, qmap, kmap, vmap, grid, s);
+}
+
+}  // namespace pkv

@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(256) kv_write_vec(const uint8_t* __restrict__ 
                                                     const int64_t* __restrict__ slots, uint8_t* kc, uint8_t* vc,
                                                     int64_t T, int64_t num_slots, int row_chunks,
                                                     int64_t k_stride_b, int64_t v_stride_b, int* err) {
+  pdl_launch_dependents();  // a following planner reads nothing this kernel writes
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {

@@ -29,16 +29,16 @@
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "pkv_tc.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA issuer, 8 softmax warps (two per row quarter)
 constexpr int kStages = 2;
 constexpr int kTileBytes = kMmaTileKeys * 128 * 2;  // 128 keys x 128 dims x bf16 = 32 KB
 constexpr int kQBytes = kMmaRows * 128 * 2;          // 32 KB
 constexpr int kPBytes = kMmaRows * kMmaTileKeys * 2;  // 32 KB
-constexpr int kHalf = 128 * 128;                      // one 64-column half of a 128-row tile (16 KB)
 // shared-memory carve-up (offsets from a 1024-byte aligned base)
 constexpr int kQOff = 0;
 constexpr int kKOff = kQOff + kQBytes;
@@ -46,96 +46,16 @@ constexpr int kVOff = kKOff + kStages * kTileBytes;
 constexpr int kPOff = kVOff + kStages * kTileBytes;
 constexpr int kBarOff = kPOff + 2 * kPBytes;
 constexpr int kNumBars = 2 + 3 * kStages + 2 * 4 + 2;
-constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
+constexpr int kRedOff = kBarOff + kNumBars * 8 + 16;  // [2 tiles][2 halves][128 rows] row maxima / sums
+// No alignment slack: the buffers need a 1024-byte aligned base, which the
+// dynamic shared memory of a kernel without static shared memory has; the
+// kernel checks and refuses to run otherwise.
+constexpr int kSmem = kRedOff + 2 * 2 * 128 * 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// ---------------------------------------------------------------------------
-// tcgen05 / TMEM wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// D[tmem] (+)= A[smem] * B[smem], bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive on `bar` once every MMA issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-#define PKV_R32(i) "=r"(v[i])
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : PKV_R32(0), PKV_R32(1), PKV_R32(2), PKV_R32(3), PKV_R32(4), PKV_R32(5), PKV_R32(6), PKV_R32(7), PKV_R32(8),
-        PKV_R32(9), PKV_R32(10), PKV_R32(11), PKV_R32(12), PKV_R32(13), PKV_R32(14), PKV_R32(15), PKV_R32(16),
-        PKV_R32(17), PKV_R32(18), PKV_R32(19), PKV_R32(20), PKV_R32(21), PKV_R32(22), PKV_R32(23), PKV_R32(24),
-        PKV_R32(25), PKV_R32(26), PKV_R32(27), PKV_R32(28), PKV_R32(29), PKV_R32(30), PKV_R32(31)
-      : "r"(taddr));
-}
-#undef PKV_R32
-#define PKV_W32(i) "r"(v[i])
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      PKV_W32(0), PKV_W32(1), PKV_W32(2), PKV_W32(3), PKV_W32(4), PKV_W32(5), PKV_W32(6), PKV_W32(7), PKV_W32(8),
-      PKV_W32(9), PKV_W32(10), PKV_W32(11), PKV_W32(12), PKV_W32(13), PKV_W32(14), PKV_W32(15), PKV_W32(16),
-      PKV_W32(17), PKV_W32(18), PKV_W32(19), PKV_W32(20), PKV_W32(21), PKV_W32(22), PKV_W32(23), PKV_W32(24),
-      PKV_W32(25), PKV_W32(26), PKV_W32(27), PKV_W32(28), PKV_W32(29), PKV_W32(30), PKV_W32(31)
-      : "memory");
-}
-#undef PKV_W32
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptors (sm_100 format: start>>4 in [0,14), leading
-// byte offset>>4 in [16,30), stride byte offset>>4 in [32,46), version 1 at
-// [46,48), layout type at [61,64) with 2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-// K-major operand, 128-byte rows swizzled, 8-row groups 1024 bytes apart
-// (Q, K, P).  The leading byte offset is not used by this layout.
-__device__ __forceinline__ uint64_t desc_k(uint32_t saddr) { return smem_desc(saddr, 16, 1024); }
-// MN-major operand (V as the B of P.V): 64-element halves 16 KB apart
-// (leading byte offset), 8-key groups 1024 bytes apart (stride byte offset).
-__device__ __forceinline__ uint64_t desc_mn(uint32_t saddr) { return smem_desc(saddr, kHalf, 1024); }
-
-// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B bf16
-// (bits 7-9 and 10-12 = 1), B major-ness at bit 16, N>>3 at 17-22, M>>4 at 24-28.
-constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-constexpr uint32_t kIdescS = idesc_bf16(128, 128, false);
-constexpr uint32_t kIdescO = idesc_bf16(128, 128, true);
+constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescO = idesc_bf16(128, 128, false, true);
 
 struct Bars {
   uint64_t q_full, q_empty;
@@ -145,21 +65,19 @@ struct Bars {
 };
 static_assert(sizeof(Bars) == kNumBars * 8, "barrier block");
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
 
 __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams p,
                                                                const __grid_constant__ CUtensorMap qmap,
                                                                const __grid_constant__ CUtensorMap kmap,
                                                                const __grid_constant__ CUtensorMap vmap) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // uniform: every thread returns before any barrier
+    if (threadIdx.x == 0) raise_error(p.err, PKV_DEVERR_INTERNAL);
+    return;
+  }
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNumBars * 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_items = p.header->n_mma;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -171,12 +89,12 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_free[b], 128);
-      mbar_init(&bars->p_full[b], 128);
+      mbar_init(&bars->s_free[b], 256);
+      mbar_init(&bars->p_full[b], 256);
       mbar_init(&bars->pv_done[b], 1);
     }
     mbar_init(&bars->o_full, 1);
-    mbar_init(&bars->o_empty, 128);
+    mbar_init(&bars->o_empty, 256);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -186,6 +104,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // the plan and the K/V write are complete and visible from here on
+  const int n_items = p.header->n_mma;
   const uint32_t tmem = *tmem_slot;
   const uint32_t smem_base = smem_u32(smem);
 
@@ -314,9 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
     __syncwarp();
   } else {
     // ================================================================ softmax / epilogue
+    // Two threads per row: warps 2-5 take key columns 0-63 of every tile,
+    // warps 6-9 columns 64-127 (the same TMEM lanes); a pair exchanges row
+    // maxima (and, at the end, row sums) through shared memory.
     const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;  // row of the tile == TMEM lane
+    const int h = (warp - 2) >> 2;      // column half
+    const int r = q4 * 32 + lane;       // row of the tile == TMEM lane
+    const int pair_bar = 1 + q4;        // warps (w, w+4) of one row quarter
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+    float* red = reinterpret_cast<float*>(smem + kRedOff);
     int g = 0, it_cnt = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++it_cnt) {
@@ -332,59 +258,63 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       const int ntiles = (it.ke - it.kb + kMmaTileKeys - 1) / kMmaTileKeys;
       for (int j = 0; j < ntiles; ++j, ++g) {
         const int b = g & 1;
-        const int k0 = it.kb + j * kMmaTileKeys;
+        const int k0 = it.kb + j * kMmaTileKeys + 64 * h;  // first key of this thread's half
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[b], (g >> 1) & 1, p.err))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t sraw[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + b * 128 + c * 32, sraw + c * 32);
+        uint32_t sraw[64];
+        tmem_ld32(lane_base + b * 128 + 64 * h, sraw);
+        tmem_ld32(lane_base + b * 128 + 64 * h + 32, sraw + 32);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bars->s_free[b]);
-        // scale, mask, row max
-        const int nvis = vis - k0;  // keys c < nvis of this tile are visible
-        float mx = -CUDART_INF_F;
+        const int nvis = vis - k0;  // keys c < nvis of this half are visible
+        if (nvis < 64) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float s = c < nvis ? __uint_as_float(sraw[c]) * p.scale_log2 : -CUDART_INF_F;
-          sraw[c] = __float_as_uint(s);
-          mx = fmaxf(mx, s);
+          for (int c = 0; c < 64; ++c)
+            if (c >= nvis) sraw[c] = __float_as_uint(-CUDART_INF_F);
         }
+        float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+        for (int c = 0; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sraw[c]));
+        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        float* redm = red + b * 256;
+        redm[h * 128 + r] = mx;
+        named_barrier(pair_bar, 64);
+        mx = fmaxf(mx, redm[(h ^ 1) * 128 + r]) * p.scale_log2;
         float alpha = 1.f;
         bool rescale = false;
         if (mx > m_ref + kRescaleThreshold) {  // false while both are -inf
-          alpha = exp2f(m_ref - mx);           // 0 when m_ref is -inf
+          alpha = fast_exp2(m_ref - mx);       // 0 when m_ref is -inf
           rescale = j > 0 && m_ref != -CUDART_INF_F;
           m_ref = mx;
         }
-        const float m_use = m_ref == -CUDART_INF_F ? 0.f : m_ref;
+        const float neg_m = m_ref == -CUDART_INF_F ? 0.f : -m_ref;
         // P buffer b is free once the P.V that read it two tiles ago is done
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[b], ((g >> 1) & 1) ^ 1, p.err))) {
           ok = false;
           break;
         }
-        uint8_t* prow = smem + kPOff + b * kPBytes + r * 128;
-        float psum = 0.f;
+        uint8_t* prow = smem + kPOff + b * kPBytes + h * kHalf + r * 128;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {  // 16-byte chunks of 8 keys
+        for (int u = 0; u < 8; ++u) {  // 16-byte chunks of 8 keys
           float e[8];
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
-            e[t] = exp2f(__uint_as_float(sraw[u * 8 + t]) - m_use);
-            psum += e[t];
+            e[t] = fast_exp2(fmaf(__uint_as_float(sraw[u * 8 + t]), p.scale_log2, neg_m));
+            ps[t & 3] += e[t];
           }
           uint4 w;
           w.x = pack_bf16(e[0], e[1]);
           w.y = pack_bf16(e[2], e[3]);
           w.z = pack_bf16(e[4], e[5]);
           w.w = pack_bf16(e[6], e[7]);
-          const int half = u >> 3, cu = u & 7;
-          *reinterpret_cast<uint4*>(prow + half * kHalf + ((cu ^ (r & 7)) << 4)) = w;
+          *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) << 4)) = w;
         }
-        l = l * alpha + psum;
+        l = fmaf(l, alpha, (ps[0] + ps[1]) + (ps[2] + ps[3]));
         if (__any_sync(0xffffffffu, rescale)) {
           // O must hold every earlier tile's P.V before it is scaled; the TMEM
           // accesses are warp-wide, rows that keep their max scale by 1
@@ -395,28 +325,27 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           tc_fence_after();
           const float f = rescale ? alpha : 1.f;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
-            tmem_ld32(lane_base + 256 + c * 32, o);
+            tmem_ld32(lane_base + 256 + 64 * h + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
             for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * f);
-            tmem_st32(lane_base + 256 + c * 32, o);
+            tmem_st32(lane_base + 256 + 64 * h + c * 32, o);
           }
           tmem_wait_st();
         }
-        if (k0 + kMmaTileKeys > L) {
+        if (it.kb + j * kMmaTileKeys + kMmaTileKeys > L) {
           // keys at or past the sequence's end hold arbitrary bits: zero their V
-          // rows (after the tile has landed) so that 0 * V stays 0
+          // rows (this thread: key r of the tile, d-half h) so that 0 * V stays 0
           if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[b], (g >> 1) & 1, p.err))) {
             ok = false;
             break;
           }
-          if (k0 + r >= L) {
-            uint4* v0 = reinterpret_cast<uint4*>(smem + kVOff + b * kTileBytes + r * 128);
-            uint4* v1 = reinterpret_cast<uint4*>(smem + kVOff + b * kTileBytes + kHalf + r * 128);
+          if (it.kb + j * kMmaTileKeys + r >= L) {
+            uint4* v0 = reinterpret_cast<uint4*>(smem + kVOff + b * kTileBytes + h * kHalf + r * 128);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) v0[t] = v1[t] = make_uint4(0, 0, 0, 0);
+            for (int t = 0; t < 8; ++t) v0[t] = make_uint4(0, 0, 0, 0);
           }
         }
         fence_proxy_async_smem();
@@ -424,22 +353,29 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         mbar_arrive(&bars->p_full[b]);
       }
       if (!ok) break;
-      // ---- epilogue
+      // ---- epilogue: row sum of the pair, O (this half's 64 columns) / l
+      // row sums go through the max buffer the last tile did not use; the
+      // second pair barrier keeps the next tile from overwriting them early
+      float* reds = red + (g & 1) * 256;
+      reds[h * 128 + r] = l;
+      named_barrier(pair_bar, 64);
+      const float ltot = l + reds[(h ^ 1) * 128 + r];
+      named_barrier(pair_bar, 64);
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_full, it_cnt & 1, p.err))) break;
       tc_fence_after();
-      uint32_t o[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + 256 + c * 32, o + c * 32);
+      uint32_t o[64];
+      tmem_ld32(lane_base + 256 + 64 * h, o);
+      tmem_ld32(lane_base + 256 + 64 * h + 32, o + 32);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->o_empty);
       if (valid) {
         if (it.part < 0) {
-          const float inv = 1.f / l;
+          const float inv = 1.f / ltot;
           __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                ((int64_t)(qstart + tok) * p.Hq + (int64_t)it.kvh * p.G + gh) * 128;
+                                ((int64_t)(qstart + tok) * p.Hq + (int64_t)it.kvh * p.G + gh) * 128 + 64 * h;
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
+          for (int u = 0; u < 8; ++u) {
             uint4 w;
             w.x = pack_bf16(__uint_as_float(o[u * 8 + 0]) * inv, __uint_as_float(o[u * 8 + 1]) * inv);
             w.y = pack_bf16(__uint_as_float(o[u * 8 + 2]) * inv, __uint_as_float(o[u * 8 + 3]) * inv);
@@ -448,13 +384,64 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
             *reinterpret_cast<uint4*>(orow + u * 8) = w;
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(p.part_acc + (int64_t)(it.part + r) * 128);
+          float4* dst = reinterpret_cast<float4*>(p.part_acc + (int64_t)(it.part + r) * 128 + 64 * h);
 #pragma unroll
-          for (int u = 0; u < 32; ++u)
+          for (int u = 0; u < 16; ++u)
             dst[u] = make_float4(__uint_as_float(o[u * 4]), __uint_as_float(o[u * 4 + 1]),
                                  __uint_as_float(o[u * 4 + 2]), __uint_as_float(o[u * 4 + 3]));
-          p.part_ml[it.part + r] = make_float2(m_ref, l);
+          if (h == 0) p.part_ml[it.part + r] = make_float2(m_ref, ltot);
         }
+      }
+      if (it.part >= 0) {
+        // the split that completes its merge group combines the group's
+        // partial rows: m = max m_p, l = sum l_p 2^(m_p - m), O = sum acc_p 2^(m_p - m) / l
+        int* flag_last = reinterpret_cast<int*>(tmem_slot + 1);
+        __threadfence();
+        named_barrier(5, 256);
+        if (r == 0 && h == 0) *flag_last = atomicAdd(p.tickets + it.grp, 1);
+        named_barrier(5, 256);
+        const MergeGroup gr = p.groups[it.grp];
+        if (*flag_last == gr.nsplit - 1 && r < gr.nrows) {
+          __threadfence();
+          float M = -CUDART_INF_F;
+#pragma unroll 8
+          for (int sp = 0; sp < gr.nsplit; ++sp) M = fmaxf(M, __ldcg(&p.part_ml[gr.part_base + sp * gr.nrows + r]).x);
+          const float Mu = M == -CUDART_INF_F ? 0.f : M;
+          float lsum = 0.f;
+          float acc[64];
+#pragma unroll
+          for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+          for (int sp = 0; sp < gr.nsplit; ++sp) {
+            const int slot = gr.part_base + sp * gr.nrows + r;
+            const float2 ml = __ldcg(&p.part_ml[slot]);
+            const float wt = exp2f(ml.x - Mu);
+            lsum = fmaf(wt, ml.y, lsum);
+            const float4* src = reinterpret_cast<const float4*>(p.part_acc + (int64_t)slot * 128 + 64 * h);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const float4 a = __ldcg(src + u);
+              acc[4 * u] = fmaf(wt, a.x, acc[4 * u]);
+              acc[4 * u + 1] = fmaf(wt, a.y, acc[4 * u + 1]);
+              acc[4 * u + 2] = fmaf(wt, a.z, acc[4 * u + 2]);
+              acc[4 * u + 3] = fmaf(wt, a.w, acc[4 * u + 3]);
+            }
+          }
+          const float inv = 1.f / lsum;
+          const int grow = gr.row0 + r;
+          const int gtok = grow / p.G, ggh = grow - gtok * p.G;
+          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                ((int64_t)(qstart + gtok) * p.Hq + (int64_t)gr.kvh * p.G + ggh) * 128 + 64 * h;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint4 w;
+            w.x = pack_bf16(acc[u * 8 + 0] * inv, acc[u * 8 + 1] * inv);
+            w.y = pack_bf16(acc[u * 8 + 2] * inv, acc[u * 8 + 3] * inv);
+            w.z = pack_bf16(acc[u * 8 + 4] * inv, acc[u * 8 + 5] * inv);
+            w.w = pack_bf16(acc[u * 8 + 6] * inv, acc[u * 8 + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + u * 8) = w;
+          }
+        }
+        named_barrier(5, 256);
       }
     }
   }
@@ -479,8 +466,8 @@ cudaError_t launch_mma(const AttnParams& p, const CUtensorMap& qmap, const CUten
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, 1ull << dev, __ATOMIC_RELEASE);
   }
-  mma_attn_kernel<<<grid, kThreads, kSmem, s>>>(p, qmap, kmap, vmap);
-  return cudaGetLastError();
+  e = launch_pdl(mma_attn_kernel, dim3(grid), dim3(kThreads), kSmem, s, p, qmap, kmap, vmap);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace pkv

@@ -106,9 +106,27 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel in the stream (launched
+// with the programmatic-serialization attribute) start its prologue now, and
+// wait here until every prerequisite grid has completed and its memory
+// writes are visible (a no-op when launched without the attribute).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Named barrier over `nthreads` threads (whole warps) with id `id` (1..15).
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// 2^x with the hardware approximation (ex2.approx.ftz: relative error about
+// 2^-22; 2^-inf = 0), for softmax weights that are rounded to bf16 or
+// accumulated in fp32 afterwards.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ---------------------------------------------------------------------------

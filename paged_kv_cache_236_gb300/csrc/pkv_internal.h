@@ -8,11 +8,14 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace pkv {
 
 // Rows of one kv head of one sequence are (query token i, head-in-group g)
 // pairs, row = i * G + g.
 constexpr int kDecRows = 4;      // rows per CUDA-core work item
+constexpr int kTcDecRows = 16;   // rows per tensor-core decode item (the MMA's N)
 constexpr int kDecTileKeys = 64;  // keys per CUDA-core pipeline stage
 constexpr int kMmaRows = 128;     // rows per tensor-core work item (M of the MMA)
 constexpr int kMmaTileKeys = 128;  // keys per tensor-core pipeline stage
@@ -33,10 +36,11 @@ struct alignas(16) PlanHeader {
 
 // One unit of attention work: `nrows` rows of sequence `seq`, kv head `kvh`,
 // starting at row `row0`, over keys [kb, ke).  part < 0: normalise and write
-// the output rows; otherwise write partial (m, l, acc) rows part .. part+nrows-1.
+// the output rows; otherwise write partial (m, l, acc) rows part .. part+nrows-1
+// of merge group `grp`, and merge the group if this item finishes it last.
 struct alignas(16) WorkItem {
   int seq, kvh, row0, nrows;
-  int kb, ke, part, pad;
+  int kb, ke, part, grp;
 };
 
 // Split-KV merge: rows row0 .. row0+nrows-1 of (seq, kvh) have nsplit
@@ -47,7 +51,7 @@ struct alignas(16) MergeGroup {
 };
 
 struct WorkspaceLayout {
-  size_t header_off, dec_off, mma_off, merge_off, ml_off, acc_off, total;
+  size_t header_off, dec_off, mma_off, merge_off, ticket_off, ml_off, acc_off, total;
   int dec_cap, mma_cap, merge_cap, part_cap;
 };
 
@@ -66,7 +70,9 @@ struct PlanParams {
   int max_blocks;   // block table row length
   int causal;
   int mma_ok;       // tensor-core path available for this call
-  int dec_rows_max;  // rows <= this go to the CUDA-core path when mma_ok
+  int dec_rows_max;  // rows <= this go to the decode-shaped path when mma_ok
+  int dec_unit_rows;  // rows per decode-shaped item (4 CUDA-core, 16 tensor-core)
+  int dec_tile_keys;  // key tile of the decode-shaped kernel (splits are multiples)
   int target_dec, target_mma;  // desired item counts
   int min_chunk_dec, min_chunk_mma;
   int dec_cap, mma_cap, merge_cap, part_cap;
@@ -74,6 +80,7 @@ struct PlanParams {
   WorkItem* dec_items;
   WorkItem* mma_items;
   MergeGroup* merges;
+  int* tickets;     // one per merge group, zeroed
   void* out;        // rows of invalid sequences are zeroed
   int out_row_bytes;  // bytes of one token's output row (Hq * D * elem)
   int* err;
@@ -90,6 +97,8 @@ struct AttnParams {
   const WorkItem* items;
   float2* part_ml;   // (m, l) per partial row, m in log2 units
   float* part_acc;   // [part_rows][D]
+  const MergeGroup* groups;
+  int* tickets;      // arrivals per merge group
   int Hq, Hkv, G, D, bs, max_blocks;
   int64_t num_blocks;
   float scale_log2;  // scale * log2(e)
@@ -97,15 +106,24 @@ struct AttnParams {
   int* err;
 };
 
-struct MergeParams {
-  void* out;
-  const int32_t* query_start_loc;
-  const PlanHeader* header;
-  const MergeGroup* groups;
-  const float2* part_ml;
-  const float* part_acc;
-  int Hq, G, D;
-};
+// Launch with programmatic stream serialization (the kernel may start before
+// its predecessor in the stream finishes; it calls pdl_wait() before
+// touching what the predecessor produces).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // launchers (return cudaGetLastError after the launch)
 cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slots, void* kc, void* vc,
@@ -114,9 +132,11 @@ cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slots, 
 cudaError_t launch_planner(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           bool bf16, int grid, cudaStream_t s);
-cudaError_t launch_merge(const MergeParams& p, bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_mma(const AttnParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
                        const CUtensorMap& vmap, int grid, cudaStream_t s);
+// rows: the largest item row count (4, 8 or 16 rows of softmax per key)
+cudaError_t launch_dectc(const AttnParams& p, int rows, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                         const CUtensorMap& vmap, int grid, cudaStream_t s);
 
 // Sets the thread-local message pkv_last_error returns.
 void set_last_error(const char* msg);

@@ -156,3 +156,22 @@ def test_host_side_errors():
     assert e.value.status == 2
     with pytest.raises(ValueError):
         pkv.paged_attention_forward(q.cpu(), kc, kc, i32(1, 1), i32(1), i32(2), 0.1, True)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (16, 2), (32, 2)])
+@pytest.mark.parametrize("max_q", [1, 2])
+def test_decode_with_length_hint(hq, hkv, max_q):
+    """Decode-shaped batches (1-2 query tokens) with the host's max_query_len
+    hint, which selects the narrower per-key row counts (4, 8) of the
+    decode kernel; also a long context to exercise its split merge."""
+    g = np.random.Generator(np.random.PCG64(hq * 10 + hkv + max_q))
+    B = 7
+    L = np.concatenate([[5000], g.integers(1, 700, size=B - 1)])
+    n = np.minimum(L, g.integers(1, max_q, size=B, endpoint=True))
+    nb = int(np.sum((L + 15) // 16)) + 3
+    w = wl.build("hint", context_lens=L, q_lens=n, num_blocks=nb, block_size=16, num_q_heads=hq,
+                 num_kv_heads=hkv, head_dim=128, dtype="bf16", seed=hq + 3 * max_q, poison=True)
+    dw = DeviceWorkload(w)
+    out = dw.run_step(0, max_query_len=int(n.max()))
+    check_step(dw, out, what=f"hint {hq}/{hkv} q<={max_q}")
+    assert pkv.device_errors() == 0
