@@ -92,6 +92,16 @@ def mma_flops(w) -> float:
     return tot
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (x itself when world == 1)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def launches_per_step(w, max_q_len: int) -> int:
     """Our kernels per step: write, planner, [tensor-core kernel], CUDA-core kernel, merge."""
     g = w.num_q_heads // w.num_kv_heads
@@ -228,11 +238,7 @@ def run_gpu(args, rank, world, local_rank):
     if flags:
         raise SystemExit(f"device error word set: {flags:#x}")
     ab = algorithmic_bytes(w)
-    tot_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([tot_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        tot_ms = float(tt.item())
+    tot_ms = max_over_ranks(sum(step_ms), world, dev)
     value = ab["step"] * args.steps * world / (tot_ms * 1e-3) / 1e9
     kern_avg_ms = sum(kern_ms) / len(kern_ms)
     if args.workload == "prefill":
@@ -276,11 +282,7 @@ def run_gpu(args, rank, world, local_rank):
         b.synchronize()
         if it >= args.warmup:
             e2e_ms.append(a.elapsed_time(b))
-    e2e_tot = sum(e2e_ms)
-    if world > 1:
-        tt = torch.tensor([e2e_tot], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_tot = float(tt.item())
+    e2e_tot = max_over_ranks(sum(e2e_ms), world, dev)
     e2e_value = ab["step"] * args.steps * world / (e2e_tot * 1e-3) / 1e9
 
     result = {

@@ -1,26 +1,31 @@
 // Tensor-core paged attention for multi-token queries (prefill chunks,
 // speculative verification): tcgen05.mma with TMEM accumulators.
 //
-// What it computes is the same as the CUDA-core kernel ("Paged Attention
-// 基础", section 2, steps 1-5; causal mask at each query's absolute position
-// L - n + i, "ADR 004" Consequences: prefill and decode share one call), for
-// a work item of up to 128 rows (query token, head-in-group) of one sequence
-// and one kv head over keys [kb, ke):
-//   S = Q K^T (128 x 128 per key tile, fp32 in TMEM), online softmax in
-//   registers (one thread per row), P (bf16) -> shared memory, O += P V
-//   (fp32 in TMEM), O / l at the end (or a partial (m, l, O) row for split-KV).
+// What it computes is the same as the other attention kernels ("Paged
+// Attention 基础", section 2, steps 1-5; causal mask at each query's absolute
+// position L - n + i; "ADR 004" Consequences: prefill and decode share one
+// call), for a work item of up to 128 rows (query token, head-in-group) of one
+// sequence and one kv head over keys [kb, ke):
+//   S = Q K^T (128 rows x 64 keys per tile, fp32 in TMEM), online softmax in
+//   registers, P (bf16) -> shared memory, O += P V (fp32 in TMEM), O / l at
+//   the end, or a partial (m, l, O) row for split-KV; the last split of a
+//   merge group to finish merges the group (atomic ticket, no waiting).
 //
-// Roles (192 threads, one CTA per SM, persistent over items):
+// Roles (320 threads, one CTA per SM, persistent over items):
 //   warp 0    TMA producer: the item's Q tile (3-D box {64, G heads, 128/G
-//             tokens} of q [T, Hq, D], two 64-column halves) and, per
-//             128-key tile, one {64, 1, block_size, 1} box per physical block
-//             and half of the pool [NB, bs, Hkv, D] for K and for V
-//             (128-byte swizzle, the layout the tensor core reads);
-//   warp 1    TMEM allocation and the single thread that issues the MMAs;
-//   warps 2-5 softmax / correction / epilogue, thread i of the 128 owning
-//             TMEM lane (row) 32*(warp%4) + i.
-// Shared memory: Q 32 KB, 2 stages of K+V (128 KB), 2 P buffers (64 KB).
-// TMEM: S double-buffered in columns [0,256), O in [256,384).
+//             tokens} of q [T, Hq, D], two 64-column halves) and, per 64-key
+//             tile, one {64, 1, block_size, 1} box per physical block and
+//             64-column half of the pool [NB, bs, Hkv, D] for K and for V
+//             (128-byte swizzle, the layout the tensor core reads); block ids
+//             are loaded one tile ahead;
+//   warp 1    TMEM allocation and the single thread issuing the MMAs; the
+//             P.V of tile g is issued after the S of tile g+1;
+//   warps 2-9 softmax / correction / epilogue: two threads per row (TMEM
+//             lane), warps 2-5 on key columns 0-31 of a tile, warps 6-9 on
+//             32-63; a pair exchanges row maxima (and at the end row sums)
+//             through shared memory.
+// Shared memory: Q 32 KB, a 5-stage ring of K+V tiles (160 KB), 2 P buffers
+// (32 KB).  TMEM: S double-buffered in columns [0,128), O in [128,256).
 //
 // The running max used for the exponentials is only raised when a tile's row
 // maximum exceeds it by more than 8 (log2 units), so O is rescaled in TMEM
@@ -34,16 +39,18 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 320;  // producer, MMA issuer, 8 softmax warps (two per row quarter)
-constexpr int kStages = 2;
-constexpr int kTileBytes = kMmaTileKeys * 128 * 2;  // 128 keys x 128 dims x bf16 = 32 KB
-constexpr int kQBytes = kMmaRows * 128 * 2;          // 32 KB
-constexpr int kPBytes = kMmaRows * kMmaTileKeys * 2;  // 32 KB
+constexpr int kThreads = 320;
+constexpr int kKeys = 64;                           // keys per tile
+constexpr int kStages = 5;
+constexpr int kHalfKV = kKeys * 128;                // one 64-column half of a K or V tile (8 KB)
+constexpr int kTileBytes = 2 * kHalfKV;             // K or V tile: 16 KB
+constexpr int kStageBytes = 2 * kTileBytes;         // K + V: 32 KB
+constexpr int kQBytes = kMmaRows * 128 * 2;         // 32 KB (two 16 KB halves)
+constexpr int kPBytes = kMmaRows * kKeys * 2;       // 16 KB
 // shared-memory carve-up (offsets from a 1024-byte aligned base)
 constexpr int kQOff = 0;
-constexpr int kKOff = kQOff + kQBytes;
-constexpr int kVOff = kKOff + kStages * kTileBytes;
-constexpr int kPOff = kVOff + kStages * kTileBytes;
+constexpr int kSOff = kQOff + kQBytes;              // stages: K tile then V tile
+constexpr int kPOff = kSOff + kStages * kStageBytes;
 constexpr int kBarOff = kPOff + 2 * kPBytes;
 constexpr int kNumBars = 2 + 3 * kStages + 2 * 4 + 2;
 constexpr int kRedOff = kBarOff + kNumBars * 8 + 16;  // [2 tiles][2 halves][128 rows] row maxima / sums
@@ -51,11 +58,16 @@ constexpr int kRedOff = kBarOff + kNumBars * 8 + 16;  // [2 tiles][2 halves][128
 // dynamic shared memory of a kernel without static shared memory has; the
 // kernel checks and refuses to run otherwise.
 constexpr int kSmem = kRedOff + 2 * 2 * 128 * 4;
-constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kSCol = 0, kOCol = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescS = idesc_bf16(128, kKeys, false, false);
 constexpr uint32_t kIdescO = idesc_bf16(128, 128, false, true);
+
+// V as the B of P.V (MN-major): the two 64-column halves are kHalfKV apart,
+// 8-key groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_v(uint32_t saddr) { return smem_desc(saddr, kHalfKV, 1024); }
 
 struct Bars {
   uint64_t q_full, q_empty;
@@ -64,7 +76,7 @@ struct Bars {
   uint64_t o_full, o_empty;
 };
 static_assert(sizeof(Bars) == kNumBars * 8, "barrier block");
-
+static_assert(kSmem <= 232448, "shared memory");
 
 __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams p,
                                                                const __grid_constant__ CUtensorMap qmap,
@@ -109,10 +121,9 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
   const uint32_t tmem = *tmem_slot;
   const uint32_t smem_base = smem_u32(smem);
 
-  // One counter g numbers the key tiles this CTA processes (across items);
-  // stage, S buffer and P buffer of tile g are all g & 1, and the phase
-  // parity of its barriers is (g >> 1) & 1.
-  static_assert(kStages == 2, "stage, S buffer and P buffer share one index");
+  // One counter g numbers the key tiles this CTA processes (across items):
+  // ring stage g % kStages (parity (g / kStages) & 1), S and P buffer g & 1
+  // (parity (g >> 1) & 1).
   if (warp == 0) {
     // ================================================================ producer
     if (lane == 0) {
@@ -120,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
     }
-    const int nb = kMmaTileKeys / p.bs;
+    const int nb = kKeys / p.bs;
     int g = 0, it_cnt = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++it_cnt) {
@@ -129,6 +140,19 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       const int qstart = p.query_start_loc[it.seq];
       const int nblk = (L + p.bs - 1) / p.bs;
       const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
+      auto block_of = [&](int kbase) -> int {  // physical block of this lane's block in the tile
+        const int lb = kbase / p.bs + lane;
+        int phys = (int)p.num_blocks;  // out of range: reads as zeros
+        if (lane < nb && lb < nblk) {
+          const int b = __ldg(bt + lb);
+          if (b >= 0 && (int64_t)b < p.num_blocks)
+            phys = b;
+          else
+            raise_error(p.err, PKV_DEVERR_BLOCK_OUT_OF_RANGE);
+        }
+        return phys;
+      };
+      int phys = block_of(it.kb);
       // Q tile: reusable once the previous item's last S MMA has completed
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_empty, (it_cnt & 1) ^ 1, p.err))) break;
       if (lane == 0) {
@@ -137,9 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         tma_load_3d(smem + kQOff, &qmap, &bars->q_full, 0, it.kvh * p.G, tok0);
         tma_load_3d(smem + kQOff + kHalf, &qmap, &bars->q_full, 64, it.kvh * p.G, tok0);
       }
-      for (int kbase = it.kb; kbase < it.ke; kbase += kMmaTileKeys, ++g) {
-        const int st = g & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->kv_empty[st], ((g >> 1) & 1) ^ 1, p.err))) {
+      for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
+        const int st = g % kStages;
+        const int next_phys = (kbase + kKeys < it.ke) ? block_of(kbase + kKeys) : 0;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->kv_empty[st], ((g / kStages) & 1) ^ 1, p.err))) {
           ok = false;
           break;
         }
@@ -149,23 +174,15 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         }
         __syncwarp();
         if (lane < nb) {
-          const int lb = kbase / p.bs + lane;
-          int phys = (int)p.num_blocks;  // out of range: reads as zeros
-          if (lb < nblk) {
-            const int b = bt[lb];
-            if (b >= 0 && (int64_t)b < p.num_blocks)
-              phys = b;
-            else
-              raise_error(p.err, PKV_DEVERR_BLOCK_OUT_OF_RANGE);
-          }
           const int row_off = lane * p.bs * 128;
-          uint8_t* kd = smem + kKOff + st * kTileBytes + row_off;
-          uint8_t* vd = smem + kVOff + st * kTileBytes + row_off;
+          uint8_t* kd = smem + kSOff + st * kStageBytes + row_off;
+          uint8_t* vd = kd + kTileBytes;
           tma_load_4d(kd, &kmap, &bars->k_full[st], 0, it.kvh, 0, phys);
-          tma_load_4d(kd + kHalf, &kmap, &bars->k_full[st], 64, it.kvh, 0, phys);
+          tma_load_4d(kd + kHalfKV, &kmap, &bars->k_full[st], 64, it.kvh, 0, phys);
           tma_load_4d(vd, &vmap, &bars->v_full[st], 0, it.kvh, 0, phys);
-          tma_load_4d(vd + kHalf, &vmap, &bars->v_full[st], 64, it.kvh, 0, phys);
+          tma_load_4d(vd + kHalfKV, &vmap, &bars->v_full[st], 64, it.kvh, 0, phys);
         }
+        phys = next_phys;
       }
     }
   } else if (warp == 1) {
@@ -175,52 +192,47 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       bool ok = true;
       // O (+)= P V for tile gp; `first` starts the item's accumulation.
       auto issue_pv = [&](int gp, bool first) -> bool {
-        const int b = gp & 1;
+        const int b = gp & 1, st = gp % kStages;
         if (!mbar_wait(&bars->p_full[b], (gp >> 1) & 1, p.err)) return false;
-        if (!mbar_wait(&bars->v_full[b], (gp >> 1) & 1, p.err)) return false;
+        if (!mbar_wait(&bars->v_full[st], (gp / kStages) & 1, p.err)) return false;
         tc_fence_after();
         const uint32_t pbase = smem_base + kPOff + b * kPBytes;
-        const uint32_t vbase = smem_base + kVOff + b * kTileBytes;
+        const uint32_t vbase = smem_base + kSOff + st * kStageBytes + kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kMmaTileKeys / 16; ++kk) {
-          const uint64_t a = desc_k(pbase + (kk >> 2) * kHalf + (kk & 3) * 32);
-          const uint64_t bd = desc_mn(vbase + kk * 2048);
-          umma_bf16(tmem + 256, a, bd, kIdescO, (first && kk == 0) ? 0u : 1u);
-        }
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          umma_bf16(tmem + kOCol, desc_k(pbase + kk * 32), desc_v(vbase + kk * 2048), kIdescO,
+                    (first && kk == 0) ? 0u : 1u);
         umma_commit(&bars->pv_done[b]);
-        umma_commit(&bars->kv_empty[b]);
+        umma_commit(&bars->kv_empty[st]);
         return true;
       };
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++it_cnt) {
         const WorkItem it = p.items[idx];
         if (!mbar_wait(&bars->q_full, it_cnt & 1, p.err)) break;
-        const int ntiles = (it.ke - it.kb + kMmaTileKeys - 1) / kMmaTileKeys;
+        const int ntiles = (it.ke - it.kb + kKeys - 1) / kKeys;
         for (int j = 0; j < ntiles; ++j, ++g) {
-          const int b = g & 1;
-          if (!mbar_wait(&bars->k_full[b], (g >> 1) & 1, p.err) ||
+          const int b = g & 1, st = g % kStages;
+          if (!mbar_wait(&bars->k_full[st], (g / kStages) & 1, p.err) ||
               !mbar_wait(&bars->s_free[b], ((g >> 1) & 1) ^ 1, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t qbase = smem_base + kQOff;
-          const uint32_t kbase = smem_base + kKOff + b * kTileBytes;
+          const uint32_t kbase = smem_base + kSOff + st * kStageBytes;
 #pragma unroll
-          for (int kk = 0; kk < 128 / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            umma_bf16(tmem + b * 128, desc_k(qbase + off), desc_k(kbase + off), kIdescS, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 128 / 16; ++kk)
+            umma_bf16(tmem + kSCol + b * kKeys, desc_k(qbase + (kk >> 2) * kHalf + (kk & 3) * 32),
+                      desc_k(kbase + (kk >> 2) * kHalfKV + (kk & 3) * 32), kIdescS, kk > 0 ? 1u : 0u);
           umma_commit(&bars->s_full[b]);
           if (j == ntiles - 1) umma_commit(&bars->q_empty);  // Q no longer read by this item
           if (j == 0 && it_cnt > 0) {
             // O is about to be overwritten: the previous item's epilogue must have read it
-            if (!mbar_wait(&bars->o_empty, ((it_cnt - 1) & 1), p.err)) {
+            if (!mbar_wait(&bars->o_empty, (it_cnt - 1) & 1, p.err)) {
               ok = false;
               break;
             }
           }
-          // P.V of the previous tile goes after this tile's S so that the
-          // softmax of this tile overlaps the tensor core
           if (j > 0 && !issue_pv(g - 1, j == 1)) {
             ok = false;
             break;
@@ -234,13 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
     __syncwarp();
   } else {
     // ================================================================ softmax / epilogue
-    // Two threads per row: warps 2-5 take key columns 0-63 of every tile,
-    // warps 6-9 columns 64-127 (the same TMEM lanes); a pair exchanges row
-    // maxima (and, at the end, row sums) through shared memory.
     const int q4 = warp & 3;
-    const int h = (warp - 2) >> 2;      // column half
-    const int r = q4 * 32 + lane;       // row of the tile == TMEM lane
-    const int pair_bar = 1 + q4;        // warps (w, w+4) of one row quarter
+    const int h = (warp - 2) >> 2;  // key half of a tile (columns 32h .. 32h+31); output half 64h .. 64h+63
+    const int r = q4 * 32 + lane;   // row of the tile == TMEM lane
+    const int pair_bar = 1 + q4;    // warps (w, w+4) of one row quarter
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
     float* red = reinterpret_cast<float*>(smem + kRedOff);
     int g = 0, it_cnt = 0;
@@ -255,30 +264,29 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       const int tok = row / p.G, gh = row - tok * p.G;
       const int vis = valid ? min(it.ke, p.causal ? L - n + tok + 1 : L) : 0;
       float m_ref = -CUDART_INF_F, l = 0.f;
-      const int ntiles = (it.ke - it.kb + kMmaTileKeys - 1) / kMmaTileKeys;
+      const int ntiles = (it.ke - it.kb + kKeys - 1) / kKeys;
       for (int j = 0; j < ntiles; ++j, ++g) {
-        const int b = g & 1;
-        const int k0 = it.kb + j * kMmaTileKeys + 64 * h;  // first key of this thread's half
+        const int b = g & 1, st = g % kStages;
+        const int kt = it.kb + j * kKeys;  // first key of the tile
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[b], (g >> 1) & 1, p.err))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t sraw[64];
-        tmem_ld32(lane_base + b * 128 + 64 * h, sraw);
-        tmem_ld32(lane_base + b * 128 + 64 * h + 32, sraw + 32);
+        uint32_t sraw[32];
+        tmem_ld32(lane_base + kSCol + b * kKeys + 32 * h, sraw);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bars->s_free[b]);
-        const int nvis = vis - k0;  // keys c < nvis of this half are visible
-        if (nvis < 64) {
+        const int nvis = vis - (kt + 32 * h);  // keys c < nvis of this half are visible
+        if (nvis < 32) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
+          for (int c = 0; c < 32; ++c)
             if (c >= nvis) sraw[c] = __float_as_uint(-CUDART_INF_F);
         }
         float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-        for (int c = 0; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sraw[c]));
+        for (int c = 0; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sraw[c]));
         float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         float* redm = red + b * 256;
         redm[h * 128 + r] = mx;
@@ -297,10 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           ok = false;
           break;
         }
-        uint8_t* prow = smem + kPOff + b * kPBytes + h * kHalf + r * 128;
+        uint8_t* prow = smem + kPOff + b * kPBytes + r * 128;
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {  // 16-byte chunks of 8 keys
+        for (int u = 0; u < 4; ++u) {  // 16-byte chunks of 8 keys: chunk 4h + u of the row
           float e[8];
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
@@ -312,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           w.y = pack_bf16(e[2], e[3]);
           w.z = pack_bf16(e[4], e[5]);
           w.w = pack_bf16(e[6], e[7]);
-          *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) << 4)) = w;
+          *reinterpret_cast<uint4*>(prow + (((4 * h + u) ^ (r & 7)) << 4)) = w;
         }
         l = fmaf(l, alpha, (ps[0] + ps[1]) + (ps[2] + ps[3]));
         if (__any_sync(0xffffffffu, rescale)) {
@@ -327,23 +335,24 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
-            tmem_ld32(lane_base + 256 + 64 * h + c * 32, o);
+            tmem_ld32(lane_base + kOCol + 64 * h + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
             for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * f);
-            tmem_st32(lane_base + 256 + 64 * h + c * 32, o);
+            tmem_st32(lane_base + kOCol + 64 * h + c * 32, o);
           }
           tmem_wait_st();
         }
-        if (it.kb + j * kMmaTileKeys + kMmaTileKeys > L) {
+        if (kt + kKeys > L) {
           // keys at or past the sequence's end hold arbitrary bits: zero their V
-          // rows (this thread: key r of the tile, d-half h) so that 0 * V stays 0
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[b], (g >> 1) & 1, p.err))) {
+          // rows (thread: key r of the tile, d-half h) so that 0 * V stays 0
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (g / kStages) & 1, p.err))) {
             ok = false;
             break;
           }
-          if (it.kb + j * kMmaTileKeys + r >= L) {
-            uint4* v0 = reinterpret_cast<uint4*>(smem + kVOff + b * kTileBytes + h * kHalf + r * 128);
+          if (r < kKeys && kt + r >= L) {
+            uint4* v0 =
+                reinterpret_cast<uint4*>(smem + kSOff + st * kStageBytes + kTileBytes + h * kHalfKV + r * 128);
 #pragma unroll
             for (int t = 0; t < 8; ++t) v0[t] = make_uint4(0, 0, 0, 0);
           }
@@ -353,9 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         mbar_arrive(&bars->p_full[b]);
       }
       if (!ok) break;
-      // ---- epilogue: row sum of the pair, O (this half's 64 columns) / l
-      // row sums go through the max buffer the last tile did not use; the
-      // second pair barrier keeps the next tile from overwriting them early
+      // ---- epilogue: row sum of the pair, O (this thread's 64 output columns) / l.
+      // The sums go through the max buffer the last tile did not use; the
+      // second pair barrier keeps the next tile from overwriting them early.
       float* reds = red + (g & 1) * 256;
       reds[h * 128 + r] = l;
       named_barrier(pair_bar, 64);
@@ -364,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_full, it_cnt & 1, p.err))) break;
       tc_fence_after();
       uint32_t o[64];
-      tmem_ld32(lane_base + 256 + 64 * h, o);
-      tmem_ld32(lane_base + 256 + 64 * h + 32, o + 32);
+      tmem_ld32(lane_base + kOCol + 64 * h, o);
+      tmem_ld32(lane_base + kOCol + 64 * h + 32, o + 32);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->o_empty);
@@ -393,52 +402,60 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         }
       }
       if (it.part >= 0) {
-        // the split that completes its merge group combines the group's
-        // partial rows: m = max m_p, l = sum l_p 2^(m_p - m), O = sum acc_p 2^(m_p - m) / l
+        // The split that completes its merge group combines the group's
+        // partial rows: m = max m_p, l = sum l_p 2^(m_p - m), O = sum acc_p 2^(m_p - m) / l.
+        // Release: the barrier orders every thread's partial writes before one
+        // thread's fence and ticket; acquire: that thread's fence, then the barrier.
         int* flag_last = reinterpret_cast<int*>(tmem_slot + 1);
-        __threadfence();
         named_barrier(5, 256);
-        if (r == 0 && h == 0) *flag_last = atomicAdd(p.tickets + it.grp, 1);
+        if (r == 0 && h == 0) {
+          __threadfence();
+          *flag_last = atomicAdd(p.tickets + it.grp, 1);
+        }
         named_barrier(5, 256);
         const MergeGroup gr = p.groups[it.grp];
-        if (*flag_last == gr.nsplit - 1 && r < gr.nrows) {
-          __threadfence();
-          float M = -CUDART_INF_F;
+        if (*flag_last == gr.nsplit - 1) {
+          if (r == 0 && h == 0) __threadfence();
+          named_barrier(5, 256);
+          if (r < gr.nrows) {
+            float M = -CUDART_INF_F;
 #pragma unroll 8
-          for (int sp = 0; sp < gr.nsplit; ++sp) M = fmaxf(M, __ldcg(&p.part_ml[gr.part_base + sp * gr.nrows + r]).x);
-          const float Mu = M == -CUDART_INF_F ? 0.f : M;
-          float lsum = 0.f;
-          float acc[64];
+            for (int sp = 0; sp < gr.nsplit; ++sp)
+              M = fmaxf(M, __ldcg(&p.part_ml[gr.part_base + sp * gr.nrows + r]).x);
+            const float Mu = M == -CUDART_INF_F ? 0.f : M;
+            float lsum = 0.f;
+            float acc[64];
 #pragma unroll
-          for (int c = 0; c < 64; ++c) acc[c] = 0.f;
-          for (int sp = 0; sp < gr.nsplit; ++sp) {
-            const int slot = gr.part_base + sp * gr.nrows + r;
-            const float2 ml = __ldcg(&p.part_ml[slot]);
-            const float wt = exp2f(ml.x - Mu);
-            lsum = fmaf(wt, ml.y, lsum);
-            const float4* src = reinterpret_cast<const float4*>(p.part_acc + (int64_t)slot * 128 + 64 * h);
+            for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+            for (int sp = 0; sp < gr.nsplit; ++sp) {
+              const int slot = gr.part_base + sp * gr.nrows + r;
+              const float2 ml = __ldcg(&p.part_ml[slot]);
+              const float wt = fast_exp2(ml.x - Mu);
+              lsum = fmaf(wt, ml.y, lsum);
+              const float4* src = reinterpret_cast<const float4*>(p.part_acc + (int64_t)slot * 128 + 64 * h);
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const float4 a = __ldcg(src + u);
-              acc[4 * u] = fmaf(wt, a.x, acc[4 * u]);
-              acc[4 * u + 1] = fmaf(wt, a.y, acc[4 * u + 1]);
-              acc[4 * u + 2] = fmaf(wt, a.z, acc[4 * u + 2]);
-              acc[4 * u + 3] = fmaf(wt, a.w, acc[4 * u + 3]);
+              for (int u = 0; u < 16; ++u) {
+                const float4 a = __ldcg(src + u);
+                acc[4 * u] = fmaf(wt, a.x, acc[4 * u]);
+                acc[4 * u + 1] = fmaf(wt, a.y, acc[4 * u + 1]);
+                acc[4 * u + 2] = fmaf(wt, a.z, acc[4 * u + 2]);
+                acc[4 * u + 3] = fmaf(wt, a.w, acc[4 * u + 3]);
+              }
             }
-          }
-          const float inv = 1.f / lsum;
-          const int grow = gr.row0 + r;
-          const int gtok = grow / p.G, ggh = grow - gtok * p.G;
-          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                ((int64_t)(qstart + gtok) * p.Hq + (int64_t)gr.kvh * p.G + ggh) * 128 + 64 * h;
+            const float inv = 1.f / lsum;
+            const int grow = gr.row0 + r;
+            const int gtok = grow / p.G, ggh = grow - gtok * p.G;
+            __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                  ((int64_t)(qstart + gtok) * p.Hq + (int64_t)gr.kvh * p.G + ggh) * 128 + 64 * h;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint4 w;
-            w.x = pack_bf16(acc[u * 8 + 0] * inv, acc[u * 8 + 1] * inv);
-            w.y = pack_bf16(acc[u * 8 + 2] * inv, acc[u * 8 + 3] * inv);
-            w.z = pack_bf16(acc[u * 8 + 4] * inv, acc[u * 8 + 5] * inv);
-            w.w = pack_bf16(acc[u * 8 + 6] * inv, acc[u * 8 + 7] * inv);
-            *reinterpret_cast<uint4*>(orow + u * 8) = w;
+            for (int u = 0; u < 8; ++u) {
+              uint4 w;
+              w.x = pack_bf16(acc[u * 8 + 0] * inv, acc[u * 8 + 1] * inv);
+              w.y = pack_bf16(acc[u * 8 + 2] * inv, acc[u * 8 + 3] * inv);
+              w.z = pack_bf16(acc[u * 8 + 4] * inv, acc[u * 8 + 5] * inv);
+              w.w = pack_bf16(acc[u * 8 + 6] * inv, acc[u * 8 + 7] * inv);
+              *reinterpret_cast<uint4*>(orow + u * 8) = w;
+            }
           }
         }
         named_barrier(5, 256);
