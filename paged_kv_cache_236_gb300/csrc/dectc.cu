@@ -282,6 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
     if (lane == 0) {
       int g = 0, it_cnt = -1;
       int pend = -1, pend_item = 0;  // tile whose P.V is still to be issued, and its item count
+      // descriptors of stage 0 / buffer 0; others are offsets of these
+      const uint64_t dk0 = desc_k(smem_base);
+      const uint64_t dv0 = desc_mn(smem_base + kTileBytes);
+      const uint64_t dq0 = desc_k(smem_base + kQOff);
+      const uint64_t dp0 = desc_k(smem_base + kPOff);
       bool pend_first = false, pend_last = false;
       auto issue_pv = [&]() -> bool {
         const int b = pend & 1, st = pend % kStages, ob = pend_item & 1;
@@ -292,14 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
         if (!mbar_wait(&bars->p_full[b], (pend >> 1) & 1, p.err)) return false;
         if (!mbar_wait(&bars->v_full[st], (pend / kStages) & 1, p.err)) return false;
         tc_fence_after();
-        const uint32_t vbase = smem_base + st * kStageBytes + kTileBytes;
-        const uint32_t pbase = smem_base + kPOff + b * 2 * kQHalf;
+        const uint64_t dv = desc_add(dv0, st * kStageBytes);
+        const uint64_t dp = desc_add(dp0, b * 2 * kQHalf);
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t a = desc_mn(vbase + kk * 2048);
-          const uint64_t bd = desc_k(pbase + (kk >> 2) * kQHalf + (kk & 3) * 32);
-          umma_bf16(tmem + kOCol + ob * kN, a, bd, kIdescO, (pend_first && kk == 0) ? 0u : 1u);
-        }
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          umma_bf16(tmem + kOCol + ob * kN, desc_add(dv, kk * 2048), desc_add(dp, (kk >> 2) * kQHalf + (kk & 3) * 32),
+                    kIdescO, (pend_first && kk == 0) ? 0u : 1u);
         umma_commit(&bars->pv_done[b]);
         umma_commit(&bars->kv_empty[st]);
         if (pend_last) umma_commit(&bars->o_full[ob]);
@@ -318,14 +321,12 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
         const int b = g & 1;
         if (!mbar_wait(&bars->s_free[b], ((g >> 1) & 1) ^ 1, p.err)) break;
         tc_fence_after();
-        const uint32_t kbase = smem_base + st * kStageBytes;
-        const uint32_t qbase = smem_base + kQOff + (it_cnt & 1) * 2 * kQHalf;
+        const uint64_t dk = desc_add(dk0, st * kStageBytes);
+        const uint64_t dq = desc_add(dq0, (it_cnt & 1) * 2 * kQHalf);
 #pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk) {
-          const uint64_t a = desc_k(kbase + (kk >> 2) * kHalf + (kk & 3) * 32);
-          const uint64_t bd = desc_k(qbase + (kk >> 2) * kQHalf + (kk & 3) * 32);
-          umma_bf16(tmem + kSCol + b * kN, a, bd, kIdescS, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 128 / 16; ++kk)
+          umma_bf16(tmem + kSCol + b * kN, desc_add(dk, (kk >> 2) * kHalf + (kk & 3) * 32),
+                    desc_add(dq, (kk >> 2) * kQHalf + (kk & 3) * 32), kIdescS, kk > 0 ? 1u : 0u);
         umma_commit(&bars->s_full[b]);
         if (pend >= 0 && !issue_pv()) break;
         pend = g;

@@ -120,6 +120,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   d |= (uint64_t)2 << 61;
   return d;
 }
+// A descriptor moved by `bytes` within its swizzle atom or to another tile:
+// only the start-address field changes (addresses stay below 256 KB, so the
+// 14-bit field never carries).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); }
+
 // K-major operand, 128-byte rows swizzled, 8-row groups 1024 bytes apart
 // (Q, K, P).  The leading byte offset is not used by this layout.
 __device__ __forceinline__ uint64_t desc_k(uint32_t saddr) { return smem_desc(saddr, 16, 1024); }
