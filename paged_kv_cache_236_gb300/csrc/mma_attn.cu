@@ -6,26 +6,41 @@
 // position L - n + i; "ADR 004" Consequences: prefill and decode share one
 // call), for a work item of up to 128 rows (query token, head-in-group) of one
 // sequence and one kv head over keys [kb, ke):
-//   S = Q K^T (128 rows x 64 keys per tile, fp32 in TMEM), online softmax in
-//   registers, P (bf16) -> shared memory, O += P V (fp32 in TMEM), O / l at
-//   the end, or a partial (m, l, O) row for split-KV; the last split of a
-//   merge group to finish merges the group (atomic ticket, no waiting).
+//   S = Q K^T (128 rows x 128 keys per tile, fp32 in TMEM), online softmax in
+//   registers, P (bf16) written to TMEM, O += P V (fp32 in TMEM; the tensor
+//   core reads P from TMEM and V from shared memory), O / l at the end, or a
+//   partial (m, l, O) row for split-KV; the last split of a merge group to
+//   finish merges the group (atomic ticket, no waiting).
 //
-// Roles (320 threads, one CTA per SM, persistent over items):
-//   warp 0    TMA producer: the item's Q tile (3-D box {64, G heads, 128/G
-//             tokens} of q [T, Hq, D], two 64-column halves) and, per 64-key
-//             tile, one {64, 1, block_size, 1} box per physical block and
-//             64-column half of the pool [NB, bs, Hkv, D] for K and for V
-//             (128-byte swizzle, the layout the tensor core reads); block ids
-//             are loaded one tile ahead;
-//   warp 1    TMEM allocation and the single thread issuing the MMAs; the
-//             P.V of tile g is issued after the S of tile g+1;
+// Tile shape and issue order follow the tensor pipe's behaviour on sm_103a:
+// an M=128 MMA with N=64 costs about as long as one with N=128, and a chain
+// of MMAs accumulating into one TMEM region runs at about two thirds of the
+// peak rate when nothing else is queued, near the peak when a second,
+// independent chain is queued beside it.  So a tile is 128 keys (N=128 for
+// Q K^T), and the MMA thread issues the P.V of tile t directly followed by
+// the Q K^T of tile t+2: two independent chains back to back, while the
+// softmax warps work on tile t+1.
+//
+// Roles (352 threads, one CTA per SM, persistent; items are taken from an
+// atomic counter in the planner's largest-first order, so SMs that run
+// slower take fewer):
+//   warp 0    item fetch, Q and K producer: publishes each item in a slot of
+//             shared memory with its Q tile (3-D box {64, G heads, 128/G
+//             tokens} of q [T, Hq, D], two 64-column halves), then per tile
+//             one {64, 1, block_size, 1} box of the pool [NB, bs, Hkv, D] per
+//             physical block and 64-column half (128-byte swizzle, the layout
+//             the tensor core reads); block ids are loaded a tile ahead;
+//   warp 1    TMEM allocation and the single thread issuing the MMAs;
 //   warps 2-9 softmax / correction / epilogue: two threads per row (TMEM
-//             lane), warps 2-5 on key columns 0-31 of a tile, warps 6-9 on
-//             32-63; a pair exchanges row maxima (and at the end row sums)
-//             through shared memory.
-// Shared memory: Q 32 KB, a 5-stage ring of K+V tiles (160 KB), 2 P buffers
-// (32 KB).  TMEM: S double-buffered in columns [0,128), O in [128,256).
+//             lane), warps 2-5 on key columns 0-63 of a tile, warps 6-9 on
+//             64-127; a pair exchanges row maxima (and at the end row sums)
+//             through shared memory;
+//   warp 10   V producer, the same boxes from the V pool.
+// Shared memory: 2 Q tiles (64 KB), a 2-stage ring of K tiles (64 KB) and a
+// 3-stage ring of V tiles (96 KB); K of a tile is released when its Q K^T is
+// done, V when its P.V is done, so each ring refills as early as it can.
+// TMEM (512 columns): S double-buffered in [0,256), P (32 columns of packed
+// bf16 per 64 keys) double-buffered in [256,384), O in [384,512).
 //
 // The running max used for the exponentials is only raised when a tile's row
 // maximum exceeds it by more than 8 (log2 units), so O is rescaled in TMEM
@@ -39,27 +54,28 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kKeys = 64;                           // keys per tile
-constexpr int kStages = 5;
-constexpr int kHalfKV = kKeys * 128;                // one 64-column half of a K or V tile (8 KB)
-constexpr int kTileBytes = 2 * kHalfKV;             // K or V tile: 16 KB
-constexpr int kStageBytes = 2 * kTileBytes;         // K + V: 32 KB
+constexpr int kThreads = 352;
+constexpr int kKeys = kMmaTileKeys;                 // 128 keys per tile
+constexpr int kKStages = 2, kVStages = 3;
+constexpr int kHalfKV = kKeys * 128;                // one 64-column half of a K or V tile (16 KB)
+constexpr int kTileBytes = 2 * kHalfKV;             // K or V tile: 32 KB
 constexpr int kQBytes = kMmaRows * 128 * 2;         // 32 KB (two 16 KB halves)
-constexpr int kPBytes = kMmaRows * kKeys * 2;       // 16 KB
 // shared-memory carve-up (offsets from a 1024-byte aligned base)
 constexpr int kQOff = 0;
-constexpr int kSOff = kQOff + kQBytes;              // stages: K tile then V tile
-constexpr int kPOff = kSOff + kStages * kStageBytes;
-constexpr int kBarOff = kPOff + 2 * kPBytes;
-constexpr int kNumBars = 2 + 3 * kStages + 2 * 4 + 2;
-constexpr int kRedOff = kBarOff + kNumBars * 8 + 16;  // [2 tiles][2 halves][128 rows] row maxima / sums
+constexpr int kKOff = kQOff + 2 * kQBytes;
+constexpr int kVOff = kKOff + kKStages * kTileBytes;
+constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+constexpr int kNumBars = 6 + 2 * kKStages + 2 * kVStages + 6 + 2;
+constexpr int kSlotOff = (kBarOff + kNumBars * 8 + 16 + 15) & ~15;  // 2 item slots
+constexpr int kRedOff = kSlotOff + 2 * 64;          // [2 tiles][2 halves][128 rows] row maxima / sums
 // No alignment slack: the buffers need a 1024-byte aligned base, which the
 // dynamic shared memory of a kernel without static shared memory has; the
 // kernel checks and refuses to run otherwise.
 constexpr int kSmem = kRedOff + 2 * 2 * 128 * 4;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kSCol = 0, kOCol = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSCol = 0;    // S buffer b at kSCol + 128 b
+constexpr uint32_t kPCol = 256;  // P buffer b at kPCol + 64 b
+constexpr uint32_t kOCol = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 constexpr uint32_t kIdescS = idesc_bf16(128, kKeys, false, false);
@@ -70,13 +86,28 @@ constexpr uint32_t kIdescO = idesc_bf16(128, 128, false, true);
 __device__ __forceinline__ uint64_t desc_v(uint32_t saddr) { return smem_desc(saddr, kHalfKV, 1024); }
 
 struct Bars {
-  uint64_t q_full, q_empty;
-  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  uint64_t q_full[2], q_empty[2], slot_free[2];
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t o_full, o_empty;
 };
+
+// An item's description, published by the item-fetching warp with its Q tile.
+struct alignas(16) ItemSlot {
+  WorkItem it;
+  int L, qstart, n, done;
+  int pad[4];
+};
+// readers of a slot: the 256 softmax threads, the MMA thread, the V producer
+constexpr int kSlotReaders = 256 + 1 + 1;
+
+static_assert(sizeof(ItemSlot) == 64, "item slot");
 static_assert(sizeof(Bars) == kNumBars * 8, "barrier block");
 static_assert(kSmem <= 232448, "shared memory");
+static_assert(kKOff % 1024 == 0 && kVOff % 1024 == 0 && kTileBytes % 1024 == 0 && kQBytes % 1024 == 0,
+              "swizzled tiles");
+static_assert(kBarOff % 8 == 0 && kSlotOff % alignof(ItemSlot) == 0 && kRedOff % 16 == 0, "alignment");
 
 __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams p,
                                                                const __grid_constant__ CUtensorMap qmap,
@@ -89,21 +120,25 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
   }
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNumBars * 8);
+  ItemSlot* slots = reinterpret_cast<ItemSlot*>(smem + kSlotOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
-    }
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->q_full[b], 1);
+      mbar_init(&bars->q_empty[b], 1);
+      mbar_init(&bars->slot_free[b], kSlotReaders);
       mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_free[b], 256);
       mbar_init(&bars->p_full[b], 256);
       mbar_init(&bars->pv_done[b], 1);
+    }
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_empty, 256);
@@ -121,64 +156,114 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
   const uint32_t tmem = *tmem_slot;
   const uint32_t smem_base = smem_u32(smem);
 
-  // One counter g numbers the key tiles this CTA processes (across items):
-  // ring stage g % kStages (parity (g / kStages) & 1), S and P buffer g & 1
-  // (parity (g >> 1) & 1).
+  // One counter g numbers the key tiles this CTA processes (across items): K
+  // stage g % 2 (parity (g / 2) & 1), V stage g % 3 (parity (g / 3) & 1), S
+  // and P buffer g % 2.  Item c of this CTA uses Q tile and slot c & 1
+  // (parity (c >> 1) & 1); O's phases count items.
+  const int nb = kKeys / p.bs;  // physical blocks per tile
+  // physical block of this lane's block in the tile of keys from kbase
+  auto block_of = [&](const int32_t* bt, int nblk, int kbase) -> int {
+    const int lb = kbase / p.bs + lane;
+    int phys = (int)p.num_blocks;  // out of range: reads as zeros
+    if (lane < nb && lb < nblk) {
+      const int b = __ldg(bt + lb);
+      if (b >= 0 && (int64_t)b < p.num_blocks)
+        phys = b;
+      else
+        raise_error(p.err, PKV_DEVERR_BLOCK_OUT_OF_RANGE);
+    }
+    return phys;
+  };
+
   if (warp == 0) {
-    // ================================================================ producer
+    // ================================================================ item fetch, Q and K
     if (lane == 0) {
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
-      prefetch_tensormap(&vmap);
     }
-    const int nb = kKeys / p.bs;
-    int g = 0, it_cnt = 0;
+    int g = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++it_cnt) {
+    int next = 0;
+    if (lane == 0) next = atomicAdd(p.counter, 1);
+    for (int c = 0; ok; ++c) {
+      const int idx = __shfl_sync(0xffffffffu, next, 0);
+      const int qb = c & 1;
+      // slot and Q tile qb: free once item c-2's last Q K^T has completed and
+      // every reader has taken its description
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_empty[qb], ((c >> 1) & 1) ^ 1, p.err) &&
+                                       mbar_wait(&bars->slot_free[qb], ((c >> 1) & 1) ^ 1, p.err)))
+        break;
+      if (idx >= n_items) {
+        if (lane == 0) {
+          slots[qb].done = 1;
+          mbar_arrive(&bars->q_full[qb]);
+        }
+        break;
+      }
       const WorkItem it = p.items[idx];
+      if (lane == 0) next = atomicAdd(p.counter, 1);  // consumed after this item's tiles
       const int L = p.context_lens[it.seq];
       const int qstart = p.query_start_loc[it.seq];
       const int nblk = (L + p.bs - 1) / p.bs;
       const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
-      auto block_of = [&](int kbase) -> int {  // physical block of this lane's block in the tile
-        const int lb = kbase / p.bs + lane;
-        int phys = (int)p.num_blocks;  // out of range: reads as zeros
-        if (lane < nb && lb < nblk) {
-          const int b = __ldg(bt + lb);
-          if (b >= 0 && (int64_t)b < p.num_blocks)
-            phys = b;
-          else
-            raise_error(p.err, PKV_DEVERR_BLOCK_OUT_OF_RANGE);
-        }
-        return phys;
-      };
-      int phys = block_of(it.kb);
-      // Q tile: reusable once the previous item's last S MMA has completed
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_empty, (it_cnt & 1) ^ 1, p.err))) break;
+      int phys = block_of(bt, nblk, it.kb);
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->q_full, kQBytes);
+        ItemSlot& sl = slots[qb];
+        sl.it = it;
+        sl.L = L;
+        sl.qstart = qstart;
+        sl.n = p.query_start_loc[it.seq + 1] - qstart;
+        sl.done = 0;
+        mbar_arrive_expect_tx(&bars->q_full[qb], kQBytes);
         const int tok0 = qstart + it.row0 / p.G;
-        tma_load_3d(smem + kQOff, &qmap, &bars->q_full, 0, it.kvh * p.G, tok0);
-        tma_load_3d(smem + kQOff + kHalf, &qmap, &bars->q_full, 64, it.kvh * p.G, tok0);
+        tma_load_3d(smem + kQOff + qb * kQBytes, &qmap, &bars->q_full[qb], 0, it.kvh * p.G, tok0);
+        tma_load_3d(smem + kQOff + qb * kQBytes + kHalf, &qmap, &bars->q_full[qb], 64, it.kvh * p.G, tok0);
       }
       for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
-        const int st = g % kStages;
-        const int next_phys = (kbase + kKeys < it.ke) ? block_of(kbase + kKeys) : 0;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->kv_empty[st], ((g / kStages) & 1) ^ 1, p.err))) {
+        const int st = g % kKStages;
+        const int next_phys = (kbase + kKeys < it.ke) ? block_of(bt, nblk, kbase + kKeys) : 0;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_empty[st], ((g / kKStages) & 1) ^ 1, p.err))) {
           ok = false;
           break;
         }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
-          mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-        }
+        if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
         __syncwarp();
         if (lane < nb) {
-          const int row_off = lane * p.bs * 128;
-          uint8_t* kd = smem + kSOff + st * kStageBytes + row_off;
-          uint8_t* vd = kd + kTileBytes;
+          uint8_t* kd = smem + kKOff + st * kTileBytes + lane * p.bs * 128;
           tma_load_4d(kd, &kmap, &bars->k_full[st], 0, it.kvh, 0, phys);
           tma_load_4d(kd + kHalfKV, &kmap, &bars->k_full[st], 64, it.kvh, 0, phys);
+        }
+        phys = next_phys;
+      }
+    }
+  } else if (warp == 10) {
+    // ================================================================ V
+    if (lane == 0) prefetch_tensormap(&vmap);
+    int g = 0;
+    bool ok = true;
+    for (int c = 0; ok; ++c) {
+      const int qb = c & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_full[qb], (c >> 1) & 1, p.err))) break;
+      const bool done = slots[qb].done != 0;
+      const WorkItem it = slots[qb].it;
+      const int L = slots[qb].L;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->slot_free[qb]);
+      if (done) break;
+      const int nblk = (L + p.bs - 1) / p.bs;
+      const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
+      int phys = block_of(bt, nblk, it.kb);
+      for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
+        const int st = g % kVStages;
+        const int next_phys = (kbase + kKeys < it.ke) ? block_of(bt, nblk, kbase + kKeys) : 0;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_empty[st], ((g / kVStages) & 1) ^ 1, p.err))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
+        __syncwarp();
+        if (lane < nb) {
+          uint8_t* vd = smem + kVOff + st * kTileBytes + lane * p.bs * 128;
           tma_load_4d(vd, &vmap, &bars->v_full[st], 0, it.kvh, 0, phys);
           tma_load_4d(vd + kHalfKV, &vmap, &bars->v_full[st], 64, it.kvh, 0, phys);
         }
@@ -188,77 +273,105 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     if (lane == 0) {
-      int g = 0, it_cnt = 0;
-      bool ok = true;
-      // O (+)= P V for tile gp; `first` starts the item's accumulation.
-      auto issue_pv = [&](int gp, bool first) -> bool {
-        const int b = gp & 1, st = gp % kStages;
-        if (!mbar_wait(&bars->p_full[b], (gp >> 1) & 1, p.err)) return false;
-        if (!mbar_wait(&bars->v_full[st], (gp / kStages) & 1, p.err)) return false;
+      // descriptors of stage 0 / buffer 0; others are offsets of these
+      const uint64_t dq = desc_k(smem_base + kQOff);
+      const uint64_t dk0 = desc_k(smem_base + kKOff);
+      const uint64_t dv0 = desc_v(smem_base + kVOff);
+      // Q K^T iterator (two tiles ahead) and P.V iterator over this CTA's tiles
+      int gs = 0, s_item = -1, s_j = 0, s_nt = 0;
+      bool s_done = false;
+      int gp = 0, p_item = 0, p_j = 0;
+      int ring_nt[4] = {0, 0, 0, 0};  // tile counts of the items between the two iterators
+      // S of the next tile; false on a timeout.  S buffer gs % 2 was last read
+      // by the softmax of tile gs-2, which finished reading it before it
+      // signalled P(gs-2) full, and P.V(gs-2) (issued only after that) precedes
+      // this call.
+      auto s_step = [&]() -> bool {
+        if (s_done) return true;
+        if (s_j == s_nt) {  // next item
+          ++s_item;
+          const int qb = s_item & 1;
+          if (!mbar_wait(&bars->q_full[qb], (s_item >> 1) & 1, p.err)) return false;
+          const bool done = slots[qb].done != 0;
+          const int nt = (slots[qb].it.ke - slots[qb].it.kb + kKeys - 1) / kKeys;
+          mbar_arrive(&bars->slot_free[qb]);
+          if (done) {
+            s_done = true;
+            return true;
+          }
+          s_nt = nt;
+          ring_nt[s_item & 3] = nt;
+          s_j = 0;
+        }
+        const int st = gs % kKStages, sb = gs & 1;
+        if (!mbar_wait(&bars->k_full[st], (gs / kKStages) & 1, p.err)) return false;
         tc_fence_after();
-        const uint32_t pbase = smem_base + kPOff + b * kPBytes;
-        const uint32_t vbase = smem_base + kSOff + st * kStageBytes + kTileBytes;
+        const uint64_t dqb = desc_add(dq, (s_item & 1) * kQBytes);
+        const uint64_t dk = desc_add(dk0, st * kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk)
-          umma_bf16(tmem + kOCol, desc_k(pbase + kk * 32), desc_v(vbase + kk * 2048), kIdescO,
-                    (first && kk == 0) ? 0u : 1u);
-        umma_commit(&bars->pv_done[b]);
-        umma_commit(&bars->kv_empty[st]);
+        for (int kk = 0; kk < 128 / 16; ++kk)
+          umma_bf16(tmem + kSCol + 128 * sb, desc_add(dqb, (kk >> 2) * kHalf + (kk & 3) * 32),
+                    desc_add(dk, (kk >> 2) * kHalfKV + (kk & 3) * 32), kIdescS, kk > 0 ? 1u : 0u);
+        umma_commit(&bars->s_full[sb]);
+        umma_commit(&bars->k_empty[st]);
+        if (s_j == s_nt - 1) umma_commit(&bars->q_empty[s_item & 1]);  // Q no longer read by this item
+        ++s_j;
+        ++gs;
         return true;
       };
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++it_cnt) {
-        const WorkItem it = p.items[idx];
-        if (!mbar_wait(&bars->q_full, it_cnt & 1, p.err)) break;
-        const int ntiles = (it.ke - it.kb + kKeys - 1) / kKeys;
-        for (int j = 0; j < ntiles; ++j, ++g) {
-          const int b = g & 1, st = g % kStages;
-          if (!mbar_wait(&bars->k_full[st], (g / kStages) & 1, p.err) ||
-              !mbar_wait(&bars->s_free[b], ((g >> 1) & 1) ^ 1, p.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t qbase = smem_base + kQOff;
-          const uint32_t kbase = smem_base + kSOff + st * kStageBytes;
-#pragma unroll
-          for (int kk = 0; kk < 128 / 16; ++kk)
-            umma_bf16(tmem + kSCol + b * kKeys, desc_k(qbase + (kk >> 2) * kHalf + (kk & 3) * 32),
-                      desc_k(kbase + (kk >> 2) * kHalfKV + (kk & 3) * 32), kIdescS, kk > 0 ? 1u : 0u);
-          umma_commit(&bars->s_full[b]);
-          if (j == ntiles - 1) umma_commit(&bars->q_empty);  // Q no longer read by this item
-          if (j == 0 && it_cnt > 0) {
-            // O is about to be overwritten: the previous item's epilogue must have read it
-            if (!mbar_wait(&bars->o_empty, (it_cnt - 1) & 1, p.err)) {
-              ok = false;
-              break;
-            }
-          }
-          if (j > 0 && !issue_pv(g - 1, j == 1)) {
-            ok = false;
-            break;
-          }
+      // O (+)= P V for the oldest tile whose S was issued; false when none is
+      // left or on a timeout
+      auto p_step = [&]() -> bool {
+        if (gp == gs) return false;
+        const int nt = ring_nt[p_item & 3];
+        if (p_j == 0) {
+          // O is about to be overwritten: item p_item-1's epilogue must have read it
+          if (!mbar_wait(&bars->o_empty, (p_item & 1) ^ 1, p.err)) return false;
         }
-        if (!ok) break;
-        if (!issue_pv(g - 1, ntiles == 1)) break;
-        umma_commit(&bars->o_full);
-      }
+        const int pb = gp & 1, st = gp % kVStages;
+        if (!mbar_wait(&bars->p_full[pb], (gp >> 1) & 1, p.err)) return false;
+        if (!mbar_wait(&bars->v_full[st], (gp / kVStages) & 1, p.err)) return false;
+        tc_fence_after();
+        const uint64_t dv = desc_add(dv0, st * kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          umma_bf16_ts(tmem + kOCol, tmem + kPCol + 64 * pb + kk * 8, desc_add(dv, kk * 2048), kIdescO,
+                       (p_j == 0 && kk == 0) ? 0u : 1u);
+        umma_commit(&bars->pv_done[pb]);
+        umma_commit(&bars->v_empty[st]);
+        if (p_j == nt - 1) {
+          umma_commit(&bars->o_full);
+          ++p_item;
+          p_j = 0;
+        } else {
+          ++p_j;
+        }
+        ++gp;
+        return true;
+      };
+      bool ok = s_step() && s_step();
+      while (ok && p_step()) ok = s_step();
     }
     __syncwarp();
   } else {
     // ================================================================ softmax / epilogue
     const int q4 = warp & 3;
-    const int h = (warp - 2) >> 2;  // key half of a tile (columns 32h .. 32h+31); output half 64h .. 64h+63
+    const int h = (warp - 2) >> 2;  // key half of a tile (columns 64h .. 64h+63); output half 64h .. 64h+63
     const int r = q4 * 32 + lane;   // row of the tile == TMEM lane
     const int pair_bar = 1 + q4;    // warps (w, w+4) of one row quarter
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
     float* red = reinterpret_cast<float*>(smem + kRedOff);
-    int g = 0, it_cnt = 0;
+    int g = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++it_cnt) {
-      const WorkItem it = p.items[idx];
-      const int L = p.context_lens[it.seq];
-      const int qstart = p.query_start_loc[it.seq];
-      const int n = p.query_start_loc[it.seq + 1] - qstart;
+    for (int c = 0; ok; ++c) {
+      const int qb = c & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_full[qb], (c >> 1) & 1, p.err))) break;
+      const ItemSlot& sl = slots[qb];
+      const bool done = sl.done != 0;
+      const WorkItem it = sl.it;
+      const int L = sl.L, qstart = sl.qstart, n = sl.n;
+      mbar_arrive(&bars->slot_free[qb]);
+      if (done) break;
       const bool valid = r < it.nrows;
       const int row = it.row0 + r;
       const int tok = row / p.G, gh = row - tok * p.G;
@@ -266,29 +379,28 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       float m_ref = -CUDART_INF_F, l = 0.f;
       const int ntiles = (it.ke - it.kb + kKeys - 1) / kKeys;
       for (int j = 0; j < ntiles; ++j, ++g) {
-        const int b = g & 1, st = g % kStages;
+        const int sb = g & 1, vs = g % kVStages;
         const int kt = it.kb + j * kKeys;  // first key of the tile
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[b], (g >> 1) & 1, p.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (g >> 1) & 1, p.err))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t sraw[32];
-        tmem_ld32(lane_base + kSCol + b * kKeys + 32 * h, sraw);
+        uint32_t sraw[64];
+        tmem_ld32(lane_base + kSCol + 128 * sb + 64 * h, sraw);
+        tmem_ld32(lane_base + kSCol + 128 * sb + 64 * h + 32, sraw + 32);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bars->s_free[b]);
-        const int nvis = vis - (kt + 32 * h);  // keys c < nvis of this half are visible
-        if (nvis < 32) {
+        const int nvis = vis - (kt + 64 * h);  // keys c < nvis of this half are visible
+        if (nvis < 64) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c >= nvis) sraw[c] = __float_as_uint(-CUDART_INF_F);
+          for (int cc = 0; cc < 64; ++cc)
+            if (cc >= nvis) sraw[cc] = __float_as_uint(-CUDART_INF_F);
         }
         float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-        for (int c = 0; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sraw[c]));
+        for (int cc = 0; cc < 64; ++cc) m4[cc & 3] = fmaxf(m4[cc & 3], __uint_as_float(sraw[cc]));
         float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        float* redm = red + b * 256;
+        float* redm = red + sb * 256;
         redm[h * 128 + r] = mx;
         named_barrier(pair_bar, 64);
         mx = fmaxf(mx, redm[(h ^ 1) * 128 + r]) * p.scale_log2;
@@ -300,66 +412,60 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           m_ref = mx;
         }
         const float neg_m = m_ref == -CUDART_INF_F ? 0.f : -m_ref;
-        // P buffer b is free once the P.V that read it two tiles ago is done
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[b], ((g >> 1) & 1) ^ 1, p.err))) {
+        // P buffer sb is free once the P.V of tile g-2, which read it, is done
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[sb], ((g >> 1) & 1) ^ 1, p.err))) {
           ok = false;
           break;
         }
-        uint8_t* prow = smem + kPOff + b * kPBytes + r * 128;
+        // P of keys 64h .. 64h+63 -> TMEM columns 32h .. 32h+31 of P buffer sb
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[32];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {  // 16-byte chunks of 8 keys: chunk 4h + u of the row
-          float e[8];
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            e[t] = fast_exp2(fmaf(__uint_as_float(sraw[u * 8 + t]), p.scale_log2, neg_m));
-            ps[t & 3] += e[t];
-          }
-          uint4 w;
-          w.x = pack_bf16(e[0], e[1]);
-          w.y = pack_bf16(e[2], e[3]);
-          w.z = pack_bf16(e[4], e[5]);
-          w.w = pack_bf16(e[6], e[7]);
-          *reinterpret_cast<uint4*>(prow + (((4 * h + u) ^ (r & 7)) << 4)) = w;
+        for (int cc = 0; cc < 32; ++cc) {
+          const float e0 = fast_exp2(fmaf(__uint_as_float(sraw[2 * cc]), p.scale_log2, neg_m));
+          const float e1 = fast_exp2(fmaf(__uint_as_float(sraw[2 * cc + 1]), p.scale_log2, neg_m));
+          ps[(2 * cc) & 3] += e0;
+          ps[(2 * cc + 1) & 3] += e1;
+          pk[cc] = pack_bf16(e0, e1);
         }
+        tmem_st32(lane_base + kPCol + 64 * sb + 32 * h, pk);
         l = fmaf(l, alpha, (ps[0] + ps[1]) + (ps[2] + ps[3]));
         if (__any_sync(0xffffffffu, rescale)) {
           // O must hold every earlier tile's P.V before it is scaled; the TMEM
           // accesses are warp-wide, rows that keep their max scale by 1
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[b ^ 1], ((g - 1) >> 1) & 1, p.err))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[sb ^ 1], ((g - 1) >> 1) & 1, p.err))) {
             ok = false;
             break;
           }
           tc_fence_after();
           const float f = rescale ? alpha : 1.f;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int cc = 0; cc < 2; ++cc) {
             uint32_t o[32];
-            tmem_ld32(lane_base + kOCol + 64 * h + c * 32, o);
+            tmem_ld32(lane_base + kOCol + 64 * h + cc * 32, o);
             tmem_wait_ld();
 #pragma unroll
             for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * f);
-            tmem_st32(lane_base + kOCol + 64 * h + c * 32, o);
+            tmem_st32(lane_base + kOCol + 64 * h + cc * 32, o);
           }
-          tmem_wait_st();
         }
         if (kt + kKeys > L) {
           // keys at or past the sequence's end hold arbitrary bits: zero their V
           // rows (thread: key r of the tile, d-half h) so that 0 * V stays 0
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (g / kStages) & 1, p.err))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[vs], (g / kVStages) & 1, p.err))) {
             ok = false;
             break;
           }
-          if (r < kKeys && kt + r >= L) {
-            uint4* v0 =
-                reinterpret_cast<uint4*>(smem + kSOff + st * kStageBytes + kTileBytes + h * kHalfKV + r * 128);
+          if (kt + r >= L) {
+            uint4* v0 = reinterpret_cast<uint4*>(smem + kVOff + vs * kTileBytes + h * kHalfKV + r * 128);
 #pragma unroll
             for (int t = 0; t < 8; ++t) v0[t] = make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
           }
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();  // P (and a rescaled O) written
         tc_fence_before();
-        mbar_arrive(&bars->p_full[b]);
+        mbar_arrive(&bars->p_full[sb]);
       }
       if (!ok) break;
       // ---- epilogue: row sum of the pair, O (this thread's 64 output columns) / l.
@@ -370,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       named_barrier(pair_bar, 64);
       const float ltot = l + reds[(h ^ 1) * 128 + r];
       named_barrier(pair_bar, 64);
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_full, it_cnt & 1, p.err))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_full, c & 1, p.err))) break;
       tc_fence_after();
       uint32_t o[64];
       tmem_ld32(lane_base + kOCol + 64 * h, o);
@@ -426,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
             float lsum = 0.f;
             float acc[64];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+            for (int cc = 0; cc < 64; ++cc) acc[cc] = 0.f;
             for (int sp = 0; sp < gr.nsplit; ++sp) {
               const int slot = gr.part_base + sp * gr.nrows + r;
               const float2 ml = __ldcg(&p.part_ml[slot]);
