@@ -337,7 +337,10 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   pp.dec_unit_rows = dectc ? tc_rows : kDecRows;
   pp.dec_tile_keys = dectc ? kMmaTileKeys : kDecTileKeys;
   pp.target_dec = dectc ? dev->sms * 6 : dec_grid * 4;
-  pp.target_mma = dev->sms * 4;
+  // Items are fetched dynamically in largest-first order, so two per SM
+  // balance the tensor-core kernel; every split costs a partial write and a
+  // merge, so no more are made than that.
+  pp.target_mma = dev->sms * 2;
   pp.min_chunk_dec = dectc ? 512 : 256;
   pp.min_chunk_mma = 512;
   pp.dec_cap = lay.dec_cap;
@@ -380,6 +383,7 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   ap.num_blocks = num_blocks;
   ap.scale_log2 = scale * 1.4426950408889634f;
   ap.causal = causal ? 1 : 0;
+  ap.out_al32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   ap.err = dev->err;
 
   if (g_prof_start && (e = cudaEventRecord(g_prof_start, s)) != cudaSuccess) return cuda_fail(e, "profile event");

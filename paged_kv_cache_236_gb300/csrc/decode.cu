@@ -86,31 +86,6 @@ struct alignas(16) Meta {
 };
 static_assert(sizeof(Meta) == 64, "meta slot");
 
-// ---------------------------------------------------------------------------
-// packed fp32x2 arithmetic (two fp32 values in one 64-bit register pair)
-// ---------------------------------------------------------------------------
-typedef unsigned long long f32x2;
-__device__ __forceinline__ f32x2 pk2(float lo, float hi) {
-  f32x2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float2 up2(f32x2 v) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-  return r;
-}
-__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
-  f32x2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
 // One 16-byte chunk of K or q as kEPC/2 fp32 pairs (elements 2j, 2j+1).
 template <typename T>
 __device__ __forceinline__ void chunk_to_pairs(const uint4 raw, f32x2* f);

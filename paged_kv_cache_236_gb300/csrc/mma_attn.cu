@@ -16,26 +16,31 @@
 // an M=128 MMA with N=64 costs about as long as one with N=128, and a chain
 // of MMAs accumulating into one TMEM region runs at about two thirds of the
 // peak rate when nothing else is queued, near the peak when a second,
-// independent chain is queued beside it.  So a tile is 128 keys (N=128 for
-// Q K^T), and the MMA thread issues the P.V of tile t directly followed by
-// the Q K^T of tile t+2: two independent chains back to back, while the
-// softmax warps work on tile t+1.
+// independent chain is queued beside it; the issuing thread cannot run
+// ahead of the pipe (issuing a chain takes about as long as running it), so
+// every wait between two issue phases leaves the pipe idle.  So a tile is 128
+// keys (N=128 for Q K^T), and per tile the MMA thread does all its waits
+// first, then issues the P.V of tile t directly followed by the Q K^T of tile
+// t+2: two independent chains back to back, while the softmax warps work on
+// tile t+1.
 //
-// Roles (352 threads, one CTA per SM, persistent; items are taken from an
+// Roles (384 threads, one CTA per SM, persistent; items are taken from an
 // atomic counter in the planner's largest-first order, so SMs that run
 // slower take fewer):
-//   warp 0    item fetch, Q and K producer: publishes each item in a slot of
+//   warp 0    item fetch and Q producer: publishes each item in a slot of
 //             shared memory with its Q tile (3-D box {64, G heads, 128/G
-//             tokens} of q [T, Hq, D], two 64-column halves), then per tile
-//             one {64, 1, block_size, 1} box of the pool [NB, bs, Hkv, D] per
-//             physical block and 64-column half (128-byte swizzle, the layout
-//             the tensor core reads); block ids are loaded a tile ahead;
+//             tokens} of q [T, Hq, D], two 64-column halves) as soon as a Q
+//             buffer is free, up to two items ahead;
 //   warp 1    TMEM allocation and the single thread issuing the MMAs;
 //   warps 2-9 softmax / correction / epilogue: two threads per row (TMEM
 //             lane), warps 2-5 on key columns 0-63 of a tile, warps 6-9 on
 //             64-127; a pair exchanges row maxima (and at the end row sums)
 //             through shared memory;
-//   warp 10   V producer, the same boxes from the V pool.
+//   warp 10   K producer: per tile one {64, 1, block_size, 1} box of the pool
+//             [NB, bs, Hkv, D] per physical block and 64-column half
+//             (128-byte swizzle, the layout the tensor core reads); block ids
+//             are loaded a tile ahead;
+//   warp 11   V producer, the same boxes from the V pool.
 // Shared memory: 2 Q tiles (64 KB), a 2-stage ring of K tiles (64 KB) and a
 // 3-stage ring of V tiles (96 KB); K of a tile is released when its Q K^T is
 // done, V when its P.V is done, so each ring refills as early as it can.
@@ -54,7 +59,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kKeys = kMmaTileKeys;                 // 128 keys per tile
 constexpr int kKStages = 2, kVStages = 3;
 constexpr int kHalfKV = kKeys * 128;                // one 64-column half of a K or V tile (16 KB)
@@ -65,7 +70,7 @@ constexpr int kQOff = 0;
 constexpr int kKOff = kQOff + 2 * kQBytes;
 constexpr int kVOff = kKOff + kKStages * kTileBytes;
 constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-constexpr int kNumBars = 6 + 2 * kKStages + 2 * kVStages + 6 + 2;
+constexpr int kNumBars = 6 + 2 * kKStages + 2 * kVStages + 8 + 2;
 constexpr int kSlotOff = (kBarOff + kNumBars * 8 + 16 + 15) & ~15;  // 2 item slots
 constexpr int kRedOff = kSlotOff + 2 * 64;          // [2 tiles][2 halves][128 rows] row maxima / sums
 // No alignment slack: the buffers need a 1024-byte aligned base, which the
@@ -89,7 +94,7 @@ struct Bars {
   uint64_t q_full[2], q_empty[2], slot_free[2];
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t o_full, o_empty;
 };
 
@@ -99,8 +104,8 @@ struct alignas(16) ItemSlot {
   int L, qstart, n, done;
   int pad[4];
 };
-// readers of a slot: the 256 softmax threads, the MMA thread, the V producer
-constexpr int kSlotReaders = 256 + 1 + 1;
+// readers of a slot: the 256 softmax threads, the MMA thread, the K and V producers
+constexpr int kSlotReaders = 256 + 1 + 1 + 1;
 
 static_assert(sizeof(ItemSlot) == 64, "item slot");
 static_assert(sizeof(Bars) == kNumBars * 8, "barrier block");
@@ -108,6 +113,19 @@ static_assert(kSmem <= 232448, "shared memory");
 static_assert(kKOff % 1024 == 0 && kVOff % 1024 == 0 && kTileBytes % 1024 == 0 && kQBytes % 1024 == 0,
               "swizzled tiles");
 static_assert(kBarOff % 8 == 0 && kSlotOff % alignof(ItemSlot) == 0 && kRedOff % 16 == 0, "alignment");
+
+// 64 bf16 (128 bytes) of an output row: four 32-byte stores when the output
+// is 32-byte aligned, else eight 16-byte ones.
+__device__ __forceinline__ void store_row128(__nv_bfloat16* dst, const uint32_t* w, int al32) {
+  if (al32) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) st_global_v8(dst + 16 * u, w + 8 * u);
+  } else {
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      *reinterpret_cast<uint4*>(dst + 8 * u) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+  }
+}
 
 __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams p,
                                                                const __grid_constant__ CUtensorMap qmap,
@@ -129,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       mbar_init(&bars->q_empty[b], 1);
       mbar_init(&bars->slot_free[b], kSlotReaders);
       mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->s_free[b], 256);
       mbar_init(&bars->p_full[b], 256);
       mbar_init(&bars->pv_done[b], 1);
     }
@@ -176,41 +195,29 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
   };
 
   if (warp == 0) {
-    // ================================================================ item fetch, Q and K
+    // ================================================================ item fetch and Q
     if (lane == 0) {
       prefetch_tensormap(&qmap);
-      prefetch_tensormap(&kmap);
-    }
-    int g = 0;
-    bool ok = true;
-    int next = 0;
-    if (lane == 0) next = atomicAdd(p.counter, 1);
-    for (int c = 0; ok; ++c) {
-      const int idx = __shfl_sync(0xffffffffu, next, 0);
-      const int qb = c & 1;
-      // slot and Q tile qb: free once item c-2's last Q K^T has completed and
-      // every reader has taken its description
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_empty[qb], ((c >> 1) & 1) ^ 1, p.err) &&
-                                       mbar_wait(&bars->slot_free[qb], ((c >> 1) & 1) ^ 1, p.err)))
-        break;
-      if (idx >= n_items) {
-        if (lane == 0) {
+      int next = atomicAdd(p.counter, 1);
+      for (int c = 0;; ++c) {
+        const int idx = next;
+        const int qb = c & 1;
+        // slot and Q tile qb: free once item c-2's last Q K^T has completed and
+        // every reader has taken its description
+        if (!mbar_wait(&bars->q_empty[qb], ((c >> 1) & 1) ^ 1, p.err) ||
+            !mbar_wait(&bars->slot_free[qb], ((c >> 1) & 1) ^ 1, p.err))
+          break;
+        if (idx >= n_items) {
           slots[qb].done = 1;
           mbar_arrive(&bars->q_full[qb]);
+          break;
         }
-        break;
-      }
-      const WorkItem it = p.items[idx];
-      if (lane == 0) next = atomicAdd(p.counter, 1);  // consumed after this item's tiles
-      const int L = p.context_lens[it.seq];
-      const int qstart = p.query_start_loc[it.seq];
-      const int nblk = (L + p.bs - 1) / p.bs;
-      const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
-      int phys = block_of(bt, nblk, it.kb);
-      if (lane == 0) {
+        const WorkItem it = p.items[idx];
+        next = atomicAdd(p.counter, 1);  // consumed at the next item
+        const int qstart = p.query_start_loc[it.seq];
         ItemSlot& sl = slots[qb];
         sl.it = it;
-        sl.L = L;
+        sl.L = p.context_lens[it.seq];
         sl.qstart = qstart;
         sl.n = p.query_start_loc[it.seq + 1] - qstart;
         sl.done = 0;
@@ -219,26 +226,17 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         tma_load_3d(smem + kQOff + qb * kQBytes, &qmap, &bars->q_full[qb], 0, it.kvh * p.G, tok0);
         tma_load_3d(smem + kQOff + qb * kQBytes + kHalf, &qmap, &bars->q_full[qb], 64, it.kvh * p.G, tok0);
       }
-      for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
-        const int st = g % kKStages;
-        const int next_phys = (kbase + kKeys < it.ke) ? block_of(bt, nblk, kbase + kKeys) : 0;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_empty[st], ((g / kKStages) & 1) ^ 1, p.err))) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
-        __syncwarp();
-        if (lane < nb) {
-          uint8_t* kd = smem + kKOff + st * kTileBytes + lane * p.bs * 128;
-          tma_load_4d(kd, &kmap, &bars->k_full[st], 0, it.kvh, 0, phys);
-          tma_load_4d(kd + kHalfKV, &kmap, &bars->k_full[st], 64, it.kvh, 0, phys);
-        }
-        phys = next_phys;
-      }
     }
-  } else if (warp == 10) {
-    // ================================================================ V
-    if (lane == 0) prefetch_tensormap(&vmap);
+    __syncwarp();
+  } else if (warp >= 10) {
+    // ================================================================ K (warp 10) or V (warp 11)
+    const bool is_k = warp == 10;
+    const CUtensorMap* map = is_k ? &kmap : &vmap;
+    const int nstages = is_k ? kKStages : kVStages;
+    uint64_t* full = is_k ? bars->k_full : bars->v_full;
+    uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+    uint8_t* ring = smem + (is_k ? kKOff : kVOff);
+    if (lane == 0) prefetch_tensormap(map);
     int g = 0;
     bool ok = true;
     for (int c = 0; ok; ++c) {
@@ -254,18 +252,18 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
       int phys = block_of(bt, nblk, it.kb);
       for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
-        const int st = g % kVStages;
+        const int st = g % nstages, ph = (g / nstages) & 1;
         const int next_phys = (kbase + kKeys < it.ke) ? block_of(bt, nblk, kbase + kKeys) : 0;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_empty[st], ((g / kVStages) & 1) ^ 1, p.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[st], ph ^ 1, p.err))) {
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
         __syncwarp();
         if (lane < nb) {
-          uint8_t* vd = smem + kVOff + st * kTileBytes + lane * p.bs * 128;
-          tma_load_4d(vd, &vmap, &bars->v_full[st], 0, it.kvh, 0, phys);
-          tma_load_4d(vd + kHalfKV, &vmap, &bars->v_full[st], 64, it.kvh, 0, phys);
+          uint8_t* d = ring + st * kTileBytes + lane * p.bs * 128;
+          tma_load_4d(d, map, &full[st], 0, it.kvh, 0, phys);
+          tma_load_4d(d + kHalfKV, map, &full[st], 64, it.kvh, 0, phys);
         }
         phys = next_phys;
       }
@@ -280,32 +278,35 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       // Q K^T iterator (two tiles ahead) and P.V iterator over this CTA's tiles
       int gs = 0, s_item = -1, s_j = 0, s_nt = 0;
       bool s_done = false;
-      int gp = 0, p_item = 0, p_j = 0;
-      int ring_nt[4] = {0, 0, 0, 0};  // tile counts of the items between the two iterators
-      // S of the next tile; false on a timeout.  S buffer gs % 2 was last read
-      // by the softmax of tile gs-2, which finished reading it before it
-      // signalled P(gs-2) full, and P.V(gs-2) (issued only after that) precedes
-      // this call.
-      auto s_step = [&]() -> bool {
-        if (s_done) return true;
+      int gp = 0, p_item = 0;
+      // bit (g & 7): tile g is the first / the last of its item (the S
+      // iterator runs at most three tiles ahead; registers, not local memory)
+      uint32_t first_bits = 0, last_bits = 0;
+      // Waits until S of the next tile can be issued (its item's Q loaded, S
+      // buffer gs % 2 read by the softmax warps, K loaded): 1 ready, 0 no tile
+      // left, -1 timeout.
+      auto s_ready = [&]() -> int {
+        if (s_done) return 0;
         if (s_j == s_nt) {  // next item
           ++s_item;
           const int qb = s_item & 1;
-          if (!mbar_wait(&bars->q_full[qb], (s_item >> 1) & 1, p.err)) return false;
+          if (!mbar_wait(&bars->q_full[qb], (s_item >> 1) & 1, p.err)) return -1;
           const bool done = slots[qb].done != 0;
           const int nt = (slots[qb].it.ke - slots[qb].it.kb + kKeys - 1) / kKeys;
           mbar_arrive(&bars->slot_free[qb]);
           if (done) {
             s_done = true;
-            return true;
+            return 0;
           }
           s_nt = nt;
-          ring_nt[s_item & 3] = nt;
           s_j = 0;
         }
+        if (!mbar_wait(&bars->s_free[gs & 1], ((gs >> 1) & 1) ^ 1, p.err)) return -1;
+        if (!mbar_wait(&bars->k_full[gs % kKStages], (gs / kKStages) & 1, p.err)) return -1;
+        return 1;
+      };
+      auto s_issue = [&]() {
         const int st = gs % kKStages, sb = gs & 1;
-        if (!mbar_wait(&bars->k_full[st], (gs / kKStages) & 1, p.err)) return false;
-        tc_fence_after();
         const uint64_t dqb = desc_add(dq, (s_item & 1) * kQBytes);
         const uint64_t dk = desc_add(dk0, st * kTileBytes);
 #pragma unroll
@@ -314,43 +315,61 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
                     desc_add(dk, (kk >> 2) * kHalfKV + (kk & 3) * 32), kIdescS, kk > 0 ? 1u : 0u);
         umma_commit(&bars->s_full[sb]);
         umma_commit(&bars->k_empty[st]);
+        const uint32_t bit = 1u << (gs & 7);
+        first_bits = s_j == 0 ? (first_bits | bit) : (first_bits & ~bit);
+        last_bits = s_j == s_nt - 1 ? (last_bits | bit) : (last_bits & ~bit);
         if (s_j == s_nt - 1) umma_commit(&bars->q_empty[s_item & 1]);  // Q no longer read by this item
         ++s_j;
         ++gs;
-        return true;
       };
-      // O (+)= P V for the oldest tile whose S was issued; false when none is
-      // left or on a timeout
-      auto p_step = [&]() -> bool {
-        if (gp == gs) return false;
-        const int nt = ring_nt[p_item & 3];
-        if (p_j == 0) {
+      // Waits until the P.V of the oldest tile whose S was issued can be issued
+      // (O free at an item's first tile, P written, V loaded): 1 ready, 0 no
+      // tile left, -1 timeout.
+      auto p_ready = [&]() -> int {
+        if (gp == gs) return 0;
+        if ((first_bits >> (gp & 7)) & 1u) {
           // O is about to be overwritten: item p_item-1's epilogue must have read it
-          if (!mbar_wait(&bars->o_empty, (p_item & 1) ^ 1, p.err)) return false;
+          if (!mbar_wait(&bars->o_empty, (p_item & 1) ^ 1, p.err)) return -1;
         }
+        if (!mbar_wait(&bars->p_full[gp & 1], (gp >> 1) & 1, p.err)) return -1;
+        if (!mbar_wait(&bars->v_full[gp % kVStages], (gp / kVStages) & 1, p.err)) return -1;
+        return 1;
+      };
+      auto p_issue = [&]() {
         const int pb = gp & 1, st = gp % kVStages;
-        if (!mbar_wait(&bars->p_full[pb], (gp >> 1) & 1, p.err)) return false;
-        if (!mbar_wait(&bars->v_full[st], (gp / kVStages) & 1, p.err)) return false;
-        tc_fence_after();
+        const bool first = (first_bits >> (gp & 7)) & 1u, last = (last_bits >> (gp & 7)) & 1u;
         const uint64_t dv = desc_add(dv0, st * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
           umma_bf16_ts(tmem + kOCol, tmem + kPCol + 64 * pb + kk * 8, desc_add(dv, kk * 2048), kIdescO,
-                       (p_j == 0 && kk == 0) ? 0u : 1u);
+                       (first && kk == 0) ? 0u : 1u);
         umma_commit(&bars->pv_done[pb]);
         umma_commit(&bars->v_empty[st]);
-        if (p_j == nt - 1) {
+        if (last) {
           umma_commit(&bars->o_full);
           ++p_item;
-          p_j = 0;
-        } else {
-          ++p_j;
         }
         ++gp;
-        return true;
       };
-      bool ok = s_step() && s_step();
-      while (ok && p_step()) ok = s_step();
+      // S(0), S(1); then per tile t, with every wait done first, P.V(t)
+      // directly followed by S(t+2): two independent chains back to back
+      bool ok = true;
+      for (int i = 0; i < 2 && ok; ++i) {
+        const int r = s_ready();
+        ok = r >= 0;
+        if (r <= 0) break;
+        tc_fence_after();
+        s_issue();
+      }
+      while (ok) {
+        const int rp = p_ready();
+        if (rp <= 0) break;
+        const int rs = s_ready();
+        if (rs < 0) break;
+        tc_fence_after();
+        p_issue();
+        if (rs > 0) s_issue();
+      }
     }
     __syncwarp();
   } else {
@@ -390,6 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         tmem_ld32(lane_base + kSCol + 128 * sb + 64 * h, sraw);
         tmem_ld32(lane_base + kSCol + 128 * sb + 64 * h + 32, sraw + 32);
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars->s_free[sb]);  // S buffer sb may take the S of tile g+2
         const int nvis = vis - (kt + 64 * h);  // keys c < nvis of this half are visible
         if (nvis < 64) {
 #pragma unroll
@@ -399,37 +420,62 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
         for (int cc = 0; cc < 64; ++cc) m4[cc & 3] = fmaxf(m4[cc & 3], __uint_as_float(sraw[cc]));
-        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        const float mloc = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));  // this half's max (raw S)
         float* redm = red + sb * 256;
-        redm[h * 128 + r] = mx;
-        named_barrier(pair_bar, 64);
-        mx = fmaxf(mx, redm[(h ^ 1) * 128 + r]) * p.scale_log2;
+        redm[h * 128 + r] = mloc;
+        // P of keys 64h .. 64h+63: 2^(S scale_log2 - m) packed to bf16 pairs
+        // (TMEM columns 32h .. 32h+31 of P buffer sb), ps2 their sums
+        const f32x2 sc2 = pk2(p.scale_log2, p.scale_log2);
+        uint32_t pk[32];
+        f32x2 ps2[2];
+        auto exps = [&](float m) {
+          const float nm = m == -CUDART_INF_F ? 0.f : -m;
+          const f32x2 nm2 = pk2(nm, nm);
+          ps2[0] = ps2[1] = pk2(0.f, 0.f);
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc) {
+            const float2 x = up2(fma2(pk2(__uint_as_float(sraw[2 * cc]), __uint_as_float(sraw[2 * cc + 1])), sc2, nm2));
+            const float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
+            ps2[cc & 1] = add2(ps2[cc & 1], pk2(e0, e1));
+            pk[cc] = pack_bf16(e0, e1);
+          }
+        };
         float alpha = 1.f;
         bool rescale = false;
-        if (mx > m_ref + kRescaleThreshold) {  // false while both are -inf
-          alpha = fast_exp2(m_ref - mx);       // 0 when m_ref is -inf
-          rescale = j > 0 && m_ref != -CUDART_INF_F;
-          m_ref = mx;
+        if (j == 0) {
+          // first tile of the item: the row max first, then the exponentials
+          named_barrier(pair_bar, 64);
+          const float mx = fmaxf(mloc, redm[(h ^ 1) * 128 + r]) * p.scale_log2;
+          if (mx > m_ref + kRescaleThreshold) {  // false while both are -inf
+            alpha = fast_exp2(m_ref - mx);       // 0: m_ref is -inf here
+            m_ref = mx;
+          }
+          exps(m_ref);
+        } else {
+          // The reference max of the earlier tiles is known, so the
+          // exponentials go ahead of the pair's max exchange; they are redone
+          // in the rare case that the row max exceeds the reference by more
+          // than the threshold (or the row had no visible key before).
+          exps(m_ref);
+          named_barrier(pair_bar, 64);
+          const float mx = fmaxf(mloc, redm[(h ^ 1) * 128 + r]) * p.scale_log2;
+          if (mx > m_ref + kRescaleThreshold) {
+            alpha = fast_exp2(m_ref - mx);  // 0 when m_ref is -inf
+            rescale = m_ref != -CUDART_INF_F;
+            m_ref = mx;
+            exps(m_ref);
+          }
         }
-        const float neg_m = m_ref == -CUDART_INF_F ? 0.f : -m_ref;
         // P buffer sb is free once the P.V of tile g-2, which read it, is done
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[sb], ((g >> 1) & 1) ^ 1, p.err))) {
           ok = false;
           break;
         }
-        // P of keys 64h .. 64h+63 -> TMEM columns 32h .. 32h+31 of P buffer sb
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[32];
-#pragma unroll
-        for (int cc = 0; cc < 32; ++cc) {
-          const float e0 = fast_exp2(fmaf(__uint_as_float(sraw[2 * cc]), p.scale_log2, neg_m));
-          const float e1 = fast_exp2(fmaf(__uint_as_float(sraw[2 * cc + 1]), p.scale_log2, neg_m));
-          ps[(2 * cc) & 3] += e0;
-          ps[(2 * cc + 1) & 3] += e1;
-          pk[cc] = pack_bf16(e0, e1);
-        }
         tmem_st32(lane_base + kPCol + 64 * sb + 32 * h, pk);
-        l = fmaf(l, alpha, (ps[0] + ps[1]) + (ps[2] + ps[3]));
+        {
+          const float2 a = up2(ps2[0]), b = up2(ps2[1]);
+          l = fmaf(l, alpha, (a.x + a.y) + (b.x + b.y));
+        }
         if (__any_sync(0xffffffffu, rescale)) {
           // O must hold every earlier tile's P.V before it is scaled; the TMEM
           // accesses are warp-wide, rows that keep their max scale by 1
@@ -489,21 +535,16 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           const float inv = 1.f / ltot;
           __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
                                 ((int64_t)(qstart + tok) * p.Hq + (int64_t)it.kvh * p.G + gh) * 128 + 64 * h;
+          uint32_t w[32];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(o[u * 8 + 0]) * inv, __uint_as_float(o[u * 8 + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(o[u * 8 + 2]) * inv, __uint_as_float(o[u * 8 + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(o[u * 8 + 4]) * inv, __uint_as_float(o[u * 8 + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(o[u * 8 + 6]) * inv, __uint_as_float(o[u * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + u * 8) = w;
-          }
+          for (int u = 0; u < 32; ++u)
+            w[u] = pack_bf16(__uint_as_float(o[2 * u]) * inv, __uint_as_float(o[2 * u + 1]) * inv);
+          store_row128(orow, w, p.out_al32);
         } else {
-          float4* dst = reinterpret_cast<float4*>(p.part_acc + (int64_t)(it.part + r) * 128 + 64 * h);
+          // this split's partial row: 256 bytes of fp32 (the workspace is 256-byte aligned)
+          float* dst = p.part_acc + (int64_t)(it.part + r) * 128 + 64 * h;
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
-            dst[u] = make_float4(__uint_as_float(o[u * 4]), __uint_as_float(o[u * 4 + 1]),
-                                 __uint_as_float(o[u * 4 + 2]), __uint_as_float(o[u * 4 + 3]));
+          for (int u = 0; u < 8; ++u) st_global_v8(dst + 8 * u, o + 8 * u);
           if (h == 0) p.part_ml[it.part + r] = make_float2(m_ref, ltot);
         }
       }
@@ -553,15 +594,10 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
             const int gtok = grow / p.G, ggh = grow - gtok * p.G;
             __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
                                   ((int64_t)(qstart + gtok) * p.Hq + (int64_t)gr.kvh * p.G + ggh) * 128 + 64 * h;
+            uint32_t w[32];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              uint4 w;
-              w.x = pack_bf16(acc[u * 8 + 0] * inv, acc[u * 8 + 1] * inv);
-              w.y = pack_bf16(acc[u * 8 + 2] * inv, acc[u * 8 + 3] * inv);
-              w.z = pack_bf16(acc[u * 8 + 4] * inv, acc[u * 8 + 5] * inv);
-              w.w = pack_bf16(acc[u * 8 + 6] * inv, acc[u * 8 + 7] * inv);
-              *reinterpret_cast<uint4*>(orow + u * 8) = w;
-            }
+            for (int u = 0; u < 32; ++u) w[u] = pack_bf16(acc[2 * u] * inv, acc[2 * u + 1] * inv);
+            store_row128(orow, w, p.out_al32);
           }
         }
         named_barrier(5, 256);

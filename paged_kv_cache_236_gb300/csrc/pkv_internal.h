@@ -103,6 +103,7 @@ struct AttnParams {
   int64_t num_blocks;
   float scale_log2;  // scale * log2(e)
   int causal;
+  int out_al32;      // out is 32-byte aligned (256-bit stores)
   int* err;
 };
 
