@@ -17,12 +17,15 @@
 // of MMAs accumulating into one TMEM region runs at about two thirds of the
 // peak rate when nothing else is queued, near the peak when a second,
 // independent chain is queued beside it; the issuing thread cannot run
-// ahead of the pipe (issuing a chain takes about as long as running it), so
-// every wait between two issue phases leaves the pipe idle.  So a tile is 128
-// keys (N=128 for Q K^T), and per tile the MMA thread does all its waits
-// first, then issues the P.V of tile t directly followed by the Q K^T of tile
-// t+2: two independent chains back to back, while the softmax warps work on
-// tile t+1.
+// ahead of the pipe: issuing one M=128, N=128 MMA takes about as long as
+// running it, so every wait or commit between MMAs leaves the pipe idle.  So
+// a tile is 128 keys (N=128 for Q K^T), and per tile the MMA thread does its
+// waits first (one instruction when all are already satisfied), then issues
+// the P.V of tile t directly followed by the Q K^T of tile t+2 and commits
+// both to one barrier, while the softmax warps work on tile t+1.  That
+// barrier (phase of "block" t) tells the softmax warps that S(t+2) is ready
+// and P buffer t % 2 free, the K producer that K stage t % 2 is free, and the
+// epilogue that O is complete.
 //
 // Roles (384 threads, one CTA per SM, persistent; items are taken from an
 // atomic counter in the planner's largest-first order, so SMs that run
@@ -70,7 +73,7 @@ constexpr int kQOff = 0;
 constexpr int kKOff = kQOff + 2 * kQBytes;
 constexpr int kVOff = kKOff + kKStages * kTileBytes;
 constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-constexpr int kNumBars = 6 + 2 * kKStages + 2 * kVStages + 8 + 2;
+constexpr int kNumBars = 6 + kKStages + 2 * kVStages + 4 + 1;
 constexpr int kSlotOff = (kBarOff + kNumBars * 8 + 16 + 15) & ~15;  // 2 item slots
 constexpr int kRedOff = kSlotOff + 2 * 64;          // [2 tiles][2 halves][128 rows] row maxima / sums
 // No alignment slack: the buffers need a 1024-byte aligned base, which the
@@ -92,10 +95,12 @@ __device__ __forceinline__ uint64_t desc_v(uint32_t saddr) { return smem_desc(sa
 
 struct Bars {
   uint64_t q_full[2], q_empty[2], slot_free[2];
-  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t k_full[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
-  uint64_t o_full, o_empty;
+  // blk[b], phase n: S of tile 2n+b complete, and with it every MMA issued
+  // before (the P.V of tile 2n+b-2 in particular)
+  uint64_t blk[2], p_full[2];
+  uint64_t o_empty;
 };
 
 // An item's description, published by the item-fetching warp with its Q tile.
@@ -109,6 +114,7 @@ constexpr int kSlotReaders = 256 + 1 + 1 + 1;
 
 static_assert(sizeof(ItemSlot) == 64, "item slot");
 static_assert(sizeof(Bars) == kNumBars * 8, "barrier block");
+static_assert(kKStages == 2, "K stage t % 2 is released by the S barrier of tile t");
 static_assert(kSmem <= 232448, "shared memory");
 static_assert(kKOff % 1024 == 0 && kVOff % 1024 == 0 && kTileBytes % 1024 == 0 && kQBytes % 1024 == 0,
               "swizzled tiles");
@@ -146,20 +152,14 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       mbar_init(&bars->q_full[b], 1);
       mbar_init(&bars->q_empty[b], 1);
       mbar_init(&bars->slot_free[b], kSlotReaders);
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_free[b], 256);
+      mbar_init(&bars->blk[b], 1);
       mbar_init(&bars->p_full[b], 256);
-      mbar_init(&bars->pv_done[b], 1);
     }
-    for (int s = 0; s < kKStages; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-    }
+    for (int s = 0; s < kKStages; ++s) mbar_init(&bars->k_full[s], 1);
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_empty, 256);
     fence_mbar_init();
   }
@@ -234,7 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
     const CUtensorMap* map = is_k ? &kmap : &vmap;
     const int nstages = is_k ? kKStages : kVStages;
     uint64_t* full = is_k ? bars->k_full : bars->v_full;
-    uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+    // K stage g % 2 is free once S(g-2) is complete (phase of blk[g % 2])
+    uint64_t* empty = is_k ? bars->blk : bars->v_empty;
     uint8_t* ring = smem + (is_k ? kKOff : kVOff);
     if (lane == 0) prefetch_tensormap(map);
     int g = 0;
@@ -278,43 +279,45 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       // Q K^T iterator (two tiles ahead) and P.V iterator over this CTA's tiles
       int gs = 0, s_item = -1, s_j = 0, s_nt = 0;
       bool s_done = false;
-      int gp = 0, p_item = 0;
+      int gp = 0, p_item = 0;  // P.V iterator: tile, item
       // bit (g & 7): tile g is the first / the last of its item (the S
       // iterator runs at most three tiles ahead; registers, not local memory)
       uint32_t first_bits = 0, last_bits = 0;
-      // Waits until S of the next tile can be issued (its item's Q loaded, S
-      // buffer gs % 2 read by the softmax warps, K loaded): 1 ready, 0 no tile
-      // left, -1 timeout.
-      auto s_ready = [&]() -> int {
-        if (s_done) return 0;
+      // Item bookkeeping for the next S: false when no tile is left (or on a
+      // timeout, with ok cleared).
+      bool ok = true;
+      auto s_next = [&]() -> bool {
+        if (s_done) return false;
         if (s_j == s_nt) {  // next item
           ++s_item;
           const int qb = s_item & 1;
-          if (!mbar_wait(&bars->q_full[qb], (s_item >> 1) & 1, p.err)) return -1;
+          if (!mbar_wait(&bars->q_full[qb], (s_item >> 1) & 1, p.err)) {
+            ok = false;
+            return false;
+          }
           const bool done = slots[qb].done != 0;
           const int nt = (slots[qb].it.ke - slots[qb].it.kb + kKeys - 1) / kKeys;
           mbar_arrive(&bars->slot_free[qb]);
           if (done) {
             s_done = true;
-            return 0;
+            return false;
           }
           s_nt = nt;
           s_j = 0;
         }
-        if (!mbar_wait(&bars->s_free[gs & 1], ((gs >> 1) & 1) ^ 1, p.err)) return -1;
-        if (!mbar_wait(&bars->k_full[gs % kKStages], (gs / kKStages) & 1, p.err)) return -1;
-        return 1;
+        return true;
       };
-      auto s_issue = [&]() {
-        const int st = gs % kKStages, sb = gs & 1;
+      // k-step kk of S(gs) into S buffer gs % 2 (K loaded; the buffer's
+      // previous S was read before P of its tile was signalled, which the
+      // caller has waited for)
+      auto s_mma = [&](int kk) {
         const uint64_t dqb = desc_add(dq, (s_item & 1) * kQBytes);
-        const uint64_t dk = desc_add(dk0, st * kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk)
-          umma_bf16(tmem + kSCol + 128 * sb, desc_add(dqb, (kk >> 2) * kHalf + (kk & 3) * 32),
-                    desc_add(dk, (kk >> 2) * kHalfKV + (kk & 3) * 32), kIdescS, kk > 0 ? 1u : 0u);
-        umma_commit(&bars->s_full[sb]);
-        umma_commit(&bars->k_empty[st]);
+        const uint64_t dk = desc_add(dk0, (gs % kKStages) * kTileBytes);
+        umma_bf16(tmem + kSCol + 128 * (gs & 1), desc_add(dqb, (kk >> 2) * kHalf + (kk & 3) * 32),
+                  desc_add(dk, (kk >> 2) * kHalfKV + (kk & 3) * 32), kIdescS, kk > 0 ? 1u : 0u);
+      };
+      // bookkeeping once S(gs) is issued
+      auto s_done_tile = [&]() {
         const uint32_t bit = 1u << (gs & 7);
         first_bits = s_j == 0 ? (first_bits | bit) : (first_bits & ~bit);
         last_bits = s_j == s_nt - 1 ? (last_bits | bit) : (last_bits & ~bit);
@@ -322,53 +325,56 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         ++s_j;
         ++gs;
       };
-      // Waits until the P.V of the oldest tile whose S was issued can be issued
-      // (O free at an item's first tile, P written, V loaded): 1 ready, 0 no
-      // tile left, -1 timeout.
-      auto p_ready = [&]() -> int {
-        if (gp == gs) return 0;
-        if ((first_bits >> (gp & 7)) & 1u) {
-          // O is about to be overwritten: item p_item-1's epilogue must have read it
-          if (!mbar_wait(&bars->o_empty, (p_item & 1) ^ 1, p.err)) return -1;
+      // S(0), S(1)
+      for (int i = 0; i < 2 && s_next(); ++i) {
+        if (!mbar_wait(&bars->k_full[gs % kKStages], (gs / kKStages) & 1, p.err)) {
+          ok = false;
+          break;
         }
-        if (!mbar_wait(&bars->p_full[gp & 1], (gp >> 1) & 1, p.err)) return -1;
-        if (!mbar_wait(&bars->v_full[gp % kVStages], (gp / kVStages) & 1, p.err)) return -1;
-        return 1;
-      };
-      auto p_issue = [&]() {
-        const int pb = gp & 1, st = gp % kVStages;
-        const bool first = (first_bits >> (gp & 7)) & 1u, last = (last_bits >> (gp & 7)) & 1u;
-        const uint64_t dv = desc_add(dv0, st * kTileBytes);
+        tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk)
-          umma_bf16_ts(tmem + kOCol, tmem + kPCol + 64 * pb + kk * 8, desc_add(dv, kk * 2048), kIdescO,
-                       (first && kk == 0) ? 0u : 1u);
-        umma_commit(&bars->pv_done[pb]);
-        umma_commit(&bars->v_empty[st]);
-        if (last) {
-          umma_commit(&bars->o_full);
-          ++p_item;
-        }
-        ++gp;
-      };
-      // S(0), S(1); then per tile t, with every wait done first, P.V(t)
-      // directly followed by S(t+2): two independent chains back to back
-      bool ok = true;
-      for (int i = 0; i < 2 && ok; ++i) {
-        const int r = s_ready();
-        ok = r >= 0;
-        if (r <= 0) break;
-        tc_fence_after();
-        s_issue();
+        for (int kk = 0; kk < 8; ++kk) s_mma(kk);
+        s_done_tile();
+        umma_commit(&bars->blk[(gs - 1) & 1]);
       }
-      while (ok) {
-        const int rp = p_ready();
-        if (rp <= 0) break;
-        const int rs = s_ready();
-        if (rs < 0) break;
+      // block t: P.V(t) and S(t+2), their MMAs interleaved (two independent
+      // accumulation chains keep the pipe busier than one after the other),
+      // one commit
+      while (ok && gp < gs) {
+        const uint32_t bit = 1u << (gp & 7);
+        const bool first = (first_bits & bit) != 0, last = (last_bits & bit) != 0;
+        if (first && !mbar_wait(&bars->o_empty, (p_item & 1) ^ 1, p.err)) break;  // O read by item p_item-1
+        const bool more = s_next();
+        if (!ok) break;
+        const int pb = gp & 1, vst = gp % kVStages;
+        uint64_t* wk = &bars->k_full[gs % kKStages];
+        const uint32_t pk_ = (gs / kKStages) & 1;
+        if (!mbar_test_wait3(&bars->p_full[pb], (gp >> 1) & 1, &bars->v_full[vst], (gp / kVStages) & 1,
+                             more ? wk : &bars->p_full[pb], more ? pk_ : ((gp >> 1) & 1))) {
+          if (!mbar_wait(&bars->p_full[pb], (gp >> 1) & 1, p.err) ||
+              !mbar_wait(&bars->v_full[vst], (gp / kVStages) & 1, p.err) || (more && !mbar_wait(wk, pk_, p.err)))
+            break;
+        }
         tc_fence_after();
-        p_issue();
-        if (rs > 0) s_issue();
+        const uint64_t dv = desc_add(dv0, vst * kTileBytes);
+        if (more) {
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            umma_bf16_ts(tmem + kOCol, tmem + kPCol + 64 * pb + kk * 8, desc_add(dv, kk * 2048), kIdescO,
+                         (first && kk == 0) ? 0u : 1u);
+            s_mma(kk);
+          }
+          s_done_tile();
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk)
+            umma_bf16_ts(tmem + kOCol, tmem + kPCol + 64 * pb + kk * 8, desc_add(dv, kk * 2048), kIdescO,
+                         (first && kk == 0) ? 0u : 1u);
+        }
+        umma_commit(&bars->v_empty[vst]);
+        umma_commit(&bars->blk[gp & 1]);  // S(gp+2) (if any) and P.V(gp) complete
+        if (last) ++p_item;
+        ++gp;
       }
     }
     __syncwarp();
@@ -400,7 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       for (int j = 0; j < ntiles; ++j, ++g) {
         const int sb = g & 1, vs = g % kVStages;
         const int kt = it.kb + j * kKeys;  // first key of the tile
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (g >> 1) & 1, p.err))) {
+        // S(g) complete; with it P.V(g-2), so P buffer sb is free too
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->blk[sb], (g >> 1) & 1, p.err))) {
           ok = false;
           break;
         }
@@ -409,8 +416,6 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         tmem_ld32(lane_base + kSCol + 128 * sb + 64 * h, sraw);
         tmem_ld32(lane_base + kSCol + 128 * sb + 64 * h + 32, sraw + 32);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bars->s_free[sb]);  // S buffer sb may take the S of tile g+2
         const int nvis = vis - (kt + 64 * h);  // keys c < nvis of this half are visible
         if (nvis < 64) {
 #pragma unroll
@@ -466,11 +471,6 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
             exps(m_ref);
           }
         }
-        // P buffer sb is free once the P.V of tile g-2, which read it, is done
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[sb], ((g >> 1) & 1) ^ 1, p.err))) {
-          ok = false;
-          break;
-        }
         tmem_st32(lane_base + kPCol + 64 * sb + 32 * h, pk);
         {
           const float2 a = up2(ps2[0]), b = up2(ps2[1]);
@@ -479,7 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         if (__any_sync(0xffffffffu, rescale)) {
           // O must hold every earlier tile's P.V before it is scaled; the TMEM
           // accesses are warp-wide, rows that keep their max scale by 1
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[sb ^ 1], ((g - 1) >> 1) & 1, p.err))) {
+          // P.V(g-1) complete: the phase of blk[(g+1) % 2] that block g-1 commits
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->blk[sb ^ 1], ((g + 1) >> 1) & 1, p.err))) {
             ok = false;
             break;
           }
@@ -522,7 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       named_barrier(pair_bar, 64);
       const float ltot = l + reds[(h ^ 1) * 128 + r];
       named_barrier(pair_bar, 64);
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_full, c & 1, p.err))) break;
+      // P.V of the item's last tile (g-1) complete: block g-1's phase of blk[(g+1) % 2]
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->blk[(g + 1) & 1], ((g + 1) >> 1) & 1, p.err))) break;
       tc_fence_after();
       uint32_t o[64];
       tmem_ld32(lane_base + kOCol + 64 * h, o);

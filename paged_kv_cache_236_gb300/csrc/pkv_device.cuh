@@ -80,6 +80,24 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of three phases at once; true when all have completed.
+__device__ __forceinline__ bool mbar_test_wait3(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb, uint64_t* c,
+                                                uint32_t pc) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p, q, r;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 r, [%5], %6;\n\t"
+      "and.pred p, p, q;\n\t"
+      "and.pred p, p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(a)), "r"(pa), "r"(smem_u32(b)), "r"(pb), "r"(smem_u32(c)), "r"(pc)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false (and
 // sets PKV_DEVERR_TIMEOUT) if it has not completed within kWaitTimeoutNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
