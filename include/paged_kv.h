@@ -141,7 +141,8 @@ size_t paged_attention_workspace_min(int32_t num_seqs, int64_t num_tokens, int32
  *                   256-byte aligned; overwritten by the call; must not be shared by
  *                   calls that may run concurrently
  * Supported: dtype bf16 or f32; head_dim 64 or 128; block_size 8, 16, 32 or 64;
- * num_q_heads / num_kv_heads <= 128.
+ * num_q_heads / num_kv_heads <= 128; num_seqs <= 32768 (PKV_ERR_UNSUPPORTED
+ * beyond).
  * Rows of a sequence whose metadata is invalid (see the error notes above)
  * are written as zeros.
  */

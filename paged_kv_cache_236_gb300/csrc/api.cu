@@ -265,6 +265,7 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   if (dtype != PKV_DTYPE_BF16 && dtype != PKV_DTYPE_F32) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", (int)dtype);
   if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_blocks <= 0 || bs <= 0 || max_blocks_per_seq <= 0)
     return fail(PKV_ERR_INVALID_ARG, "sizes must be positive (num_seqs, num_tokens >= 0)");
+  if (B > kMaxPlanSeqs) return fail(PKV_ERR_UNSUPPORTED, "more than %d sequences per call", kMaxPlanSeqs);
   if (Hq % Hkv != 0) return fail(PKV_ERR_INVALID_ARG, "num_q_heads (%d) %% num_kv_heads (%d) != 0", Hq, Hkv);
   if (Hq / Hkv > 128) return fail(PKV_ERR_UNSUPPORTED, "more than 128 q heads per kv head");
   if (D != 64 && D != 128) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", D);

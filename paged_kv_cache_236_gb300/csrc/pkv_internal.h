@@ -20,6 +20,7 @@ constexpr int kDecTileKeys = 64;  // keys per CUDA-core pipeline stage
 constexpr int kMmaRows = 128;     // rows per tensor-core work item (M of the MMA)
 constexpr int kMmaTileKeys = 128;  // keys per tensor-core pipeline stage
 constexpr int kMaxSplits = 64;
+constexpr int kMaxPlanSeqs = 32768;  // sequences per call (the planner keeps per-sequence offsets on chip)
 
 struct alignas(16) PlanHeader {
   int n_dec;        // CUDA-core work items

@@ -17,20 +17,24 @@
 // chunk), so that the attention kernels, which take items in list order,
 // end with small ones and finish together.
 //
-// One CTA of kThreads threads; each thread owns a contiguous range of
-// (sequence, kv head) pairs, and block-wide exclusive scans give every item
-// a fixed slot (items ordered by size class, then pair, then row unit and
-// split).
+// One CTA.  The unit instances (kv head, sequence, row unit) are numbered
+// kv head major, each sequence's units contiguous (per-sequence unit offsets
+// in shared memory); each thread walks a contiguous range of that numbering,
+// so that a long prefill sequence's many units spread over many threads.
+// Block-wide exclusive scans give every item a fixed slot (items ordered by
+// size class, then unit instance, then split).
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kClasses = 8;            // item size classes
-constexpr int kNumCounts = 2 * kClasses + 2;  // dec classes, mma classes, merges, partial rows
+constexpr int kClasses = 8;  // item size classes
+// per-thread counters: dec classes, mma classes, merge groups, partial rows (dec, mma)
+constexpr int kNumCounts = 2 * kClasses + 3;
+constexpr int kCntMerge = 2 * kClasses, kCntPartDec = 2 * kClasses + 1, kCntPartMma = 2 * kClasses + 2;
 
 struct SeqDesc {
   int n, L;
@@ -73,12 +77,14 @@ __device__ __forceinline__ int size_class(int keys, int chunk) {
   return min(max(c, 0), kClasses - 1);
 }
 
-// Block-wide exclusive scan of K ints per thread (in place); totals[] gets the sums.
+// Block-wide exclusive scan of K ints per thread (in place); totals[] gets the
+// sums.  Warp scans with shuffles; then K threads each scan one counter across
+// the warps' totals in shared memory.
 template <int K>
 __device__ void block_scan(int (&v)[K], int (&totals)[K]) {
   __shared__ int warp_tot[kWarps][K];
+  __shared__ int sum_tot[K];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl[K];
 #pragma unroll
   for (int k = 0; k < K; ++k) {
     int x = v[k];
@@ -87,65 +93,123 @@ __device__ void block_scan(int (&v)[K], int (&totals)[K]) {
       const int y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
-    incl[k] = x;
     if (lane == 31) warp_tot[warp][k] = x;
+    v[k] = x - v[k];  // exclusive within the warp
+  }
+  __syncthreads();
+  if (threadIdx.x < K) {
+    int run = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int x = warp_tot[w][threadIdx.x];
+      warp_tot[w][threadIdx.x] = run;
+      run += x;
+    }
+    sum_tot[threadIdx.x] = run;
   }
   __syncthreads();
 #pragma unroll
   for (int k = 0; k < K; ++k) {
-    int before = 0, tot = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const int t = warp_tot[w][k];
-      before += w < warp ? t : 0;
-      tot += t;
-    }
-    v[k] = before + incl[k] - v[k];
-    totals[k] = tot;
+    v[k] += warp_tot[warp][k];
+    totals[k] = sum_tot[k];
   }
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
+// Walks a contiguous range of unit instances i = kvh * U + seq_off[s] + u.
+struct UnitIter {
+  int i, end, U, B, kvh, s, u;
+  SeqDesc d;
+};
+
+__device__ __forceinline__ void iter_seek(UnitIter& t, const PlanParams& p, const int* seq_off) {
+  if (t.i >= t.end) return;
+  t.kvh = t.i / t.U;
+  const int j = t.i - t.kvh * t.U;
+  int lo = 0, hi = t.B - 1;  // the last sequence whose first unit is <= j
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (seq_off[mid] <= j) lo = mid; else hi = mid - 1;
+  }
+  t.s = lo;
+  t.u = j - seq_off[lo];
+  t.d = describe(p, lo);
+}
+
+__device__ __forceinline__ void iter_next(UnitIter& t, const PlanParams& p, const int* seq_off) {
+  ++t.i;
+  if (t.i >= t.end) return;
+  if (++t.u < t.d.units) return;
+  // next sequence with units (or the next kv head's first one)
+  int s = t.s + 1;
+  while (s < t.B && seq_off[s + 1] == seq_off[s]) ++s;
+  if (s >= t.B) {
+    ++t.kvh;
+    s = 0;
+    while (seq_off[s + 1] == seq_off[s]) ++s;
+  }
+  t.s = s;
+  t.u = 0;
+  t.d = describe(p, s);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   // The attention kernel may start its prologue while this plans (it waits
   // for this grid).  This grid waits for its own predecessor before reading
   // the metadata, which that predecessor may have produced.
   pdl_launch_dependents();
   pdl_wait();
+  extern __shared__ int seq_off[];  // [B + 1]: first unit of each sequence (per kv head)
   const int tid = threadIdx.x;
-  const int np = p.B * p.Hkv;  // (sequence, kv head) pairs
-  const int per_thread = (np + kThreads - 1) / kThreads;
-  const int q0 = min(np, tid * per_thread);
-  const int q1 = min(np, q0 + per_thread);
+  const int B = p.B;
 
-  // ---- total work per path (keys of all units of all pairs); zero the rows of invalid sequences
-  __shared__ unsigned long long sh_work[2];
-  __shared__ int sh_chunk[2];
-  __shared__ int sh_state;
-  if (tid < 2) sh_work[tid] = 0;
-  __syncthreads();
-  unsigned long long w_dec = 0, w_mma = 0;
-  for (int q = q0; q < q1; ++q) {
-    const int s = q / p.Hkv;
+  // ---- units per sequence; zero the rows of invalid sequences
+  for (int s = tid; s < B; s += kThreads) {
     const SeqDesc d = describe(p, s);
     if (!d.valid) {
-      if (q % p.Hkv == 0) {  // once per sequence
-        raise_error(p.err, PKV_DEVERR_BAD_SEQUENCE);
-        const int a = p.query_start_loc[s], b = p.query_start_loc[s + 1];
-        if (a >= 0 && b > a && (int64_t)b <= p.T) {  // zero the rows that are addressable
-          int4* o = reinterpret_cast<int4*>(static_cast<uint8_t*>(p.out) + (int64_t)a * p.out_row_bytes);
-          const int64_t n16 = (int64_t)(b - a) * p.out_row_bytes / 16;
-          for (int64_t i = 0; i < n16; ++i) o[i] = make_int4(0, 0, 0, 0);
-        }
+      raise_error(p.err, PKV_DEVERR_BAD_SEQUENCE);
+      const int a = p.query_start_loc[s], b = p.query_start_loc[s + 1];
+      if (a >= 0 && b > a && (int64_t)b <= p.T) {  // zero the rows that are addressable
+        int4* o = reinterpret_cast<int4*>(static_cast<uint8_t*>(p.out) + (int64_t)a * p.out_row_bytes);
+        const int64_t n16 = (int64_t)(b - a) * p.out_row_bytes / 16;
+        for (int64_t i = 0; i < n16; ++i) o[i] = make_int4(0, 0, 0, 0);
       }
-      continue;
     }
-    unsigned long long w = 0;
-    for (int u = 0; u < d.units; ++u) w += (unsigned long long)unit_keys(d, u, p.G, p.causal);
-    (d.mma ? w_mma : w_dec) += w;
+    seq_off[s] = d.units;  // 0 for an invalid sequence
+  }
+  __syncthreads();
+  {
+    // exclusive scan of seq_off[0 .. B) in place; seq_off[B] = units per kv head
+    const int per = (B + kThreads - 1) / kThreads;
+    const int s0 = min(B, tid * per), s1 = min(B, s0 + per);
+    int sum = 0;
+    for (int s = s0; s < s1; ++s) sum += seq_off[s];
+    int v[1] = {sum}, tot[1];
+    block_scan<1>(v, tot);
+    int run = v[0];
+    for (int s = s0; s < s1; ++s) {
+      const int x = seq_off[s];
+      seq_off[s] = run;
+      run += x;
+    }
+    if (tid == 0) seq_off[B] = tot[0];
+    __syncthreads();
+  }
+  const int U = seq_off[B];
+  const int N = U * p.Hkv;  // unit instances
+  const int per_thread = (N + kThreads - 1) / kThreads;
+  const int i0 = min(N, tid * per_thread), i1 = min(N, i0 + per_thread);
+
+  // ---- total keys per path, for the chunk sizes
+  __shared__ unsigned long long sh_wsum[kWarps][2];
+  __shared__ int sh_chunk[2];
+  __shared__ int sh_state;
+  unsigned long long w_dec = 0, w_mma = 0;
+  {
+    UnitIter t{i0, i1, U, B, 0, 0, 0, {}};
+    for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off))
+      (t.d.mma ? w_mma : w_dec) += (unsigned long long)unit_keys(t.d, t.u, p.G, p.causal);
   }
   // warp sums, then one thread adds the warps' (no contended 64-bit atomics)
-  __shared__ unsigned long long sh_wsum[kWarps][2];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     w_dec += __shfl_xor_sync(0xffffffffu, w_dec, o);
@@ -157,13 +221,14 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
   }
   __syncthreads();
   if (tid == 0) {
+    unsigned long long wd = 0, wm = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      sh_work[0] += sh_wsum[w][0];
-      sh_work[1] += sh_wsum[w][1];
+      wd += sh_wsum[w][0];
+      wm += sh_wsum[w][1];
     }
-    unsigned long long cd = (sh_work[0] + p.target_dec - 1) / (unsigned long long)max(1, p.target_dec);
-    unsigned long long cm = (sh_work[1] + p.target_mma - 1) / (unsigned long long)max(1, p.target_mma);
+    unsigned long long cd = (wd + p.target_dec - 1) / (unsigned long long)max(1, p.target_dec);
+    unsigned long long cm = (wm + p.target_mma - 1) / (unsigned long long)max(1, p.target_mma);
     cd = max(cd, (unsigned long long)p.min_chunk_dec);
     cm = max(cm, (unsigned long long)p.min_chunk_mma);
     cd = (cd + p.dec_tile_keys - 1) / p.dec_tile_keys * p.dec_tile_keys;
@@ -173,36 +238,50 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
   }
   __syncthreads();
 
-  // ---- grow chunks until the plan fits the workspace
+  // ---- count items per size class, merge groups and partial rows; grow the
+  // chunks until the plan fits the workspace
+  __shared__ int s_cnt[kNumCounts][kThreads];  // per-thread counters, then running offsets
+  int cnt[kNumCounts], tot[kNumCounts];
   for (int iter = 0;; ++iter) {
     const int cd = sh_chunk[0], cm = sh_chunk[1];
-    int c[5] = {0, 0, 0, 0, 0};  // dec items, mma items, merges, partial rows (dec), partial rows (mma)
-    for (int q = q0; q < q1; ++q) {
-      const SeqDesc d = describe(p, q / p.Hkv);
-      if (!d.valid || d.rows == 0) continue;
-      for (int u = 0; u < d.units; ++u) {
-        int ns, per;
-        split_of(unit_keys(d, u, p.G, p.causal), d.mma ? cm : cd, d.mma ? kMmaTileKeys : p.dec_tile_keys, ns, per);
-        c[d.mma ? 1 : 0] += ns;
-        if (ns > 1) {
-          c[2] += 1;
-          c[d.mma ? 4 : 3] += ns * min(d.rows - u * d.unit_rows, d.unit_rows);
-        }
+#pragma unroll
+    for (int k = 0; k < kNumCounts; ++k) s_cnt[k][tid] = 0;
+    UnitIter t{i0, i1, U, B, 0, 0, 0, {}};
+    for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off)) {
+      const SeqDesc& d = t.d;
+      const int chunk = d.mma ? cm : cd;
+      const int cb = d.mma ? kClasses : 0;
+      const int keys = unit_keys(d, t.u, p.G, p.causal);
+      int ns, per;
+      split_of(keys, chunk, d.mma ? kMmaTileKeys : p.dec_tile_keys, ns, per);
+      s_cnt[cb + size_class(per, chunk)][tid] += ns - 1;  // all splits but the last are full
+      s_cnt[cb + size_class(keys - (ns - 1) * per, chunk)][tid] += 1;
+      if (ns > 1) {
+        s_cnt[kCntMerge][tid] += 1;
+        s_cnt[d.mma ? kCntPartMma : kCntPartDec][tid] += ns * min(d.rows - t.u * d.unit_rows, d.unit_rows);
       }
     }
-    int tot[5];
-    block_scan<5>(c, tot);
+#pragma unroll
+    for (int k = 0; k < kNumCounts; ++k) cnt[k] = s_cnt[k][tid];
+    block_scan<kNumCounts>(cnt, tot);
     if (tid == 0) {
-      const bool fits = tot[0] <= p.dec_cap && tot[1] <= p.mma_cap && tot[2] <= p.merge_cap &&
-                        (int64_t)tot[3] + tot[4] <= p.part_cap;
+      int nd = 0, nm = 0;
+#pragma unroll
+      for (int k = 0; k < kClasses; ++k) {
+        nd += tot[k];
+        nm += tot[kClasses + k];
+      }
+      const int pd = tot[kCntPartDec], pm = tot[kCntPartMma];
+      const bool fits = nd <= p.dec_cap && nm <= p.mma_cap && tot[kCntMerge] <= p.merge_cap &&
+                        (int64_t)pd + pm <= p.part_cap;
       sh_state = fits ? 1 : 0;
       if (!fits) {
         if (iter >= 40) {
           raise_error(p.err, PKV_DEVERR_PLAN_OVERFLOW);
           sh_state = 2;
         }
-        const bool dec_over = tot[0] > p.dec_cap || tot[3] >= tot[4];
-        const bool mma_over = tot[1] > p.mma_cap || tot[4] > tot[3];
+        const bool dec_over = nd > p.dec_cap || pd >= pm;
+        const bool mma_over = nm > p.mma_cap || pm > pd;
         if (dec_over) sh_chunk[0] = (int)min(2LL * cd, (long long)(1 << 30));
         if (mma_over) sh_chunk[1] = (int)min(2LL * cm, (long long)(1 << 30));
       }
@@ -219,55 +298,28 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
     return;
   }
 
-  // ---- count items per size class, scan, emit largest class first
+  // ---- emit: class k's items start after all larger classes' (largest first)
   const int cd = sh_chunk[0], cm = sh_chunk[1];
-  __shared__ int s_ctr[kNumCounts][kThreads];  // per-thread counters, then running offsets
-#pragma unroll
-  for (int k = 0; k < kNumCounts; ++k) s_ctr[k][tid] = 0;
-  for (int q = q0; q < q1; ++q) {
-    const SeqDesc d = describe(p, q / p.Hkv);
-    if (!d.valid || d.rows == 0) continue;
-    const int chunk = d.mma ? cm : cd;
-    const int cb = d.mma ? kClasses : 0;
-    for (int u = 0; u < d.units; ++u) {
-      const int keys = unit_keys(d, u, p.G, p.causal);
-      int ns, per;
-      split_of(keys, chunk, d.mma ? kMmaTileKeys : p.dec_tile_keys, ns, per);
-      s_ctr[cb + size_class(per, chunk)][tid] += ns - 1;  // all splits but the last are full
-      s_ctr[cb + size_class(keys - (ns - 1) * per, chunk)][tid] += 1;
-      if (ns > 1) {
-        s_ctr[2 * kClasses][tid] += 1;
-        s_ctr[2 * kClasses + 1][tid] += ns * min(d.rows - u * d.unit_rows, d.unit_rows);
-      }
-    }
-  }
-  int cnt[kNumCounts];
-#pragma unroll
-  for (int k = 0; k < kNumCounts; ++k) cnt[k] = s_ctr[k][tid];
-  int tot[kNumCounts];
-  block_scan<kNumCounts>(cnt, tot);
   {
     int base_dec = 0, base_mma = 0;
 #pragma unroll
     for (int k = 0; k < kClasses; ++k) {
-      s_ctr[k][tid] = base_dec + cnt[k];
+      s_cnt[k][tid] = base_dec + cnt[k];
       base_dec += tot[k];
-      s_ctr[kClasses + k][tid] = base_mma + cnt[kClasses + k];
+      s_cnt[kClasses + k][tid] = base_mma + cnt[kClasses + k];
       base_mma += tot[kClasses + k];
     }
-    s_ctr[2 * kClasses][tid] = cnt[2 * kClasses];
-    s_ctr[2 * kClasses + 1][tid] = cnt[2 * kClasses + 1];
   }
-  int* off_grp = &s_ctr[2 * kClasses][tid];
-  int* off_part = &s_ctr[2 * kClasses + 1][tid];
-  for (int q = q0; q < q1; ++q) {
-    const int s = q / p.Hkv, kvh = q - s * p.Hkv;
-    const SeqDesc d = describe(p, s);
-    if (!d.valid || d.rows == 0) continue;
-    WorkItem* items = d.mma ? p.mma_items : p.dec_items;
-    const int chunk = d.mma ? cm : cd;
-    const int cbase = d.mma ? kClasses : 0;
-    for (int u = 0; u < d.units; ++u) {
+  int off_grp = cnt[kCntMerge];
+  int off_part = cnt[kCntPartDec] + cnt[kCntPartMma];
+  {
+    UnitIter t{i0, i1, U, B, 0, 0, 0, {}};
+    for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off)) {
+      const SeqDesc& d = t.d;
+      const int s = t.s, kvh = t.kvh, u = t.u;
+      WorkItem* items = d.mma ? p.mma_items : p.dec_items;
+      const int chunk = d.mma ? cm : cd;
+      const int cbase = d.mma ? kClasses : 0;
       const int keys = unit_keys(d, u, p.G, p.causal);
       const int r0 = u * d.unit_rows;
       const int nr = min(d.rows - r0, d.unit_rows);
@@ -275,9 +327,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
       split_of(keys, chunk, d.mma ? kMmaTileKeys : p.dec_tile_keys, ns, per);
       int grp = -1, part_base = 0;
       if (ns > 1) {
-        grp = (*off_grp)++;
-        part_base = *off_part;
-        *off_part += ns * nr;
+        grp = off_grp++;
+        part_base = off_part;
+        off_part += ns * nr;
         MergeGroup g;
         g.seq = s;
         g.kvh = kvh;
@@ -301,7 +353,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
         it.ke = min(keys, (sp + 1) * per);
         it.part = ns > 1 ? part_base + sp * nr : -1;
         it.grp = grp;
-        items[s_ctr[sp == ns - 1 ? last_cls : full_cls][tid]++] = it;
+        items[s_cnt[sp == ns - 1 ? last_cls : full_cls][tid]++] = it;
       }
     }
   }
@@ -314,10 +366,10 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
     }
     p.header->n_dec = nd;
     p.header->n_mma = nm;
-    p.header->n_merge = tot[2 * kClasses];
+    p.header->n_merge = tot[kCntMerge];
     p.header->chunk_dec = cd;
     p.header->chunk_mma = cm;
-    p.header->part_rows = tot[2 * kClasses + 1];
+    p.header->part_rows = tot[kCntPartDec] + tot[kCntPartMma];
     p.header->dec_counter = 0;
     p.header->mma_counter = 0;
     p.header->merge_counter = 0;
@@ -327,7 +379,20 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
 }  // namespace
 
 cudaError_t launch_planner(const PlanParams& p, cudaStream_t s) {
-  const cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(kThreads), 0, s, p);
+  const size_t smem = (size_t)(p.B + 1) * sizeof(int);
+  if (p.B > kMaxPlanSeqs) return cudaErrorInvalidValue;
+  static unsigned long long done_mask = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+    e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)((kMaxPlanSeqs + 1) * sizeof(int)));
+    if (e != cudaSuccess) return e;
+    __atomic_fetch_or(&done_mask, 1ull << dev, __ATOMIC_RELEASE);
+  }
+  e = launch_pdl(plan_kernel, dim3(1), dim3(kThreads), smem, s, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
