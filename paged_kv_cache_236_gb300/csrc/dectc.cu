@@ -18,7 +18,7 @@
 // so one thread per key does the softmax arithmetic for its key (16 values)
 // and one thread per output column writes the result, coalesced.
 //
-// Roles (320 threads, one CTA per SM, persistent, items from an atomic
+// Roles (352 threads, one CTA per SM, persistent, items from an atomic
 // counter in the planner's largest-first order):
 //   warp 0    TMA producer: per 128-key tile one {64, 1, block_size, 1} box
 //             per physical block and 64-column half of K and V (128-byte
@@ -28,7 +28,12 @@
 //   warp 1    TMEM allocation and the single thread issuing the MMAs; the
 //             P.V of tile g is issued after the S of tile g+1;
 //   warps 2-5 softmax (thread = key = TMEM lane) and epilogue (thread =
-//             output column = TMEM lane of O^T).
+//             output column = TMEM lane of O^T);
+//   warp 10   item fetch: up to two items ahead, it reads each item's record,
+//             its sequence's length and query offset and the block ids of
+//             its first tile into a slot in shared memory, so that the
+//             producer starts an item's loads without a chain of dependent
+//             global reads.
 // Shared memory: 3 stages of K+V (192 KB), 2 Q tiles and 2 P tiles (4 KB
 // each).  TMEM: S^T double-buffered in columns [0,32), O^T in [32,48).
 #include <math_constants.h>
@@ -40,7 +45,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kStages = 3;
 constexpr int kKeys = kMmaTileKeys;            // 128 keys per tile
 constexpr int kN = kTcDecRows;                 // 16 rows (MMA N)
@@ -52,8 +57,9 @@ constexpr int kPOff = kQOff + 2 * 2 * kQHalf;
 constexpr int kMetaOff = kPOff + 2 * 2 * kQHalf;
 constexpr int kRedOff = kMetaOff + kStages * 64;
 constexpr int kSlotOff = kRedOff + 2 * 4 * kN * 4;
-constexpr int kBarOff = kSlotOff + 2 * 256;
-constexpr int kNumBars = 3 * kStages + 2 * 8;
+constexpr int kISlotOff = kSlotOff + 2 * 256;  // 2 item slots
+constexpr int kBarOff = kISlotOff + 2 * 192;
+constexpr int kNumBars = 3 * kStages + 2 * 8 + 4;
 constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
 constexpr uint32_t kTmemCols = 64;
 constexpr uint32_t kSCol = 0, kOCol = 32;
@@ -75,7 +81,17 @@ struct Bars {
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t o_full[2], o_empty[2], ml_full[2], ml_empty[2];
+  uint64_t islot_full[2], islot_free[2];
 };
+
+// An item as the item-fetch warp hands it to the producer.
+struct alignas(16) ItemSlot {
+  WorkItem it;
+  int idx, L, qstart, n;
+  int done, pad[3];
+  int phys0[32];  // physical block of each of the item's first tile's blocks
+};
+static_assert(sizeof(ItemSlot) == 192, "item slot");
 
 // What the softmax warps hand the epilogue at an item's end.
 struct alignas(16) EpSlot {
@@ -146,7 +162,6 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNumBars * 8);
-  int* flag_last = reinterpret_cast<int*>(tmem_slot + 1);
   Meta* meta = reinterpret_cast<Meta*>(smem + kMetaOff);
   float* red = reinterpret_cast<float*>(smem + kRedOff);  // [2][4 warps][NR rows]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -168,6 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
       mbar_init(&bars->o_empty[b], 128);
       mbar_init(&bars->ml_full[b], 128);
       mbar_init(&bars->ml_empty[b], 128);
+      mbar_init(&bars->islot_full[b], 32);
+      mbar_init(&bars->islot_free[b], 1);
     }
     fence_mbar_init();
   }
@@ -191,12 +208,19 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
       prefetch_tensormap(&vmap);
     }
     const int nb_per_tile = kKeys / p.bs;
-    int g = 0, it_cnt = 0;
-    int idx = 0;
-    if (lane == 0) idx = atomicAdd(p.counter, 1);
-    idx = __shfl_sync(0xffffffffu, idx, 0);
-    for (;;) {
-      if (idx >= n_items) {
+    const ItemSlot* islots = reinterpret_cast<const ItemSlot*>(smem + kISlotOff);
+    int g = 0;
+    for (int it_cnt = 0;; ++it_cnt) {
+      const int qb = it_cnt & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->islot_full[qb], (it_cnt >> 1) & 1, p.err))) break;
+      const ItemSlot& isl = islots[qb];
+      const bool done = isl.done != 0;
+      const WorkItem it = isl.it;
+      const int idx = isl.idx, L = isl.L, qstart = isl.qstart, n = isl.n;
+      int phys = isl.phys0[lane];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->islot_free[qb]);
+      if (done) {
         const int st = g % kStages;
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->kv_empty[st], ((g / kStages) & 1) ^ 1, p.err))) break;
         if (lane == 0) {
@@ -206,27 +230,20 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
         }
         break;
       }
-      const WorkItem it = p.items[idx];
-      int next = 0;
-      if (lane == 0) next = atomicAdd(p.counter, 1);  // consumed after this item's tiles
-      const int L = p.context_lens[it.seq];
-      const int qstart = p.query_start_loc[it.seq];
-      const int n = p.query_start_loc[it.seq + 1] - qstart;
       const int nblk = (L + p.bs - 1) / p.bs;
       const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
       auto block_of = [&](int kbase) -> int {  // physical block of this lane's block in the tile
         const int lb = kbase / p.bs + lane;
-        int phys = (int)p.num_blocks;  // out of range: the box reads as zeros
+        int phys_ = (int)p.num_blocks;  // out of range: the box reads as zeros
         if (lane < nb_per_tile && lb < nblk) {
           const int b = __ldg(bt + lb);
           if (b >= 0 && (int64_t)b < p.num_blocks)
-            phys = b;
+            phys_ = b;
           else
             raise_error(p.err, PKV_DEVERR_BLOCK_OUT_OF_RANGE);
         }
-        return phys;
+        return phys_;
       };
-      int phys = block_of(it.kb);
       bool ok = true;
       for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
         const int st = g % kStages;
@@ -274,8 +291,49 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
         phys = next_phys;
       }
       if (!ok) break;
-      ++it_cnt;
-      idx = __shfl_sync(0xffffffffu, next, 0);
+    }
+  } else if (warp == 10) {
+    // ================================================================ item fetch
+    const int nb_per_tile = kKeys / p.bs;
+    ItemSlot* islots = reinterpret_cast<ItemSlot*>(smem + kISlotOff);
+    int next = 0;
+    if (lane == 0) next = atomicAdd(p.counter, 1);
+    for (int c = 0;; ++c) {
+      const int qb = c & 1;
+      // slot qb is free once the producer has read item c-2 from it
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->islot_free[qb], ((c >> 1) & 1) ^ 1, p.err))) break;
+      const int idx = __shfl_sync(0xffffffffu, next, 0);
+      ItemSlot& isl = islots[qb];
+      if (idx >= n_items) {
+        if (lane == 0) isl.done = 1;
+        mbar_arrive(&bars->islot_full[qb]);  // every lane: count 32
+        break;
+      }
+      const WorkItem it = p.items[idx];
+      if (lane == 0) next = atomicAdd(p.counter, 1);  // consumed at the next item
+      const int L = p.context_lens[it.seq];
+      const int qstart = p.query_start_loc[it.seq];
+      const int n = p.query_start_loc[it.seq + 1] - qstart;
+      const int nblk = (L + p.bs - 1) / p.bs;
+      const int lb = it.kb / p.bs + lane;
+      int phys = (int)p.num_blocks;  // out of range: the box reads as zeros
+      if (lane < nb_per_tile && lb < nblk) {
+        const int b = __ldg(p.block_tables + (int64_t)it.seq * p.max_blocks + lb);
+        if (b >= 0 && (int64_t)b < p.num_blocks)
+          phys = b;
+        else
+          raise_error(p.err, PKV_DEVERR_BLOCK_OUT_OF_RANGE);
+      }
+      isl.phys0[lane] = phys;
+      if (lane == 0) {
+        isl.it = it;
+        isl.idx = idx;
+        isl.L = L;
+        isl.qstart = qstart;
+        isl.n = n;
+        isl.done = 0;
+      }
+      mbar_arrive(&bars->islot_full[qb]);  // every lane, after its own writes
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
