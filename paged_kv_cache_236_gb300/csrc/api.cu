@@ -337,7 +337,11 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   pp.dec_rows_max = dec_rows_max;
   pp.dec_unit_rows = dectc ? tc_rows : kDecRows;
   pp.dec_tile_keys = dectc ? kMmaTileKeys : kDecTileKeys;
-  pp.target_dec = dectc ? dev->sms * 6 : dec_grid * 4;
+  // Four items per CTA of the decode kernels: fewer, longer items cost less
+  // per item (pipeline restarts, partial writes, merges) than a finer tail
+  // saves (measured on the decode, mixed and long-context batches).
+  pp.target_dec = dectc ? dev->sms * 4 : dec_grid * 4;
+  pp.dec_ctas = dectc ? dev->sms : dec_grid;
   // Items are fetched dynamically in largest-first order, so two per SM
   // balance the tensor-core kernel; every split costs a partial write and a
   // merge, so no more are made than that.

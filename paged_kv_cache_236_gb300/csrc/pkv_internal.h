@@ -75,6 +75,7 @@ struct PlanParams {
   int dec_unit_rows;  // rows per decode-shaped item (4 CUDA-core, 16 tensor-core)
   int dec_tile_keys;  // key tile of the decode-shaped kernel (splits are multiples)
   int target_dec, target_mma;  // desired item counts
+  int dec_ctas;     // CTAs of the decode-shaped kernel (one wave of items)
   int min_chunk_dec, min_chunk_mma;
   int dec_cap, mma_cap, merge_cap, part_cap;
   PlanHeader* header;

@@ -275,6 +275,16 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       const bool fits = nd <= p.dec_cap && nm <= p.mma_cap && tot[kCntMerge] <= p.merge_cap &&
                         (int64_t)pd + pm <= p.part_cap;
       sh_state = fits ? 1 : 0;
+      // Once: if the decode items are mostly full chunks (long sequences
+      // split) and leave a last wave less than half full, grow the chunk so
+      // that the count drops to whole waves.  Items of mixed sizes are left
+      // to the largest-first order.
+      const int P = max(1, p.dec_ctas), extra = nd % P;
+      if (fits && iter == 0 && nd > P && extra > 0 && 2 * extra <= P && 4 * tot[0] >= 3 * nd) {
+        const long long grown = ((long long)cd * nd + (nd - extra) - 1) / (nd - extra);
+        sh_chunk[0] = (int)min((grown + p.dec_tile_keys - 1) / p.dec_tile_keys * p.dec_tile_keys, (long long)(1 << 30));
+        sh_state = 0;
+      }
       if (!fits) {
         if (iter >= 40) {
           raise_error(p.err, PKV_DEVERR_PLAN_OVERFLOW);
