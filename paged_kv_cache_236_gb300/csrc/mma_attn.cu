@@ -13,40 +13,36 @@
 //   finish merges the group (atomic ticket, no waiting).
 //
 // Tile shape and issue order follow the tensor pipe's behaviour on sm_103a:
-// an M=128 MMA with N=64 costs about as long as one with N=128, and a chain
-// of MMAs accumulating into one TMEM region runs at about two thirds of the
-// peak rate when nothing else is queued, near the peak when a second,
-// independent chain is queued beside it; the issuing thread cannot run
-// ahead of the pipe: issuing one M=128, N=128 MMA takes about as long as
-// running it, so every wait or commit between MMAs leaves the pipe idle.  So
-// a tile is 128 keys (N=128 for Q K^T), and per tile the MMA thread does its
-// waits first (one instruction when all are already satisfied), then issues
-// the P.V of tile t directly followed by the Q K^T of tile t+2 and commits
-// both to one barrier, while the softmax warps work on tile t+1.  That
-// barrier (phase of "block" t) tells the softmax warps that S(t+2) is ready
-// and P buffer t % 2 free, the K producer that K stage t % 2 is free, and the
-// epilogue that O is complete.
+// an M=128 MMA with N=64 costs about as long as one with N=128; a chain of
+// MMAs accumulating into one TMEM region runs at about two thirds of the peak
+// rate alone, at the peak when a second, independent chain runs beside it,
+// whether one thread or two issue them; and one thread cannot issue faster
+// than the pipe runs, so every wait or commit between its MMAs leaves the
+// pipe idle.  So a tile is 128 keys (N=128 for Q K^T), and two threads issue
+// the MMAs, each with its own waits: one the Q K^T chains, as soon as the
+// softmax warps have read the S buffer it writes, the other the P.V chains,
+// as soon as their P is written.  Either one's waits overlap the other's MMAs.
 //
 // Roles (384 threads, one CTA per SM, persistent; items are taken from an
 // atomic counter in the planner's largest-first order, so SMs that run
 // slower take fewer):
-//   warp 0    item fetch and Q producer: publishes each item in a slot of
-//             shared memory with its Q tile (3-D box {64, G heads, 128/G
-//             tokens} of q [T, Hq, D], two 64-column halves) as soon as a Q
-//             buffer is free, up to two items ahead;
-//   warp 1    TMEM allocation and the single thread issuing the MMAs;
+//   warp 0    the thread issuing P.V (O += P V, P from TMEM, V from shared memory);
+//   warp 1    TMEM allocation and the thread issuing Q K^T (S = Q K^T);
 //   warps 2-9 softmax / correction / epilogue: two threads per row (TMEM
 //             lane), warps 2-5 on key columns 0-63 of a tile, warps 6-9 on
 //             64-127; a pair exchanges row maxima (and at the end row sums)
 //             through shared memory;
-//   warp 10   K producer: per tile one {64, 1, block_size, 1} box of the pool
-//             [NB, bs, Hkv, D] per physical block and 64-column half
-//             (128-byte swizzle, the layout the tensor core reads); block ids
-//             are loaded a tile ahead;
+//   warp 10   item fetch, Q and K: publishes each item in a slot of shared
+//             memory (with the block ids of its first key tile), loads its Q
+//             tile (3-D box {64, G heads, 128/G tokens} of q [T, Hq, D], two
+//             64-column halves), then its K tiles: per tile one
+//             {64, 1, block_size, 1} box of the pool [NB, bs, Hkv, D] per
+//             physical block and 64-column half (128-byte swizzle, the layout
+//             the tensor core reads), block ids loaded a tile ahead;
 //   warp 11   V producer, the same boxes from the V pool.
-// Shared memory: 2 Q tiles (64 KB), a 2-stage ring of K tiles (64 KB) and a
-// 3-stage ring of V tiles (96 KB); K of a tile is released when its Q K^T is
-// done, V when its P.V is done, so each ring refills as early as it can.
+// Shared memory: 2 Q tiles (64 KB), a 3-stage ring of K tiles (96 KB) and a
+// 2-stage ring of V tiles (64 KB); K of a tile is released when its Q K^T is
+// done, V when its P.V is done (K is needed two tiles ahead of V).
 // TMEM (512 columns): S double-buffered in [0,256), P (32 columns of packed
 // bf16 per 64 keys) double-buffered in [256,384), O in [384,512).
 //
@@ -64,7 +60,7 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kKeys = kMmaTileKeys;                 // 128 keys per tile
-constexpr int kKStages = 2, kVStages = 3;
+constexpr int kKStages = 3, kVStages = 2;
 constexpr int kHalfKV = kKeys * 128;                // one 64-column half of a K or V tile (16 KB)
 constexpr int kTileBytes = 2 * kHalfKV;             // K or V tile: 32 KB
 constexpr int kQBytes = kMmaRows * 128 * 2;         // 32 KB (two 16 KB halves)
@@ -73,9 +69,9 @@ constexpr int kQOff = 0;
 constexpr int kKOff = kQOff + 2 * kQBytes;
 constexpr int kVOff = kKOff + kKStages * kTileBytes;
 constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-constexpr int kNumBars = 6 + kKStages + 2 * kVStages + 4 + 1;
+constexpr int kNumBars = 8 + 2 * kKStages + kVStages + 8 + 1;
 constexpr int kSlotOff = (kBarOff + kNumBars * 8 + 16 + 15) & ~15;  // 2 item slots
-constexpr int kRedOff = kSlotOff + 2 * 64;          // [2 tiles][2 halves][128 rows] row maxima / sums
+constexpr int kRedOff = kSlotOff + 2 * 176;         // [2 tiles][2 halves][128 rows] row maxima / sums
 // No alignment slack: the buffers need a 1024-byte aligned base, which the
 // dynamic shared memory of a kernel without static shared memory has; the
 // kernel checks and refuses to run otherwise.
@@ -94,27 +90,29 @@ constexpr uint32_t kIdescO = idesc_bf16(128, 128, false, true);
 __device__ __forceinline__ uint64_t desc_v(uint32_t saddr) { return smem_desc(saddr, kHalfKV, 1024); }
 
 struct Bars {
-  uint64_t q_full[2], q_empty[2], slot_free[2];
-  uint64_t k_full[kKStages];
-  uint64_t v_full[kVStages], v_empty[kVStages];
-  // blk[b], phase n: S of tile 2n+b complete, and with it every MMA issued
-  // before (the P.V of tile 2n+b-2 in particular)
-  uint64_t blk[2], p_full[2];
+  uint64_t q_full[2], q_empty[2], slot_full[2], slot_free[2];
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  // s_full[b], phase n: S of tile 2n+b complete; s_free[b]: the softmax
+  // warps have read it.  pv_done[b], phase n: the P.V of tile 2n+b complete,
+  // and with it every earlier P.V.
+  uint64_t s_full[2], s_free[2], pv_done[2], p_full[2];
   uint64_t o_empty;
 };
 
-// An item's description, published by the item-fetching warp with its Q tile.
+// An item's description, published by the item-fetching warp before its Q
+// tile is loaded (slot_full), with the block ids of its first key tile.
 struct alignas(16) ItemSlot {
   WorkItem it;
   int L, qstart, n, done;
-  int pad[4];
+  int phys0[32];
 };
-// readers of a slot: the 256 softmax threads, the MMA thread, the K and V producers
+// readers of a slot: the 256 softmax threads, the two MMA-issuing threads, the V producer
 constexpr int kSlotReaders = 256 + 1 + 1 + 1;
 
-static_assert(sizeof(ItemSlot) == 64, "item slot");
+static_assert(sizeof(ItemSlot) == 176, "item slot");
 static_assert(sizeof(Bars) == kNumBars * 8, "barrier block");
-static_assert(kKStages == 2, "K stage t % 2 is released by the S barrier of tile t");
+static_assert(kVStages == 2, "V stage t % 2 is released by the P.V barrier of tile t");
 static_assert(kSmem <= 232448, "shared memory");
 static_assert(kKOff % 1024 == 0 && kVOff % 1024 == 0 && kTileBytes % 1024 == 0 && kQBytes % 1024 == 0,
               "swizzled tiles");
@@ -151,15 +149,18 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->q_full[b], 1);
       mbar_init(&bars->q_empty[b], 1);
+      mbar_init(&bars->slot_full[b], 32);
       mbar_init(&bars->slot_free[b], kSlotReaders);
-      mbar_init(&bars->blk[b], 1);
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->s_free[b], 256);
+      mbar_init(&bars->pv_done[b], 1);
       mbar_init(&bars->p_full[b], 256);
     }
-    for (int s = 0; s < kKStages; ++s) mbar_init(&bars->k_full[s], 1);
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
     }
+    for (int s = 0; s < kVStages; ++s) mbar_init(&bars->v_full[s], 1);
     mbar_init(&bars->o_empty, 256);
     fence_mbar_init();
   }
@@ -194,187 +195,178 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
     return phys;
   };
 
-  if (warp == 0) {
-    // ================================================================ item fetch and Q
+  if (warp == 10) {
+    // ================================================================ item fetch, Q and K
     if (lane == 0) {
       prefetch_tensormap(&qmap);
-      int next = atomicAdd(p.counter, 1);
-      for (int c = 0;; ++c) {
-        const int idx = next;
-        const int qb = c & 1;
-        // slot and Q tile qb: free once item c-2's last Q K^T has completed and
-        // every reader has taken its description
-        if (!mbar_wait(&bars->q_empty[qb], ((c >> 1) & 1) ^ 1, p.err) ||
-            !mbar_wait(&bars->slot_free[qb], ((c >> 1) & 1) ^ 1, p.err))
-          break;
-        if (idx >= n_items) {
-          slots[qb].done = 1;
-          mbar_arrive(&bars->q_full[qb]);
-          break;
-        }
-        const WorkItem it = p.items[idx];
-        next = atomicAdd(p.counter, 1);  // consumed at the next item
-        const int qstart = p.query_start_loc[it.seq];
-        ItemSlot& sl = slots[qb];
+      prefetch_tensormap(&kmap);
+    }
+    int next = 0;
+    if (lane == 0) next = atomicAdd(p.counter, 1);
+    int g = 0;
+    bool ok = true;
+    for (int c = 0; ok; ++c) {
+      const int qb = c & 1;
+      // slot and Q tile qb: free once item c-2's last Q K^T has completed and
+      // every reader has taken its description
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_empty[qb], ((c >> 1) & 1) ^ 1, p.err) &&
+                                       mbar_wait(&bars->slot_free[qb], ((c >> 1) & 1) ^ 1, p.err)))
+        break;
+      const int idx = __shfl_sync(0xffffffffu, next, 0);
+      ItemSlot& sl = slots[qb];
+      if (idx >= n_items) {
+        if (lane == 0) sl.done = 1;
+        mbar_arrive(&bars->slot_full[qb]);  // every lane: count 32
+        if (lane == 0) mbar_arrive(&bars->q_full[qb]);
+        break;
+      }
+      const WorkItem it = p.items[idx];
+      if (lane == 0) next = atomicAdd(p.counter, 1);  // consumed at the next item
+      const int L = p.context_lens[it.seq];
+      const int qstart = p.query_start_loc[it.seq];
+      const int nblk = (L + p.bs - 1) / p.bs;
+      const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
+      int phys = block_of(bt, nblk, it.kb);
+      sl.phys0[lane] = phys;
+      if (lane == 0) {
         sl.it = it;
-        sl.L = p.context_lens[it.seq];
+        sl.L = L;
         sl.qstart = qstart;
         sl.n = p.query_start_loc[it.seq + 1] - qstart;
         sl.done = 0;
+      }
+      mbar_arrive(&bars->slot_full[qb]);  // every lane, after its own writes
+      if (lane == 0) {
         mbar_arrive_expect_tx(&bars->q_full[qb], kQBytes);
         const int tok0 = qstart + it.row0 / p.G;
         tma_load_3d(smem + kQOff + qb * kQBytes, &qmap, &bars->q_full[qb], 0, it.kvh * p.G, tok0);
         tma_load_3d(smem + kQOff + qb * kQBytes + kHalf, &qmap, &bars->q_full[qb], 64, it.kvh * p.G, tok0);
       }
+      for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
+        const int st = g % kKStages;
+        const int next_phys = (kbase + kKeys < it.ke) ? block_of(bt, nblk, kbase + kKeys) : 0;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_empty[st], ((g / kKStages) & 1) ^ 1, p.err))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
+        __syncwarp();
+        if (lane < nb) {
+          uint8_t* d = smem + kKOff + st * kTileBytes + lane * p.bs * 128;
+          tma_load_4d(d, &kmap, &bars->k_full[st], 0, it.kvh, 0, phys);
+          tma_load_4d(d + kHalfKV, &kmap, &bars->k_full[st], 64, it.kvh, 0, phys);
+        }
+        phys = next_phys;
+      }
     }
-    __syncwarp();
-  } else if (warp >= 10) {
-    // ================================================================ K (warp 10) or V (warp 11)
-    const bool is_k = warp == 10;
-    const CUtensorMap* map = is_k ? &kmap : &vmap;
-    const int nstages = is_k ? kKStages : kVStages;
-    uint64_t* full = is_k ? bars->k_full : bars->v_full;
-    // K stage g % 2 is free once S(g-2) is complete (phase of blk[g % 2])
-    uint64_t* empty = is_k ? bars->blk : bars->v_empty;
-    uint8_t* ring = smem + (is_k ? kKOff : kVOff);
-    if (lane == 0) prefetch_tensormap(map);
+  } else if (warp == 11) {
+    // ================================================================ V
+    if (lane == 0) prefetch_tensormap(&vmap);
     int g = 0;
     bool ok = true;
     for (int c = 0; ok; ++c) {
       const int qb = c & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_full[qb], (c >> 1) & 1, p.err))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->slot_full[qb], (c >> 1) & 1, p.err))) break;
       const bool done = slots[qb].done != 0;
       const WorkItem it = slots[qb].it;
       const int L = slots[qb].L;
+      int phys = slots[qb].phys0[lane];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->slot_free[qb]);
       if (done) break;
       const int nblk = (L + p.bs - 1) / p.bs;
       const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
-      int phys = block_of(bt, nblk, it.kb);
       for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
-        const int st = g % nstages, ph = (g / nstages) & 1;
+        const int st = g % kVStages;
         const int next_phys = (kbase + kKeys < it.ke) ? block_of(bt, nblk, kbase + kKeys) : 0;
-        if (!__all_sync(0xffffffffu, mbar_wait(&empty[st], ph ^ 1, p.err))) {
+        // V stage g % 2 is free once P.V(g-2) is complete (phase of pv_done[g % 2])
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[st], ((g / kVStages) & 1) ^ 1, p.err))) {
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
+        if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
         __syncwarp();
         if (lane < nb) {
-          uint8_t* d = ring + st * kTileBytes + lane * p.bs * 128;
-          tma_load_4d(d, map, &full[st], 0, it.kvh, 0, phys);
-          tma_load_4d(d + kHalfKV, map, &full[st], 64, it.kvh, 0, phys);
+          uint8_t* d = smem + kVOff + st * kTileBytes + lane * p.bs * 128;
+          tma_load_4d(d, &vmap, &bars->v_full[st], 0, it.kvh, 0, phys);
+          tma_load_4d(d + kHalfKV, &vmap, &bars->v_full[st], 64, it.kvh, 0, phys);
         }
         phys = next_phys;
       }
     }
   } else if (warp == 1) {
-    // ================================================================ MMA issuer
+    // ================================================================ Q K^T issuer
     if (lane == 0) {
-      // descriptors of stage 0 / buffer 0; others are offsets of these
       const uint64_t dq = desc_k(smem_base + kQOff);
       const uint64_t dk0 = desc_k(smem_base + kKOff);
-      const uint64_t dv0 = desc_v(smem_base + kVOff);
-      // Q K^T iterator (two tiles ahead) and P.V iterator over this CTA's tiles
       int gs = 0, s_item = -1, s_j = 0, s_nt = 0;
-      bool s_done = false;
-      int gp = 0, p_item = 0;  // P.V iterator: tile, item
-      // bit (g & 7): tile g is the first / the last of its item (the S
-      // iterator runs at most three tiles ahead; registers, not local memory)
-      uint32_t first_bits = 0, last_bits = 0;
-      // Item bookkeeping for the next S: false when no tile is left (or on a
-      // timeout, with ok cleared).
-      bool ok = true;
-      auto s_next = [&]() -> bool {
-        if (s_done) return false;
-        if (s_j == s_nt) {  // next item
+      for (;;) {
+        if (s_j == s_nt) {  // next item: its Q tile loaded (its slot written before)
           ++s_item;
           const int qb = s_item & 1;
-          if (!mbar_wait(&bars->q_full[qb], (s_item >> 1) & 1, p.err)) {
-            ok = false;
-            return false;
-          }
+          if (!mbar_wait(&bars->q_full[qb], (s_item >> 1) & 1, p.err)) break;
           const bool done = slots[qb].done != 0;
           const int nt = (slots[qb].it.ke - slots[qb].it.kb + kKeys - 1) / kKeys;
           mbar_arrive(&bars->slot_free[qb]);
-          if (done) {
-            s_done = true;
-            return false;
-          }
+          if (done) break;
           s_nt = nt;
           s_j = 0;
         }
-        return true;
-      };
-      // k-step kk of S(gs) into S buffer gs % 2 (K loaded; the buffer's
-      // previous S was read before P of its tile was signalled, which the
-      // caller has waited for)
-      auto s_mma = [&](int kk) {
+        const int sb = gs & 1, st = gs % kKStages;
+        // S buffer sb: the softmax warps have read S(gs-2) from it; K(gs) loaded
+        if (!mbar_test_wait3(&bars->s_free[sb], ((gs >> 1) & 1) ^ 1, &bars->k_full[st], (gs / kKStages) & 1,
+                             &bars->k_full[st], (gs / kKStages) & 1) &&
+            (!mbar_wait(&bars->s_free[sb], ((gs >> 1) & 1) ^ 1, p.err) ||
+             !mbar_wait(&bars->k_full[st], (gs / kKStages) & 1, p.err)))
+          break;
+        tc_fence_after();
         const uint64_t dqb = desc_add(dq, (s_item & 1) * kQBytes);
-        const uint64_t dk = desc_add(dk0, (gs % kKStages) * kTileBytes);
-        umma_bf16(tmem + kSCol + 128 * (gs & 1), desc_add(dqb, (kk >> 2) * kHalf + (kk & 3) * 32),
-                  desc_add(dk, (kk >> 2) * kHalfKV + (kk & 3) * 32), kIdescS, kk > 0 ? 1u : 0u);
-      };
-      // bookkeeping once S(gs) is issued
-      auto s_done_tile = [&]() {
-        const uint32_t bit = 1u << (gs & 7);
-        first_bits = s_j == 0 ? (first_bits | bit) : (first_bits & ~bit);
-        last_bits = s_j == s_nt - 1 ? (last_bits | bit) : (last_bits & ~bit);
+        const uint64_t dk = desc_add(dk0, st * kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16(tmem + kSCol + 128 * sb, desc_add(dqb, (kk >> 2) * kHalf + (kk & 3) * 32),
+                    desc_add(dk, (kk >> 2) * kHalfKV + (kk & 3) * 32), kIdescS, kk > 0 ? 1u : 0u);
+        umma_commit(&bars->s_full[sb]);
+        umma_commit(&bars->k_empty[st]);
         if (s_j == s_nt - 1) umma_commit(&bars->q_empty[s_item & 1]);  // Q no longer read by this item
         ++s_j;
         ++gs;
-      };
-      // S(0), S(1)
-      for (int i = 0; i < 2 && s_next(); ++i) {
-        if (!mbar_wait(&bars->k_full[gs % kKStages], (gs / kKStages) & 1, p.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) s_mma(kk);
-        s_done_tile();
-        umma_commit(&bars->blk[(gs - 1) & 1]);
       }
-      // block t: P.V(t) and S(t+2), their MMAs interleaved (two independent
-      // accumulation chains keep the pipe busier than one after the other),
-      // one commit
-      while (ok && gp < gs) {
-        const uint32_t bit = 1u << (gp & 7);
-        const bool first = (first_bits & bit) != 0, last = (last_bits & bit) != 0;
-        if (first && !mbar_wait(&bars->o_empty, (p_item & 1) ^ 1, p.err)) break;  // O read by item p_item-1
-        const bool more = s_next();
-        if (!ok) break;
-        const int pb = gp & 1, vst = gp % kVStages;
-        uint64_t* wk = &bars->k_full[gs % kKStages];
-        const uint32_t pk_ = (gs / kKStages) & 1;
-        if (!mbar_test_wait3(&bars->p_full[pb], (gp >> 1) & 1, &bars->v_full[vst], (gp / kVStages) & 1,
-                             more ? wk : &bars->p_full[pb], more ? pk_ : ((gp >> 1) & 1))) {
-          if (!mbar_wait(&bars->p_full[pb], (gp >> 1) & 1, p.err) ||
-              !mbar_wait(&bars->v_full[vst], (gp / kVStages) & 1, p.err) || (more && !mbar_wait(wk, pk_, p.err)))
+    }
+    __syncwarp();
+  } else if (warp == 0) {
+    // ================================================================ P.V issuer
+    if (lane == 0) {
+      const uint64_t dv0 = desc_v(smem_base + kVOff);
+      int gp = 0;
+      bool ok = true;
+      for (int c = 0; ok; ++c) {
+        const int qb = c & 1;
+        if (!mbar_wait(&bars->slot_full[qb], (c >> 1) & 1, p.err)) break;
+        const bool done = slots[qb].done != 0;
+        const int nt = (slots[qb].it.ke - slots[qb].it.kb + kKeys - 1) / kKeys;
+        mbar_arrive(&bars->slot_free[qb]);
+        if (done) break;
+        // O is about to be overwritten: item c-1's epilogue must have read it
+        if (!mbar_wait(&bars->o_empty, (c & 1) ^ 1, p.err)) break;
+        for (int j = 0; j < nt; ++j, ++gp) {
+          const int pb = gp & 1, vst = gp % kVStages;
+          // P(gp) written, V(gp) loaded
+          if (!mbar_test_wait3(&bars->p_full[pb], (gp >> 1) & 1, &bars->v_full[vst], (gp / kVStages) & 1,
+                               &bars->v_full[vst], (gp / kVStages) & 1) &&
+              (!mbar_wait(&bars->p_full[pb], (gp >> 1) & 1, p.err) ||
+               !mbar_wait(&bars->v_full[vst], (gp / kVStages) & 1, p.err))) {
+            ok = false;
             break;
-        }
-        tc_fence_after();
-        const uint64_t dv = desc_add(dv0, vst * kTileBytes);
-        if (more) {
-#pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
-            umma_bf16_ts(tmem + kOCol, tmem + kPCol + 64 * pb + kk * 8, desc_add(dv, kk * 2048), kIdescO,
-                         (first && kk == 0) ? 0u : 1u);
-            s_mma(kk);
           }
-          s_done_tile();
-        } else {
+          tc_fence_after();
+          const uint64_t dv = desc_add(dv0, vst * kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk)
             umma_bf16_ts(tmem + kOCol, tmem + kPCol + 64 * pb + kk * 8, desc_add(dv, kk * 2048), kIdescO,
-                         (first && kk == 0) ? 0u : 1u);
+                         (j == 0 && kk == 0) ? 0u : 1u);
+          umma_commit(&bars->pv_done[pb]);  // P.V(gp) complete: frees P buffer and V stage gp % 2
         }
-        umma_commit(&bars->v_empty[vst]);
-        umma_commit(&bars->blk[gp & 1]);  // S(gp+2) (if any) and P.V(gp) complete
-        if (last) ++p_item;
-        ++gp;
       }
     }
     __syncwarp();
@@ -390,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
     bool ok = true;
     for (int c = 0; ok; ++c) {
       const int qb = c & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_full[qb], (c >> 1) & 1, p.err))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->slot_full[qb], (c >> 1) & 1, p.err))) break;
       const ItemSlot& sl = slots[qb];
       const bool done = sl.done != 0;
       const WorkItem it = sl.it;
@@ -406,8 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       for (int j = 0; j < ntiles; ++j, ++g) {
         const int sb = g & 1, vs = g % kVStages;
         const int kt = it.kb + j * kKeys;  // first key of the tile
-        // S(g) complete; with it P.V(g-2), so P buffer sb is free too
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->blk[sb], (g >> 1) & 1, p.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (g >> 1) & 1, p.err))) {
           ok = false;
           break;
         }
@@ -416,6 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         tmem_ld32(lane_base + kSCol + 128 * sb + 64 * h, sraw);
         tmem_ld32(lane_base + kSCol + 128 * sb + 64 * h + 32, sraw + 32);
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars->s_free[sb]);  // S buffer sb may take S(g+2)
         const int nvis = vis - (kt + 64 * h);  // keys c < nvis of this half are visible
         if (nvis < 64) {
 #pragma unroll
@@ -471,6 +464,11 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
             exps(m_ref);
           }
         }
+        // P buffer sb is free once the P.V of tile g-2, which read it, is done
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[sb], ((g >> 1) & 1) ^ 1, p.err))) {
+          ok = false;
+          break;
+        }
         tmem_st32(lane_base + kPCol + 64 * sb + 32 * h, pk);
         {
           const float2 a = up2(ps2[0]), b = up2(ps2[1]);
@@ -479,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         if (__any_sync(0xffffffffu, rescale)) {
           // O must hold every earlier tile's P.V before it is scaled; the TMEM
           // accesses are warp-wide, rows that keep their max scale by 1
-          // P.V(g-1) complete: the phase of blk[(g+1) % 2] that block g-1 commits
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars->blk[sb ^ 1], ((g + 1) >> 1) & 1, p.err))) {
+          // P.V(g-1) complete
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[sb ^ 1], ((g - 1) >> 1) & 1, p.err))) {
             ok = false;
             break;
           }
@@ -523,8 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       named_barrier(pair_bar, 64);
       const float ltot = l + reds[(h ^ 1) * 128 + r];
       named_barrier(pair_bar, 64);
-      // P.V of the item's last tile (g-1) complete: block g-1's phase of blk[(g+1) % 2]
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->blk[(g + 1) & 1], ((g + 1) >> 1) & 1, p.err))) break;
+      // P.V of the item's last tile (g-1) complete
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, p.err))) break;
       tc_fence_after();
       uint32_t o[64];
       tmem_ld32(lane_base + kOCol + 64 * h, o);
