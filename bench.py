@@ -395,9 +395,10 @@ def run_reference(args):
 # whose hash is recorded; reported as null once those sources change.  The
 # captures and their commands are summarised under profiles/.
 NCU_TRAFFIC = {
-    "sources": "12030eb24408e78f",
-    "decode": 613784064 + 5651712,    # dectc_kernel<4>, decode batch
-    "prefill": 81150720 + 8880896,    # mma_attn_kernel, prefill chunks
+    "sources": "da02570d76831f93",
+    "decode": 612998656 + 5149440,       # dectc_kernel<4>, decode batch
+    "prefill": 81453824 + 10598400,      # mma_attn_kernel, prefill chunks
+    "specverify": 1076825856 + 13650688,  # mma_attn_kernel, spec-verify
 }
 
 
