@@ -18,21 +18,24 @@
 // so one thread per key does the softmax arithmetic for its key (16 values)
 // and one thread per output column writes the result, coalesced.
 //
-// Roles (352 threads, one CTA per SM, persistent, items from an atomic
+// Roles (384 threads, one CTA per SM, persistent, items from an atomic
 // counter in the planner's largest-first order):
-//   warp 0    TMA producer: per 128-key tile one {64, 1, block_size, 1} box
-//             per physical block and 64-column half of K and V (128-byte
-//             swizzle; out-of-range boxes for blocks past the end read as
-//             zeros), and an item's Q tile ({64, G, 16/G} box of q) with its
-//             first tile; item descriptions travel in per-stage metadata;
+//   warp 0    K producer: per 128-key tile one {64, 1, block_size, 1} box
+//             per physical block and 64-column half of K (128-byte swizzle;
+//             out-of-range boxes for blocks past the end read as zeros), and
+//             an item's Q tile ({64, G, 16/G} box of q) with its first tile;
+//             item descriptions travel in per-stage metadata;
+//   warp 11   V producer, the same boxes of V.  One warp's tensor copies are
+//             processed at about one 2 KB box per 100 cycles, under the
+//             HBM rate an SM needs, so K and V are issued by two warps;
 //   warp 1    TMEM allocation and the single thread issuing the MMAs; the
 //             P.V of tile g is issued after the S of tile g+1;
-//   warps 2-5 softmax (thread = key = TMEM lane) and epilogue (thread =
-//             output column = TMEM lane of O^T);
+//   warps 2-5 softmax (thread = key = TMEM lane);
+//   warps 6-9 epilogue (thread = output column = TMEM lane of O^T);
 //   warp 10   item fetch: up to two items ahead, it reads each item's record,
 //             its sequence's length and query offset and the block ids of
 //             its first tile into a slot in shared memory, so that the
-//             producer starts an item's loads without a chain of dependent
+//             producers start an item's loads without a chain of dependent
 //             global reads.
 // Shared memory: 3 stages of K+V (192 KB), 2 Q tiles and 2 P tiles (4 KB
 // each).  TMEM: S^T double-buffered in columns [0,32), O^T in [32,48).
@@ -45,7 +48,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kStages = 3;
 constexpr int kKeys = kMmaTileKeys;            // 128 keys per tile
 constexpr int kN = kTcDecRows;                 // 16 rows (MMA N)
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
       mbar_init(&bars->ml_full[b], 128);
       mbar_init(&bars->ml_empty[b], 128);
       mbar_init(&bars->islot_full[b], 32);
-      mbar_init(&bars->islot_free[b], 1);
+      mbar_init(&bars->islot_free[b], 2);  // both producers read the slot
     }
     fence_mbar_init();
   }
@@ -200,12 +203,16 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
   const uint32_t tmem = *tmem_slot;
   const uint32_t smem_base = smem_u32(smem);
 
-  if (warp == 0) {
-    // ================================================================ producer
+  if (warp == 0 || warp == 11) {
+    // ================================================================ K / V producers
+    const bool vprod = warp == 11;
     if (lane == 0) {
-      prefetch_tensormap(&qmap);
-      prefetch_tensormap(&kmap);
-      prefetch_tensormap(&vmap);
+      if (vprod) {
+        prefetch_tensormap(&vmap);
+      } else {
+        prefetch_tensormap(&qmap);
+        prefetch_tensormap(&kmap);
+      }
     }
     const int nb_per_tile = kKeys / p.bs;
     const ItemSlot* islots = reinterpret_cast<const ItemSlot*>(smem + kISlotOff);
@@ -221,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->islot_free[qb]);
       if (done) {
+        if (vprod) break;
         const int st = g % kStages;
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->kv_empty[st], ((g / kStages) & 1) ^ 1, p.err))) break;
         if (lane == 0) {
@@ -255,6 +263,17 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
         }
         uint8_t* kd = smem + st * kStageBytes;
         uint8_t* vd = kd + kTileBytes;
+        if (vprod) {
+          if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
+          __syncwarp();
+          if (lane < nb_per_tile) {
+            const int row_off = lane * p.bs * 128;
+            tma_load_4d(vd + row_off, &vmap, &bars->v_full[st], 0, it.kvh, 0, phys);
+            tma_load_4d(vd + kHalf + row_off, &vmap, &bars->v_full[st], 64, it.kvh, 0, phys);
+          }
+          phys = next_phys;
+          continue;
+        }
         if (lane == 0) {
           Meta& m = meta[st];
           m.item = idx;
@@ -271,7 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
           m.n = n;
           m.qstart = qstart;
           mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes + (first ? 2 * kQHalf : 0));
-          mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
           if (first) {
             // this item's Q rows: tokens row0/G .. of the item, G heads each
             uint8_t* qd = smem + kQOff + (it_cnt & 1) * 2 * kQHalf;
@@ -285,8 +303,6 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
           const int row_off = lane * p.bs * 128;
           tma_load_4d(kd + row_off, &kmap, &bars->k_full[st], 0, it.kvh, 0, phys);
           tma_load_4d(kd + kHalf + row_off, &kmap, &bars->k_full[st], 64, it.kvh, 0, phys);
-          tma_load_4d(vd + row_off, &vmap, &bars->v_full[st], 0, it.kvh, 0, phys);
-          tma_load_4d(vd + kHalf + row_off, &vmap, &bars->v_full[st], 64, it.kvh, 0, phys);
         }
         phys = next_phys;
       }
