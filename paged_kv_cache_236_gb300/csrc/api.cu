@@ -401,9 +401,13 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
     if ((st = encode_pool_map(&vmap_sw, v_cache, dtype, num_blocks, bs, Hkv, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) !=
         PKV_OK)
       return st;
+    // the output in the q tile's layout: full 128-row tiles leave through TMA stores
+    CUtensorMap omap;
+    if ((st = encode_q_map(&omap, out, T, Hq, D, 64, G, kMmaRows / G)) != PKV_OK) return st;
     ap.counter = &header->mma_counter;
     ap.items = mma_items;
-    if ((e = launch_mma(ap, qmap, kmap_sw, vmap_sw, dev->sms, s)) != cudaSuccess) return cuda_fail(e, "mma launch");
+    if ((e = launch_mma(ap, qmap, kmap_sw, vmap_sw, omap, dev->sms, s)) != cudaSuccess)
+      return cuda_fail(e, "mma launch");
   }
   ap.counter = &header->dec_counter;
   ap.items = dec_items;

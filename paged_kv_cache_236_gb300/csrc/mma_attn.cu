@@ -23,23 +23,35 @@
 // softmax warps have read the S buffer it writes, the other the P.V chains,
 // as soon as their P is written.  Either one's waits overlap the other's MMAs.
 //
-// Roles (384 threads, one CTA per SM, persistent; items are taken from an
+// Roles (512 threads, one CTA per SM, persistent; items are taken from an
 // atomic counter in the planner's largest-first order, so SMs that run
 // slower take fewer):
-//   warp 0    the thread issuing P.V (O += P V, P from TMEM, V from shared memory);
-//   warp 1    TMEM allocation and the thread issuing Q K^T (S = Q K^T);
-//   warps 2-9 softmax / correction / epilogue: two threads per row (TMEM
-//             lane), warps 2-5 on key columns 0-63 of a tile, warps 6-9 on
-//             64-127; a pair exchanges row maxima (and at the end row sums)
-//             through shared memory;
-//   warp 10   item fetch, Q and K: publishes each item in a slot of shared
-//             memory (with the block ids of its first key tile), loads its Q
-//             tile (3-D box {64, G heads, 128/G tokens} of q [T, Hq, D], two
-//             64-column halves), then its K tiles: per tile one
-//             {64, 1, block_size, 1} box of the pool [NB, bs, Hkv, D] per
-//             physical block and 64-column half (128-byte swizzle, the layout
-//             the tensor core reads), block ids loaded a tile ahead;
-//   warp 11   V producer, the same boxes from the V pool.
+//   warp 0     the thread issuing P.V (O += P V, P from TMEM, V from shared memory);
+//   warp 1     TMEM allocation and the thread issuing Q K^T (S = Q K^T);
+//   warps 2-3  K producers, one per 64-column half: per tile one
+//              {64, 1, block_size, 1} box of the pool [NB, bs, Hkv, D] per
+//              physical block (128-byte swizzle, the layout the tensor core
+//              reads), block ids loaded a tile ahead;
+//   warps 4-11 softmax / correction / epilogue: two threads per row (TMEM
+//              lane), warps 4-7 on key columns 0-63 of a tile, warps 8-11 on
+//              64-127; a pair exchanges row maxima (and at the end row sums)
+//              through shared memory;
+//   warps 12-13 V producers, the same boxes from the V pool;
+//   warp 14    item fetch, Q and output stores: publishes each item in a
+//              slot of shared memory (with the block ids of its first key
+//              tile), then loads its Q tile (3-D box {64, G heads, 128/G
+//              tokens} of q [T, Hq, D], two 64-column halves).  Before a Q
+//              tile buffer takes a new item it stores, with two TMA stores of
+//              the same boxes of out, the output tile that the epilogue of
+//              the buffer's previous item left there: a finished 128-row tile
+//              (whole tokens x G heads) is 32 KB that per-row stores would
+//              write as 32-byte pieces 256 bytes to 8 KB apart.
+// One warp's tensor copies of these 2 KB boxes are processed at about one
+// box per 100 cycles whatever the number of issuing lanes, and copies
+// completing on one barrier add up slower than on separate ones, so each
+// 64-column half of K and of V has its own producer warp and barrier: four
+// warps together supply the 64 KB of K and V a tile needs at the tensor
+// core's pace.
 // Shared memory: 2 Q tiles (64 KB), a 3-stage ring of K tiles (96 KB) and a
 // 2-stage ring of V tiles (64 KB); K of a tile is released when its Q K^T is
 // done, V when its P.V is done (K is needed two tiles ahead of V).
@@ -58,7 +70,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kKeys = kMmaTileKeys;                 // 128 keys per tile
 constexpr int kKStages = 3, kVStages = 2;
 constexpr int kHalfKV = kKeys * 128;                // one 64-column half of a K or V tile (16 KB)
@@ -69,7 +81,7 @@ constexpr int kQOff = 0;
 constexpr int kKOff = kQOff + 2 * kQBytes;
 constexpr int kVOff = kKOff + kKStages * kTileBytes;
 constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-constexpr int kNumBars = 8 + 2 * kKStages + kVStages + 8 + 1;
+constexpr int kNumBars = 8 + 3 * kKStages + 2 * kVStages + 8 + 1 + 2;
 constexpr int kSlotOff = (kBarOff + kNumBars * 8 + 16 + 15) & ~15;  // 2 item slots
 constexpr int kRedOff = kSlotOff + 2 * 176;         // [2 tiles][2 halves][128 rows] row maxima / sums
 // No alignment slack: the buffers need a 1024-byte aligned base, which the
@@ -81,6 +93,12 @@ constexpr uint32_t kSCol = 0;    // S buffer b at kSCol + 128 b
 constexpr uint32_t kPCol = 256;  // P buffer b at kPCol + 64 b
 constexpr uint32_t kOCol = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Register split between warpgroups (setmaxnreg): warpgroups 0 and 3 (MMA
+// issuers, producers, item fetch) give up registers that warpgroups 1 and 2
+// (softmax) take.  The sum must stay within what the block is launched with
+// (kThreads x the kernel's register count); the launcher checks the count.
+constexpr int kRegsLight = 64, kRegsSoftmax = 184;
+static_assert(2 * 128 * (kRegsLight + kRegsSoftmax) <= kThreads * 128, "register split above 128 per thread");
 
 constexpr uint32_t kIdescS = idesc_bf16(128, kKeys, false, false);
 constexpr uint32_t kIdescO = idesc_bf16(128, 128, false, true);
@@ -91,13 +109,16 @@ __device__ __forceinline__ uint64_t desc_v(uint32_t saddr) { return smem_desc(sa
 
 struct Bars {
   uint64_t q_full[2], q_empty[2], slot_full[2], slot_free[2];
-  uint64_t k_full[kKStages], k_empty[kKStages];
-  uint64_t v_full[kVStages];
+  uint64_t k_full[kKStages][2], k_empty[kKStages];  // k_full[stage][64-column half]
+  uint64_t v_full[kVStages][2];
   // s_full[b], phase n: S of tile 2n+b complete; s_free[b]: the softmax
   // warps have read it.  pv_done[b], phase n: the P.V of tile 2n+b complete,
   // and with it every earlier P.V.
   uint64_t s_full[2], s_free[2], pv_done[2], p_full[2];
   uint64_t o_empty;
+  // o_staged[b], phase n: the epilogue of item 2n+b has left its output tile
+  // in Q buffer b (or written it directly)
+  uint64_t o_staged[2];
 };
 
 // An item's description, published by the item-fetching warp before its Q
@@ -107,8 +128,8 @@ struct alignas(16) ItemSlot {
   int L, qstart, n, done;
   int phys0[32];
 };
-// readers of a slot: the 256 softmax threads, the two MMA-issuing threads, the V producer
-constexpr int kSlotReaders = 256 + 1 + 1 + 1;
+// readers of a slot: the 256 softmax threads, the two MMA-issuing threads, the four K / V producers
+constexpr int kSlotReaders = 256 + 1 + 1 + 4;
 
 static_assert(sizeof(ItemSlot) == 176, "item slot");
 static_assert(sizeof(Bars) == kNumBars * 8, "barrier block");
@@ -134,7 +155,8 @@ __device__ __forceinline__ void store_row128(__nv_bfloat16* dst, const uint32_t*
 __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams p,
                                                                const __grid_constant__ CUtensorMap qmap,
                                                                const __grid_constant__ CUtensorMap kmap,
-                                                               const __grid_constant__ CUtensorMap vmap) {
+                                                               const __grid_constant__ CUtensorMap vmap,
+                                                               const __grid_constant__ CUtensorMap omap) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // uniform: every thread returns before any barrier
     if (threadIdx.x == 0) raise_error(p.err, PKV_DEVERR_INTERNAL);
@@ -157,11 +179,17 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       mbar_init(&bars->p_full[b], 256);
     }
     for (int s = 0; s < kKStages; ++s) {
-      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_full[s][0], 1);
+      mbar_init(&bars->k_full[s][1], 1);
       mbar_init(&bars->k_empty[s], 1);
     }
-    for (int s = 0; s < kVStages; ++s) mbar_init(&bars->v_full[s], 1);
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&bars->v_full[s][0], 1);
+      mbar_init(&bars->v_full[s][1], 1);
+    }
     mbar_init(&bars->o_empty, 256);
+    mbar_init(&bars->o_staged[0], 256);
+    mbar_init(&bars->o_staged[1], 256);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -177,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
   const uint32_t smem_base = smem_u32(smem);
 
   // One counter g numbers the key tiles this CTA processes (across items): K
-  // stage g % 2 (parity (g / 2) & 1), V stage g % 3 (parity (g / 3) & 1), S
+  // stage g % 3 (parity (g / 3) & 1), V stage g % 2 (parity (g / 2) & 1), S
   // and P buffer g % 2.  Item c of this CTA uses Q tile and slot c & 1
   // (parity (c >> 1) & 1); O's phases count items.
   const int nb = kKeys / p.bs;  // physical blocks per tile
@@ -195,185 +223,221 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
     return phys;
   };
 
-  if (warp == 10) {
-    // ================================================================ item fetch, Q and K
-    if (lane == 0) {
-      prefetch_tensormap(&qmap);
-      prefetch_tensormap(&kmap);
-    }
-    int next = 0;
-    if (lane == 0) next = atomicAdd(p.counter, 1);
-    int g = 0;
-    bool ok = true;
-    for (int c = 0; ok; ++c) {
-      const int qb = c & 1;
-      // slot and Q tile qb: free once item c-2's last Q K^T has completed and
-      // every reader has taken its description
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_empty[qb], ((c >> 1) & 1) ^ 1, p.err) &&
-                                       mbar_wait(&bars->slot_free[qb], ((c >> 1) & 1) ^ 1, p.err)))
-        break;
-      const int idx = __shfl_sync(0xffffffffu, next, 0);
-      ItemSlot& sl = slots[qb];
-      if (idx >= n_items) {
-        if (lane == 0) sl.done = 1;
-        mbar_arrive(&bars->slot_full[qb]);  // every lane: count 32
-        if (lane == 0) mbar_arrive(&bars->q_full[qb]);
-        break;
-      }
-      const WorkItem it = p.items[idx];
-      if (lane == 0) next = atomicAdd(p.counter, 1);  // consumed at the next item
-      const int L = p.context_lens[it.seq];
-      const int qstart = p.query_start_loc[it.seq];
-      const int nblk = (L + p.bs - 1) / p.bs;
-      const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
-      int phys = block_of(bt, nblk, it.kb);
-      sl.phys0[lane] = phys;
+  // The branches below are per warpgroup first (the register split is a
+  // warpgroup-wide instruction), then per warp.
+  if (warp < 4 || warp >= 12) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLight));
+    if (warp == 14) {
+      // ================================================================ item fetch, Q, output stores
       if (lane == 0) {
-        sl.it = it;
-        sl.L = L;
-        sl.qstart = qstart;
-        sl.n = p.query_start_loc[it.seq + 1] - qstart;
-        sl.done = 0;
+        prefetch_tensormap(&qmap);
+        prefetch_tensormap(&omap);
       }
-      mbar_arrive(&bars->slot_full[qb]);  // every lane, after its own writes
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->q_full[qb], kQBytes);
-        const int tok0 = qstart + it.row0 / p.G;
-        tma_load_3d(smem + kQOff + qb * kQBytes, &qmap, &bars->q_full[qb], 0, it.kvh * p.G, tok0);
-        tma_load_3d(smem + kQOff + qb * kQBytes + kHalf, &qmap, &bars->q_full[qb], 64, it.kvh * p.G, tok0);
-      }
-      for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
-        const int st = g % kKStages;
-        const int next_phys = (kbase + kKeys < it.ke) ? block_of(bt, nblk, kbase + kKeys) : 0;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_empty[st], ((g / kKStages) & 1) ^ 1, p.err))) {
+      // where the output tile staged in Q buffer b goes: token and head
+      // coordinates of its TMA stores, token -1 when the epilogue wrote it itself
+      int otok0 = -1, otok1 = -1, ohead0 = 0, ohead1 = 0;
+      auto store_staged = [&](int ci) -> bool {  // item ci's output, once its epilogue is done
+        const int b = ci & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_staged[b], (ci >> 1) & 1, p.err))) return false;
+        const int tok = b ? otok1 : otok0, head = b ? ohead1 : ohead0;
+        if (lane == 0 && tok >= 0) {
+          tma_store_3d(&omap, smem + kQOff + b * kQBytes, 0, head, tok);
+          tma_store_3d(&omap, smem + kQOff + b * kQBytes + kHalf, 64, head, tok);
+          bulk_commit_group();
+          bulk_wait_read_all();  // the buffer may take the next Q tile
+        }
+        __syncwarp();
+        return true;
+      };
+      int c = 0;
+      bool ok = true;
+      for (;; ++c) {
+        const int qb = c & 1;
+        // Item c is taken from the queue once item c-2's last Q K^T is
+        // complete (Q tile qb free) and every reader has taken item c-2's
+        // description (slot qb free): while item c-2 ends, item c-1 waits
+        // with its Q loaded.  Taking items no earlier keeps the queue's
+        // largest-first order close to the order in which the SMs fall idle,
+        // which is what keeps the tail short.
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_empty[qb], ((c >> 1) & 1) ^ 1, p.err) &&
+                                         mbar_wait(&bars->slot_free[qb], ((c >> 1) & 1) ^ 1, p.err))) {
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
-        __syncwarp();
-        if (lane < nb) {
-          uint8_t* d = smem + kKOff + st * kTileBytes + lane * p.bs * 128;
-          tma_load_4d(d, &kmap, &bars->k_full[st], 0, it.kvh, 0, phys);
-          tma_load_4d(d + kHalfKV, &kmap, &bars->k_full[st], 64, it.kvh, 0, phys);
+        int idx = 0;
+        if (lane == 0) idx = atomicAdd(p.counter, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        const bool done = idx >= n_items;
+        ItemSlot& sl = slots[qb];
+        WorkItem it{};
+        int qstart = 0;
+        if (done) {
+          if (lane == 0) sl.done = 1;
+        } else {
+          it = p.items[idx];
+          const int L = p.context_lens[it.seq];
+          qstart = p.query_start_loc[it.seq];
+          const int nblk = (L + p.bs - 1) / p.bs;
+          const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
+          sl.phys0[lane] = block_of(bt, nblk, it.kb);
+          if (lane == 0) {
+            sl.it = it;
+            sl.L = L;
+            sl.qstart = qstart;
+            sl.n = p.query_start_loc[it.seq + 1] - qstart;
+            sl.done = 0;
+          }
         }
-        phys = next_phys;
+        mbar_arrive(&bars->slot_full[qb]);  // every lane, after its own writes (count 32)
+        // Q tile qb: item c-2's output, staged there by its epilogue, read out
+        if (c >= 2 && !store_staged(c - 2)) {
+          ok = false;
+          break;
+        }
+        if (done) {
+          if (lane == 0) mbar_arrive(&bars->q_full[qb]);
+          break;
+        }
+        // a full tile of whole tokens, not a split: its epilogue stages the output
+        const int tok = (it.nrows == kMmaRows && it.part < 0) ? qstart + it.row0 / p.G : -1;
+        if (qb) {
+          otok1 = tok;
+          ohead1 = it.kvh * p.G;
+        } else {
+          otok0 = tok;
+          ohead0 = it.kvh * p.G;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->q_full[qb], kQBytes);
+          const int tok0 = qstart + it.row0 / p.G;
+          tma_load_3d(smem + kQOff + qb * kQBytes, &qmap, &bars->q_full[qb], 0, it.kvh * p.G, tok0);
+          tma_load_3d(smem + kQOff + qb * kQBytes + kHalf, &qmap, &bars->q_full[qb], 64, it.kvh * p.G, tok0);
+        }
       }
-    }
-  } else if (warp == 11) {
-    // ================================================================ V
-    if (lane == 0) prefetch_tensormap(&vmap);
-    int g = 0;
-    bool ok = true;
-    for (int c = 0; ok; ++c) {
-      const int qb = c & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->slot_full[qb], (c >> 1) & 1, p.err))) break;
-      const bool done = slots[qb].done != 0;
-      const WorkItem it = slots[qb].it;
-      const int L = slots[qb].L;
-      int phys = slots[qb].phys0[lane];
+      if (ok && c >= 1) store_staged(c - 1);  // the last item's output
+      if (lane == 0) bulk_wait_all();
+    } else if (warp == 2 || warp == 3 || warp == 12 || warp == 13) {
+      // ================================================================ K / V producers
+      const bool is_v = warp >= 12;
+      const int hh = warp & 1;  // 64-column half
+      const CUtensorMap* map = is_v ? &vmap : &kmap;
+      if (lane == 0) prefetch_tensormap(map);
+      const int nst = is_v ? kVStages : kKStages;
+      uint8_t* const ring = smem + (is_v ? kVOff : kKOff) + hh * kHalfKV;
+      int g = 0;
+      bool ok = true;
+      for (int c = 0; ok; ++c) {
+        const int qb = c & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->slot_full[qb], (c >> 1) & 1, p.err))) break;
+        const bool done = slots[qb].done != 0;
+        const WorkItem it = slots[qb].it;
+        const int L = slots[qb].L;
+        int phys = slots[qb].phys0[lane];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->slot_free[qb]);
+        if (done) break;
+        const int nblk = (L + p.bs - 1) / p.bs;
+        const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
+        for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
+          const int st = g % nst, ph = (g / nst) & 1;
+          const int next_phys = (kbase + kKeys < it.ke) ? block_of(bt, nblk, kbase + kKeys) : 0;
+          // K stage g % 3 is free once Q K^T(g-3) is complete; V stage g % 2
+          // once P.V(g-2) is complete (phase of pv_done[g % 2])
+          if (!__all_sync(0xffffffffu, mbar_wait(is_v ? &bars->pv_done[st] : &bars->k_empty[st], ph ^ 1, p.err))) {
+            ok = false;
+            break;
+          }
+          uint64_t* full = is_v ? &bars->v_full[st][hh] : &bars->k_full[st][hh];
+          if (lane == 0) mbar_arrive_expect_tx(full, kHalfKV);
+          __syncwarp();
+          if (lane < nb) tma_load_4d(ring + st * kTileBytes + lane * p.bs * 128, map, full, 64 * hh, it.kvh, 0, phys);
+          phys = next_phys;
+        }
+      }
+    } else if (warp == 1) {
+      // ================================================================ Q K^T issuer
+      if (lane == 0) {
+        const uint64_t dq = desc_k(smem_base + kQOff);
+        const uint64_t dk0 = desc_k(smem_base + kKOff);
+        int gs = 0, s_item = -1, s_j = 0, s_nt = 0;
+        for (;;) {
+          if (s_j == s_nt) {  // next item: its Q tile loaded (its slot written before)
+            ++s_item;
+            const int qb = s_item & 1;
+            if (!mbar_wait(&bars->q_full[qb], (s_item >> 1) & 1, p.err)) break;
+            const bool done = slots[qb].done != 0;
+            const int nt = (slots[qb].it.ke - slots[qb].it.kb + kKeys - 1) / kKeys;
+            mbar_arrive(&bars->slot_free[qb]);
+            if (done) break;
+            s_nt = nt;
+            s_j = 0;
+          }
+          const int sb = gs & 1, st = gs % kKStages;
+          // S buffer sb: the softmax warps have read S(gs-2) from it; both halves of K(gs) loaded
+          const uint32_t kph = (gs / kKStages) & 1;
+          if (!mbar_test_wait3(&bars->s_free[sb], ((gs >> 1) & 1) ^ 1, &bars->k_full[st][0], kph, &bars->k_full[st][1],
+                               kph) &&
+              (!mbar_wait(&bars->s_free[sb], ((gs >> 1) & 1) ^ 1, p.err) ||
+               !mbar_wait(&bars->k_full[st][0], kph, p.err) || !mbar_wait(&bars->k_full[st][1], kph, p.err)))
+            break;
+          tc_fence_after();
+          const uint64_t dqb = desc_add(dq, (s_item & 1) * kQBytes);
+          const uint64_t dk = desc_add(dk0, st * kTileBytes);
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16(tmem + kSCol + 128 * sb, desc_add(dqb, (kk >> 2) * kHalf + (kk & 3) * 32),
+                      desc_add(dk, (kk >> 2) * kHalfKV + (kk & 3) * 32), kIdescS, kk > 0 ? 1u : 0u);
+          umma_commit(&bars->s_full[sb]);
+          umma_commit(&bars->k_empty[st]);
+          if (s_j == s_nt - 1) umma_commit(&bars->q_empty[s_item & 1]);  // Q no longer read by this item
+          ++s_j;
+          ++gs;
+        }
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->slot_free[qb]);
-      if (done) break;
-      const int nblk = (L + p.bs - 1) / p.bs;
-      const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
-      for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
-        const int st = g % kVStages;
-        const int next_phys = (kbase + kKeys < it.ke) ? block_of(bt, nblk, kbase + kKeys) : 0;
-        // V stage g % 2 is free once P.V(g-2) is complete (phase of pv_done[g % 2])
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[st], ((g / kVStages) & 1) ^ 1, p.err))) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-        __syncwarp();
-        if (lane < nb) {
-          uint8_t* d = smem + kVOff + st * kTileBytes + lane * p.bs * 128;
-          tma_load_4d(d, &vmap, &bars->v_full[st], 0, it.kvh, 0, phys);
-          tma_load_4d(d + kHalfKV, &vmap, &bars->v_full[st], 64, it.kvh, 0, phys);
-        }
-        phys = next_phys;
-      }
-    }
-  } else if (warp == 1) {
-    // ================================================================ Q K^T issuer
-    if (lane == 0) {
-      const uint64_t dq = desc_k(smem_base + kQOff);
-      const uint64_t dk0 = desc_k(smem_base + kKOff);
-      int gs = 0, s_item = -1, s_j = 0, s_nt = 0;
-      for (;;) {
-        if (s_j == s_nt) {  // next item: its Q tile loaded (its slot written before)
-          ++s_item;
-          const int qb = s_item & 1;
-          if (!mbar_wait(&bars->q_full[qb], (s_item >> 1) & 1, p.err)) break;
+    } else if (warp == 0) {
+      // ================================================================ P.V issuer
+      if (lane == 0) {
+        const uint64_t dv0 = desc_v(smem_base + kVOff);
+        int gp = 0;
+        bool ok = true;
+        for (int c = 0; ok; ++c) {
+          const int qb = c & 1;
+          if (!mbar_wait(&bars->slot_full[qb], (c >> 1) & 1, p.err)) break;
           const bool done = slots[qb].done != 0;
           const int nt = (slots[qb].it.ke - slots[qb].it.kb + kKeys - 1) / kKeys;
           mbar_arrive(&bars->slot_free[qb]);
           if (done) break;
-          s_nt = nt;
-          s_j = 0;
-        }
-        const int sb = gs & 1, st = gs % kKStages;
-        // S buffer sb: the softmax warps have read S(gs-2) from it; K(gs) loaded
-        if (!mbar_test_wait3(&bars->s_free[sb], ((gs >> 1) & 1) ^ 1, &bars->k_full[st], (gs / kKStages) & 1,
-                             &bars->k_full[st], (gs / kKStages) & 1) &&
-            (!mbar_wait(&bars->s_free[sb], ((gs >> 1) & 1) ^ 1, p.err) ||
-             !mbar_wait(&bars->k_full[st], (gs / kKStages) & 1, p.err)))
-          break;
-        tc_fence_after();
-        const uint64_t dqb = desc_add(dq, (s_item & 1) * kQBytes);
-        const uint64_t dk = desc_add(dk0, st * kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16(tmem + kSCol + 128 * sb, desc_add(dqb, (kk >> 2) * kHalf + (kk & 3) * 32),
-                    desc_add(dk, (kk >> 2) * kHalfKV + (kk & 3) * 32), kIdescS, kk > 0 ? 1u : 0u);
-        umma_commit(&bars->s_full[sb]);
-        umma_commit(&bars->k_empty[st]);
-        if (s_j == s_nt - 1) umma_commit(&bars->q_empty[s_item & 1]);  // Q no longer read by this item
-        ++s_j;
-        ++gs;
-      }
-    }
-    __syncwarp();
-  } else if (warp == 0) {
-    // ================================================================ P.V issuer
-    if (lane == 0) {
-      const uint64_t dv0 = desc_v(smem_base + kVOff);
-      int gp = 0;
-      bool ok = true;
-      for (int c = 0; ok; ++c) {
-        const int qb = c & 1;
-        if (!mbar_wait(&bars->slot_full[qb], (c >> 1) & 1, p.err)) break;
-        const bool done = slots[qb].done != 0;
-        const int nt = (slots[qb].it.ke - slots[qb].it.kb + kKeys - 1) / kKeys;
-        mbar_arrive(&bars->slot_free[qb]);
-        if (done) break;
-        // O is about to be overwritten: item c-1's epilogue must have read it
-        if (!mbar_wait(&bars->o_empty, (c & 1) ^ 1, p.err)) break;
-        for (int j = 0; j < nt; ++j, ++gp) {
-          const int pb = gp & 1, vst = gp % kVStages;
-          // P(gp) written, V(gp) loaded
-          if (!mbar_test_wait3(&bars->p_full[pb], (gp >> 1) & 1, &bars->v_full[vst], (gp / kVStages) & 1,
-                               &bars->v_full[vst], (gp / kVStages) & 1) &&
-              (!mbar_wait(&bars->p_full[pb], (gp >> 1) & 1, p.err) ||
-               !mbar_wait(&bars->v_full[vst], (gp / kVStages) & 1, p.err))) {
-            ok = false;
-            break;
+          // O is about to be overwritten: item c-1's epilogue must have read it
+          if (!mbar_wait(&bars->o_empty, (c & 1) ^ 1, p.err)) break;
+          for (int j = 0; j < nt; ++j, ++gp) {
+            const int pb = gp & 1, vst = gp % kVStages;
+            // P(gp) written, both halves of V(gp) loaded
+            const uint32_t vph = (gp / kVStages) & 1;
+            if (!mbar_test_wait3(&bars->p_full[pb], (gp >> 1) & 1, &bars->v_full[vst][0], vph, &bars->v_full[vst][1],
+                                 vph) &&
+                (!mbar_wait(&bars->p_full[pb], (gp >> 1) & 1, p.err) || !mbar_wait(&bars->v_full[vst][0], vph, p.err) ||
+                 !mbar_wait(&bars->v_full[vst][1], vph, p.err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t dv = desc_add(dv0, vst * kTileBytes);
+  #pragma unroll
+            for (int kk = 0; kk < kKeys / 16; ++kk)
+              umma_bf16_ts(tmem + kOCol, tmem + kPCol + 64 * pb + kk * 8, desc_add(dv, kk * 2048), kIdescO,
+                           (j == 0 && kk == 0) ? 0u : 1u);
+            umma_commit(&bars->pv_done[pb]);  // P.V(gp) complete: frees P buffer and V stage gp % 2
           }
-          tc_fence_after();
-          const uint64_t dv = desc_add(dv0, vst * kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk)
-            umma_bf16_ts(tmem + kOCol, tmem + kPCol + 64 * pb + kk * 8, desc_add(dv, kk * 2048), kIdescO,
-                         (j == 0 && kk == 0) ? 0u : 1u);
-          umma_commit(&bars->pv_done[pb]);  // P.V(gp) complete: frees P buffer and V stage gp % 2
         }
       }
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ================================================================ softmax / epilogue
     const int q4 = warp & 3;
-    const int h = (warp - 2) >> 2;  // key half of a tile (columns 64h .. 64h+63); output half 64h .. 64h+63
+    const int h = (warp - 4) >> 2;  // key half of a tile (columns 64h .. 64h+63); output half 64h .. 64h+63
     const int r = q4 * 32 + lane;   // row of the tile == TMEM lane
     const int pair_bar = 1 + q4;    // warps (w, w+4) of one row quarter
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
@@ -497,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         if (kt + kKeys > L) {
           // keys at or past the sequence's end hold arbitrary bits: zero their V
           // rows (thread: key r of the tile, d-half h) so that 0 * V stays 0
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[vs], (g / kVStages) & 1, p.err))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[vs][h], (g / kVStages) & 1, p.err))) {
             ok = false;
             break;
           }
@@ -530,16 +594,28 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->o_empty);
+      // a full tile of whole tokens leaves through TMA stores from Q buffer qb
+      // (its Q K^T are complete), in the Q tile's layout: row r, 16-byte
+      // chunk j at chunk j ^ (r & 7) of the row (128-byte swizzle)
+      const bool staged = it.nrows == kMmaRows && it.part < 0;
       if (valid) {
         if (it.part < 0) {
           const float inv = 1.f / ltot;
-          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                ((int64_t)(qstart + tok) * p.Hq + (int64_t)it.kvh * p.G + gh) * 128 + 64 * h;
           uint32_t w[32];
 #pragma unroll
           for (int u = 0; u < 32; ++u)
             w[u] = pack_bf16(__uint_as_float(o[2 * u]) * inv, __uint_as_float(o[2 * u + 1]) * inv);
-          store_row128(orow, w, p.out_al32);
+          if (staged) {
+            uint8_t* srow = smem + kQOff + qb * kQBytes + h * kHalf + r * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(srow + ((j ^ (r & 7)) << 4)) =
+                  make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          } else {
+            __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                  ((int64_t)(qstart + tok) * p.Hq + (int64_t)it.kvh * p.G + gh) * 128 + 64 * h;
+            store_row128(orow, w, p.out_al32);
+          }
         } else {
           // this split's partial row: 256 bytes of fp32 (the workspace is 256-byte aligned)
           float* dst = p.part_acc + (int64_t)(it.part + r) * 128 + 64 * h;
@@ -548,6 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           if (h == 0) p.part_ml[it.part + r] = make_float2(m_ref, ltot);
         }
       }
+      if (staged) fence_proxy_async_smem();  // the staged rows, for the TMA stores
+      mbar_arrive(&bars->o_staged[qb]);
       if (it.part >= 0) {
         // The split that completes its merge group combines the group's
         // partial rows: m = max m_p, l = sum l_p 2^(m_p - m), O = sum acc_p 2^(m_p - m) / l.
@@ -614,18 +692,23 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
 }  // namespace
 
 cudaError_t launch_mma(const AttnParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                       int grid, cudaStream_t s) {
+                       const CUtensorMap& omap, int grid, cudaStream_t s) {
   static unsigned long long done_mask = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+    // the register split needs the block launched with 128 registers per thread
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, mma_attn_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(mma_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, 1ull << dev, __ATOMIC_RELEASE);
   }
-  e = launch_pdl(mma_attn_kernel, dim3(grid), dim3(kThreads), kSmem, s, p, qmap, kmap, vmap);
+  e = launch_pdl(mma_attn_kernel, dim3(grid), dim3(kThreads), kSmem, s, p, qmap, kmap, vmap, omap);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -136,7 +136,7 @@ cudaError_t launch_planner(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_mma(const AttnParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                       const CUtensorMap& vmap, int grid, cudaStream_t s);
+                       const CUtensorMap& vmap, const CUtensorMap& omap, int grid, cudaStream_t s);
 // rows: the largest item row count (4, 8 or 16 rows of softmax per key)
 cudaError_t launch_dectc(const AttnParams& p, int rows, const CUtensorMap& qmap, const CUtensorMap& kmap,
                          const CUtensorMap& vmap, int grid, cudaStream_t s);
