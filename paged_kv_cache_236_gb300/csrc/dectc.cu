@@ -32,7 +32,7 @@
 //             P.V of tile g is issued after the S of tile g+1;
 //   warps 2-5 softmax (thread = key = TMEM lane);
 //   warps 6-9 epilogue (thread = output column = TMEM lane of O^T);
-//   warp 10   item fetch: up to two items ahead, it reads each item's record,
+//   warp 10   item fetch: one item ahead, it reads each item's record,
 //             its sequence's length and query offset and the block ids of
 //             its first tile into a slot in shared memory, so that the
 //             producers start an item's loads without a chain of dependent
@@ -312,13 +312,18 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
     // ================================================================ item fetch
     const int nb_per_tile = kKeys / p.bs;
     ItemSlot* islots = reinterpret_cast<ItemSlot*>(smem + kISlotOff);
-    int next = 0;
-    if (lane == 0) next = atomicAdd(p.counter, 1);
     for (int c = 0;; ++c) {
       const int qb = c & 1;
-      // slot qb is free once the producer has read item c-2 from it
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->islot_free[qb], ((c >> 1) & 1) ^ 1, p.err))) break;
-      const int idx = __shfl_sync(0xffffffffu, next, 0);
+      // Item c is taken from the queue once the producers have taken item
+      // c-1 (and so item c-2, freeing slot qb): one item waits while one is
+      // loaded.  Taking items no earlier keeps the queue's largest-first
+      // order close to the order in which the SMs fall idle.
+      if (c >= 1 &&
+          !__all_sync(0xffffffffu, mbar_wait(&bars->islot_free[(c - 1) & 1], ((c - 1) >> 1) & 1, p.err)))
+        break;
+      int idx = 0;
+      if (lane == 0) idx = atomicAdd(p.counter, 1);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
       ItemSlot& isl = islots[qb];
       if (idx >= n_items) {
         if (lane == 0) isl.done = 1;
@@ -326,7 +331,6 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
         break;
       }
       const WorkItem it = p.items[idx];
-      if (lane == 0) next = atomicAdd(p.counter, 1);  // consumed at the next item
       const int L = p.context_lens[it.seq];
       const int qstart = p.query_start_loc[it.seq];
       const int n = p.query_start_loc[it.seq + 1] - qstart;
