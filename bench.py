@@ -187,7 +187,9 @@ def run_gpu(args, rank, world, local_rank):
         return dict(kc=to_dev(w.k_cache), vc=to_dev(w.v_cache), q=to_dev(st.q), k=to_dev(st.k_new),
                     v=to_dev(st.v_new), slots=torch.from_numpy(st.slot_mapping).to(dev),
                     bt=torch.from_numpy(st.block_tables).to(dev), ctx=torch.from_numpy(st.context_lens).to(dev),
-                    qsl=torch.from_numpy(st.query_start_loc).to(dev), mql=int(st.q_lens.max(initial=0)))
+                    qsl=torch.from_numpy(st.query_start_loc).to(dev), mql=int(st.q_lens.max(initial=0)),
+                    # a serving system knows when it shares cached prefix blocks between requests
+                    sp=bool(w.meta.get("shared_prefix_tokens") or w.meta.get("share_groups")))
 
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
@@ -199,7 +201,7 @@ def run_gpu(args, rank, world, local_rank):
         def one():
             pkv.paged_kv_write(t["k"], t["v"], t["slots"], t["kc"], t["vc"])
             pkv.paged_attention_forward(t["q"], t["kc"], t["vc"], t["bt"], t["ctx"], t["qsl"], w.scale, w.causal,
-                                        out=out, workspace=ws, max_query_len=t["mql"])
+                                        out=out, workspace=ws, max_query_len=t["mql"], shared_prefix=t["sp"])
 
         for _ in range(warmup):
             flush.fill_(1)
@@ -289,7 +291,7 @@ def run_gpu(args, rank, world, local_rank):
         d = {k2: x.to(dev, non_blocking=True) for k2, x in host_in.items()}
         pkv.paged_kv_write(d["k"], d["v"], d["slots"], t["kc"], t["vc"])
         o = pkv.paged_attention_forward(d["q"], t["kc"], t["vc"], d["bt"], d["ctx"], d["qsl"], w.scale, w.causal,
-                                        workspace=ws, max_query_len=t["mql"])
+                                        workspace=ws, max_query_len=t["mql"], shared_prefix=t["sp"])
         host_out.copy_(o, non_blocking=True)
         b.record()
         b.synchronize()

@@ -73,6 +73,22 @@ typedef enum {
   PKV_DTYPE_BF16 = 1
 } pkv_dtype;
 
+/*
+ * Host hints for paged_attention_forward (bit flags).
+ *
+ * PKV_HINT_SHARED_PREFIX: consecutive sequences of the batch may start with
+ * the same physical blocks (prefix caching: several requests built on one
+ * cached prompt; "PagedAttention" prefix sharing).  The call then looks for
+ * runs of at least 4 decode-shaped sequences whose block tables agree on
+ * their first whole 128-key tiles (up to 31 tiles, keys every query of the
+ * run sees) and reads those keys once for the whole run, as tensor-core work
+ * over all the run's query rows; each member's remaining keys are read as
+ * usual and the two parts merged (the result is the same attention, up to
+ * rounding).  Only on the bf16 / head_dim 128 tensor-core decode path;
+ * ignored elsewhere.  Costs a short scan of the block tables per call.
+ */
+#define PKV_HINT_SHARED_PREFIX 0x1
+
 /* Device error word bits (pkv_device_errors). */
 #define PKV_DEVERR_SLOT_OUT_OF_RANGE 0x1   /* slot_mapping entry >= num_blocks * block_size */
 #define PKV_DEVERR_BLOCK_OUT_OF_RANGE 0x2  /* block table entry outside [0, num_blocks) */
@@ -137,6 +153,7 @@ size_t paged_attention_workspace_min(int32_t num_seqs, int64_t num_tokens, int32
  *                   0 if unknown (only used to skip launching kernels with no work)
  *   scale           logit scale (e.g. 1/sqrt(head_dim))
  *   causal          non-zero: bottom-right aligned causal mask
+ *   hints           PKV_HINT_* bits (0: none)
  *   workspace       device scratch of workspace_bytes (>= paged_attention_workspace_min),
  *                   256-byte aligned; overwritten by the call; must not be shared by
  *                   calls that may run concurrently
@@ -153,8 +170,8 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
                                    int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
                                    int32_t block_size, int32_t max_blocks_per_seq,
                                    int32_t max_query_len, float scale, int32_t causal,
-                                   void* workspace, size_t workspace_bytes, pkv_dtype dtype,
-                                   void* stream);
+                                   int32_t hints, void* workspace, size_t workspace_bytes,
+                                   pkv_dtype dtype, void* stream);
 
 /*
  * paged_attention_forward_static_ws - paged_attention_forward for callers
@@ -184,7 +201,7 @@ pkv_status paged_attention_forward_static_ws(const void* q, const void* k_cache,
                                              int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
                                              int32_t block_size, int32_t max_blocks_per_seq,
                                              int32_t max_query_len, float scale, int32_t causal,
-                                             pkv_dtype dtype, void* stream);
+                                             int32_t hints, pkv_dtype dtype, void* stream);
 
 /* Bytes of the static scratch used by paged_attention_forward_static_ws. */
 size_t paged_attention_static_workspace_bytes(void);

@@ -33,6 +33,7 @@ LIB_PATH = os.path.join(_HERE, "libpaged_kv.so")
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_WORKSPACE = range(5)
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+HINT_SHARED_PREFIX = 0x1  # PKV_HINT_SHARED_PREFIX
 DEVERR = {
     "slot_out_of_range": 0x1,
     "block_out_of_range": 0x2,
@@ -78,8 +79,8 @@ def lib() -> ctypes.CDLL:
             L.paged_attention_workspace_min.argtypes = [c_i32, c_i64, c_i32, c_i32, c_i32]
             L.paged_attention_forward.restype = c_i32
             L.paged_attention_forward.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i64, c_i32,
-                                                  c_i32, c_i32, c_i64, c_i32, c_i32, c_i32, c_f, c_i32, c_vp,
-                                                  c_sz, c_i32, c_vp]
+                                                  c_i32, c_i32, c_i64, c_i32, c_i32, c_i32, c_f, c_i32, c_i32,
+                                                  c_vp, c_sz, c_i32, c_vp]
             L.pkv_last_error.restype = ctypes.c_char_p
             L.pkv_last_error.argtypes = []
             L.pkv_device_errors.restype = c_i32
@@ -162,13 +163,16 @@ def paged_attention_forward(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
                             block_tables: torch.Tensor, context_lens: torch.Tensor,
                             query_start_loc: torch.Tensor, scale: float, causal: bool = True, *,
                             out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                            max_query_len: int = 0) -> torch.Tensor:
+                            max_query_len: int = 0, shared_prefix: bool = False) -> torch.Tensor:
     """Varlen attention of ``q [T, Hq, D]`` through per-sequence block tables.
 
     ``context_lens[s]`` counts sequence s's tokens after this step's write
     (its query tokens included); query i of n sits at position L - n + i.
     ``workspace`` (uint8, >= ``workspace_min``) defaults to a cached buffer
     per (device, stream).  ``max_query_len`` is an optional host hint.
+    ``shared_prefix`` tells the call that consecutive sequences may start
+    with the same physical blocks (prefix caching): runs of them then read
+    their common prefix once (``PKV_HINT_SHARED_PREFIX``).
     """
     dev = _need_cuda(q, k_cache, v_cache, block_tables, context_lens, query_start_loc)
     if q.dtype not in DTYPE or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
@@ -205,7 +209,7 @@ def paged_attention_forward(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
             q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
             context_lens.data_ptr(), query_start_loc.data_ptr(), out.data_ptr(), B, T, Hq, Hkv, D, NB, bs,
             max(1, block_tables.shape[1]), int(max_query_len), float(scale), 1 if causal else 0,
-            workspace.data_ptr(), workspace.numel(), DTYPE[q.dtype], _stream(dev)))
+            HINT_SHARED_PREFIX if shared_prefix else 0, workspace.data_ptr(), workspace.numel(), DTYPE[q.dtype], _stream(dev)))
     return out
 
 

@@ -150,6 +150,10 @@ WorkspaceLayout workspace_layout(int B, int64_t T, int Hq, int Hkv, int D, size_
   off = align_up(off + (size_t)merge_cap * sizeof(MergeGroup));
   L.ticket_off = off;
   off = align_up(off + (size_t)merge_cap * sizeof(int));
+  L.seq_off = off;  // per-sequence planner scratch: prefix keys, group, tile-match mask
+  off = align_up(off + (size_t)B * 4 * sizeof(int));
+  L.pre_off = off;  // prefix groups (at most one per sequence)
+  off = align_up(off + (size_t)B * sizeof(PreGroup));
   const size_t fixed = off;
   const size_t per_row = sizeof(float2) + (size_t)D * sizeof(float);
   int64_t part_cap = 0;
@@ -257,8 +261,8 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
                                    const int32_t* query_start_loc, void* out, int32_t num_seqs, int64_t num_tokens,
                                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
                                    int32_t block_size, int32_t max_blocks_per_seq, int32_t max_query_len,
-                                   float scale, int32_t causal, void* workspace, size_t workspace_bytes,
-                                   pkv_dtype dtype, void* stream) {
+                                   float scale, int32_t causal, int32_t hints, void* workspace,
+                                   size_t workspace_bytes, pkv_dtype dtype, void* stream) {
   g_msg[0] = 0;
   const int B = num_seqs, Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim, bs = block_size;
   const int64_t T = num_tokens;
@@ -319,8 +323,12 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
     const int64_t want = std::max<int64_t>(G, (int64_t)max_query_len * G);
     tc_rows = want <= 4 ? 4 : want <= 8 ? 8 : kTcDecRows;
   }
+  // shared prefixes are read once per group by the tensor-core kernel, and
+  // the rest of each member's keys by the tensor-core decode kernel
+  const bool cascade = (hints & PKV_HINT_SHARED_PREFIX) != 0 && dectc;
   // with a host hint that no sequence has more rows than that, skip the launch
-  const bool mma_launch = mma_ok && !(max_query_len > 0 && (int64_t)max_query_len * G <= dec_rows_max);
+  const bool mma_launch =
+      mma_ok && (cascade || !(max_query_len > 0 && (int64_t)max_query_len * G <= dec_rows_max));
   const int dec_grid = dev->sms * dec_ctas;
 
   PlanParams pp{};
@@ -334,6 +342,8 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   pp.max_blocks = max_blocks_per_seq;
   pp.causal = causal ? 1 : 0;
   pp.mma_ok = mma_launch ? 1 : 0;
+  pp.cascade = cascade ? 1 : 0;
+  pp.block_tables = block_tables;
   pp.dec_rows_max = dec_rows_max;
   pp.dec_unit_rows = dectc ? tc_rows : kDecRows;
   pp.dec_tile_keys = dectc ? kMmaTileKeys : kDecTileKeys;
@@ -357,6 +367,12 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   pp.mma_items = mma_items;
   pp.merges = merges;
   pp.tickets = tickets;
+  int* seq_scratch = reinterpret_cast<int*>(ws + lay.seq_off);
+  pp.seq_pre = seq_scratch;
+  pp.seq_grp = seq_scratch + B;
+  pp.seq_mask = reinterpret_cast<uint32_t*>(seq_scratch + 2 * B);
+  pp.seq_tmp = seq_scratch + 3 * B;
+  pp.pre_groups = reinterpret_cast<PreGroup*>(ws + lay.pre_off);
   pp.out = out;
   pp.out_row_bytes = Hq * D * elem_bytes(dtype);
   pp.err = dev->err;

@@ -585,14 +585,40 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
         mbar_arrive(&bars->o_empty[ob]);
         const int nr = mt.nrows;
         if (mt.part < 0) {
+          // The item finishes its rows.  With a merge group it follows a
+          // shared prefix, whose partial rows (complete before this kernel
+          // started) are folded in: m = max, weights 2^(m_p - m).
+          int pre_base = 0, pre_n = 0, pre_stride = 0;
+          if (mt.grp >= 0) {
+            const MergeGroup gr = p.groups[mt.grp];
+            pre_base = gr.pre_base;
+            pre_n = gr.pre_n;
+            pre_stride = gr.pre_stride;
+          }
 #pragma unroll
           for (int r = 0; r < NR; ++r) {
             if (r < nr) {
+              float acc = __uint_as_float(o[r]), lt = lrow[r];
+              if (pre_n > 0) {
+                float M = mrow[r];
+                for (int c = 0; c < pre_n; ++c) M = fmaxf(M, __ldcg(&p.part_ml[pre_base + c * pre_stride + r]).x);
+                const float Mu = M == -CUDART_INF_F ? 0.f : M;
+                const float w0 = fast_exp2(mrow[r] - Mu);
+                acc *= w0;
+                lt *= w0;
+                for (int c = 0; c < pre_n; ++c) {
+                  const int slot = pre_base + c * pre_stride + r;
+                  const float2 ml = __ldcg(&p.part_ml[slot]);
+                  const float wt = fast_exp2(ml.x - Mu);
+                  lt = fmaf(wt, ml.y, lt);
+                  acc = fmaf(wt, __ldcg(&p.part_acc[(int64_t)slot * 128 + d]), acc);
+                }
+              }
               const int row = mt.row0 + r;
               const int tok = row / p.G, gh = row - tok * p.G;
               __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
                                     ((int64_t)(mt.qstart + tok) * p.Hq + (int64_t)mt.kvh * p.G + gh) * 128;
-              orow[d] = __float2bfloat16_rn(__uint_as_float(o[r]) / lrow[r]);
+              orow[d] = __float2bfloat16_rn(acc / lt);
             }
           }
           continue;
@@ -619,18 +645,23 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
         if (*flag_last == gr.nsplit - 1) {
           if (d == 0) __threadfence();
           named_barrier(2, 128);
+          // the splits' partial rows, then those over the group's shared prefix
+          // (written by the tensor-core kernel, which ran before this one)
+          const int nparts = gr.nsplit + gr.pre_n;
+          auto slot_of = [&](int k, int r) {
+            return k < gr.nsplit ? gr.part_base + k * gr.nrows + r : gr.pre_base + (k - gr.nsplit) * gr.pre_stride + r;
+          };
 #pragma unroll
           for (int r = 0; r < NR; ++r) {
             if (r < gr.nrows) {
               float M = -CUDART_INF_F;
 #pragma unroll 8
-              for (int sp = 0; sp < gr.nsplit; ++sp)
-                M = fmaxf(M, __ldcg(&p.part_ml[gr.part_base + sp * gr.nrows + r]).x);
+              for (int k = 0; k < nparts; ++k) M = fmaxf(M, __ldcg(&p.part_ml[slot_of(k, r)]).x);
               const float Mu = M == -CUDART_INF_F ? 0.f : M;
               float lt = 0.f, acc = 0.f;
 #pragma unroll 8
-              for (int sp = 0; sp < gr.nsplit; ++sp) {
-                const int slot = gr.part_base + sp * gr.nrows + r;
+              for (int k = 0; k < nparts; ++k) {
+                const int slot = slot_of(k, r);
                 const float2 ml = __ldcg(&p.part_ml[slot]);
                 const float wt = fast_exp2(ml.x - Mu);
                 lt = fmaf(wt, ml.y, lt);

@@ -626,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       }
       if (staged) fence_proxy_async_smem();  // the staged rows, for the TMA stores
       mbar_arrive(&bars->o_staged[qb]);
-      if (it.part >= 0) {
+      if (it.grp >= 0) {
         // The split that completes its merge group combines the group's
         // partial rows: m = max m_p, l = sum l_p 2^(m_p - m), O = sum acc_p 2^(m_p - m) / l.
         // Release: the barrier orders every thread's partial writes before one

@@ -21,6 +21,13 @@ constexpr int kMmaRows = 128;     // rows per tensor-core work item (M of the MM
 constexpr int kMmaTileKeys = 128;  // keys per tensor-core pipeline stage
 constexpr int kMaxSplits = 64;
 constexpr int kMaxPlanSeqs = 32768;  // sequences per call (the planner keeps per-sequence offsets on chip)
+// Shared prefixes ("cascade"): consecutive decode-shaped sequences whose
+// block tables start with the same physical blocks form a group when there
+// are at least kMinGroupSeqs of them; the group's common prefix (whole tiles
+// of kMmaTileKeys keys visible to all its queries, at most kMaxPreTiles) is
+// read once for all the group's rows, as multi-row tensor-core work.
+constexpr int kMinGroupSeqs = 4;
+constexpr int kMaxPreTiles = 31;
 
 struct alignas(16) PlanHeader {
   int n_dec;        // CUDA-core work items
@@ -32,7 +39,9 @@ struct alignas(16) PlanHeader {
   int dec_counter;  // work counters (dynamic item fetch), zeroed by the planner
   int mma_counter;
   int merge_counter;
-  int pad[7];
+  int n_pre;        // of the tensor-core items, those over shared prefixes (the last n_pre)
+  int n_groups;     // prefix groups read once
+  int pad[5];
 };
 
 // One unit of attention work: `nrows` rows of sequence `seq`, kv head `kvh`,
@@ -45,14 +54,26 @@ struct alignas(16) WorkItem {
 };
 
 // Split-KV merge: rows row0 .. row0+nrows-1 of (seq, kvh) have nsplit
-// partial states at part_base + p * nrows + r.
+// partial states at part_base + p * nrows + r, and pre_n more (over a shared
+// prefix, written before the split items run) at pre_base + c * pre_stride + r.
 struct alignas(16) MergeGroup {
   int seq, kvh, row0, nrows;
-  int nsplit, part_base, pad0, pad1;
+  int nsplit, part_base, pre_base, pre_n;
+  int pre_stride, pad0, pad1, pad2;
+};
+
+// A run of consecutive sequences s0 .. s1 sharing their first pre_keys keys
+// (planner scratch).  Its rows (tokens query_start_loc[s0] ..
+// query_start_loc[s1 + 1] - 1, G heads each) are cut into 128-row tiles; each
+// (kv head, tile) reads the prefix in npre chunks, whose partial rows sit at
+// part_off + (kvh * npre + c) * rows + row.
+struct alignas(16) PreGroup {
+  int s0, s1, pre_tiles, npre;
+  int rows, item_off, part_off, valid;
 };
 
 struct WorkspaceLayout {
-  size_t header_off, dec_off, mma_off, merge_off, ticket_off, ml_off, acc_off, total;
+  size_t header_off, dec_off, mma_off, merge_off, ticket_off, seq_off, pre_off, ml_off, acc_off, total;
   int dec_cap, mma_cap, merge_cap, part_cap;
 };
 
@@ -71,6 +92,8 @@ struct PlanParams {
   int max_blocks;   // block table row length
   int causal;
   int mma_ok;       // tensor-core path available for this call
+  int cascade;      // look for groups of sequences sharing a prefix (tensor-core decode only)
+  const int32_t* block_tables;
   int dec_rows_max;  // rows <= this go to the decode-shaped path when mma_ok
   int dec_unit_rows;  // rows per decode-shaped item (4 CUDA-core, 16 tensor-core)
   int dec_tile_keys;  // key tile of the decode-shaped kernel (splits are multiples)
@@ -83,6 +106,11 @@ struct PlanParams {
   WorkItem* mma_items;
   MergeGroup* merges;
   int* tickets;     // one per merge group, zeroed
+  int* seq_pre;     // [B] scratch: keys of each sequence's prefix read by its group (0: none)
+  int* seq_grp;     // [B] scratch: prefix group of each sequence
+  uint32_t* seq_mask;  // [B] scratch: tiles equal to the previous sequence's
+  int* seq_tmp;     // [B] scratch
+  PreGroup* pre_groups;  // [B] scratch
   void* out;        // rows of invalid sequences are zeroed
   int out_row_bytes;  // bytes of one token's output row (Hq * D * elem)
   int* err;

@@ -23,6 +23,17 @@
 // so that a long prefill sequence's many units spread over many threads.
 // Block-wide exclusive scans give every item a fixed slot (items ordered by
 // size class, then unit instance, then split).
+//
+// Shared prefixes (when the call asks for them): consecutive decode-shaped
+// sequences whose block tables start with the same physical blocks read
+// those keys once for the whole run ("cascade").  For each run of at least
+// kMinGroupSeqs sequences the common prefix (whole 128-key tiles visible to
+// every query of the run) becomes tensor-core items over the run's rows
+// (their tokens are contiguous in q), split into npre key chunks, each
+// writing partial rows; every member's own decode units then start after the
+// prefix, always as merge groups, whose merge folds in the prefix partials.
+// Those are complete before the decode kernel runs (the tensor-core kernel
+// precedes it in the stream).
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -30,6 +41,7 @@ namespace pkv {
 namespace {
 
 constexpr int kThreads = 512;
+
 constexpr int kWarps = kThreads / 32;
 constexpr int kClasses = 8;  // item size classes
 // per-thread counters: dec classes, mma classes, merge groups, partial rows (dec, mma)
@@ -40,9 +52,10 @@ struct SeqDesc {
   int n, L;
   bool valid, mma;
   int rows, unit_rows, units;
+  int pre;  // leading keys read by the sequence's prefix group (0: none)
 };
 
-__device__ __forceinline__ SeqDesc describe(const PlanParams& p, int s) {
+__device__ __forceinline__ SeqDesc describe_base(const PlanParams& p, int s) {
   SeqDesc d;
   const int a = __ldg(p.query_start_loc + s), b = __ldg(p.query_start_loc + s + 1);
   d.L = __ldg(p.context_lens + s);
@@ -53,6 +66,13 @@ __device__ __forceinline__ SeqDesc describe(const PlanParams& p, int s) {
   d.mma = p.mma_ok && d.rows > p.dec_rows_max;
   d.unit_rows = d.mma ? kMmaRows : p.dec_unit_rows;
   d.units = (d.rows + d.unit_rows - 1) / d.unit_rows;
+  d.pre = 0;
+  return d;
+}
+
+__device__ __forceinline__ SeqDesc describe(const PlanParams& p, int s) {
+  SeqDesc d = describe_base(p, s);
+  if (p.cascade) d.pre = p.seq_pre[s];
   return d;
 }
 
@@ -152,6 +172,196 @@ __device__ __forceinline__ void iter_next(UnitIter& t, const PlanParams& p, cons
   t.d = describe(p, s);
 }
 
+// Finds the runs of sequences sharing a prefix and sizes their prefix work:
+// sh_pre = {prefix items, prefix partial rows, groups read once, groups}.
+// Leaves, per sequence s: seq_pre[s] (keys read by its group, 0 if none),
+// seq_grp[s] (first partial row of its rows in the group's prefix partials,
+// relative to their base) and seq_tmp[s] (npre << 24 | the group's rows); and
+// pre_groups[] for the prefix items.  Called by the whole block.
+__device__ void plan_prefix_groups(const PlanParams& p, int* sh_pre) {
+  __shared__ int sh_npre;
+  const int tid = threadIdx.x, B = p.B;
+  const int bpt = kMmaTileKeys / p.bs;  // blocks per tile
+  const int per = (B + kThreads - 1) / kThreads;
+  const int a0 = min(B, tid * per), a1 = min(B, a0 + per);
+  int* eqb = reinterpret_cast<int*>(p.seq_mask);  // leading blocks equal to the predecessor's
+  // (a) whole tiles visible to every query of each decode-shaped sequence
+  for (int s = a0; s < a1; ++s) {
+    const SeqDesc d = describe_base(p, s);
+    p.seq_pre[s] = (d.valid && !d.mma && d.n > 0) ? min(kMaxPreTiles, (d.L - d.n) / kMmaTileKeys) : 0;
+  }
+  __syncthreads();
+  // (b) candidates: the first block equals the predecessor's.  Their equal
+  // leading blocks start at the shared limit and come down to the first
+  // differing block below; listed in seq_tmp.
+  int nc = 0;
+  for (int s = a0; s < a1; ++s) {
+    int lim = 0;
+    if (s >= 1 && p.seq_pre[s] > 0 && p.seq_pre[s - 1] > 0 &&
+        __ldg(p.block_tables + (int64_t)s * p.max_blocks) == __ldg(p.block_tables + (int64_t)(s - 1) * p.max_blocks))
+      lim = min(p.seq_pre[s], p.seq_pre[s - 1]) * bpt;
+    eqb[s] = lim;
+    nc += lim > 0;
+  }
+  {
+    int v[1] = {nc}, tot[1];
+    block_scan<1>(v, tot);  // also orders the writes above before the reads below
+    int o = v[0];
+    for (int s = a0; s < a1; ++s)
+      if (eqb[s] > 0) p.seq_tmp[o++] = s;
+    nc = tot[0];
+  }
+  __syncthreads();
+  // (c) compare the candidates' rows with their predecessors' in groups of
+  // four blocks, eight groups per thread and round, all loads of a round in
+  // flight together; the first differing block lowers eqb[s]
+  {
+    const int nq = (kMaxPreTiles * bpt + 3) / 4;
+    const bool vec = (p.max_blocks & 3) == 0 && (reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0;
+    for (int k0 = tid; k0 < nc * nq; k0 += 8 * kThreads) {
+      int sq[8], b0q[8], limq[8];
+      int4 x[8], y[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u * kThreads;
+        sq[u] = -1;
+        b0q[u] = 0;
+        limq[u] = 0;
+        x[u] = y[u] = make_int4(0, 0, 0, 0);
+        if (k >= nc * nq) continue;
+        const int s = p.seq_tmp[k / nq], b0 = (k % nq) * 4;
+        const int lim = min(p.seq_pre[s], p.seq_pre[s - 1]) * bpt;
+        if (b0 >= lim) continue;
+        sq[u] = s;
+        b0q[u] = b0;
+        limq[u] = lim;
+        const int32_t* prev = p.block_tables + (int64_t)(s - 1) * p.max_blocks + b0;
+        const int32_t* cur = prev + p.max_blocks;
+        if (vec) {
+          x[u] = __ldg(reinterpret_cast<const int4*>(prev));
+          y[u] = __ldg(reinterpret_cast<const int4*>(cur));
+        } else {
+          const int m = min(4, lim - b0);
+          x[u].x = __ldg(prev);
+          y[u].x = __ldg(cur);
+          if (m > 1) { x[u].y = __ldg(prev + 1); y[u].y = __ldg(cur + 1); }
+          if (m > 2) { x[u].z = __ldg(prev + 2); y[u].z = __ldg(cur + 2); }
+          if (m > 3) { x[u].w = __ldg(prev + 3); y[u].w = __ldg(cur + 3); }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (sq[u] < 0) continue;
+        const int m = min(4, limq[u] - b0q[u]);
+        int j = m;  // first differing block of the group (m: none)
+        if (m > 3 && x[u].w != y[u].w) j = 3;
+        if (m > 2 && x[u].z != y[u].z) j = 2;
+        if (m > 1 && x[u].y != y[u].y) j = 1;
+        if (x[u].x != y[u].x) j = 0;
+        if (j < m) atomicMin(&eqb[sq[u]], b0q[u] + j);
+      }
+    }
+  }
+  __syncthreads();
+  // (d) runs: a sequence with no leading tile equal to its predecessor's starts one
+  auto equal_tiles = [&](int s) { return eqb[s] / bpt; };
+  int ng = 0;
+  {
+    int nl = 0;
+    for (int s = a0; s < a1; ++s) nl += equal_tiles(s) == 0;
+    int v[1] = {nl}, tot[1];
+    block_scan<1>(v, tot);
+    int g = v[0] - 1;
+    for (int s = a0; s < a1; ++s) {
+      if (equal_tiles(s) == 0) {
+        ++g;
+        PreGroup pg{};
+        pg.s0 = s;
+        pg.s1 = s;
+        pg.pre_tiles = kMaxPreTiles;
+        p.pre_groups[g] = pg;
+      }
+      p.seq_grp[s] = g;
+    }
+    ng = tot[0];
+  }
+  __syncthreads();
+  for (int s = a0; s < a1; ++s) {
+    const int g = p.seq_grp[s], c = equal_tiles(s);
+    if (c > 0) atomicMin(&p.pre_groups[g].pre_tiles, c);  // the run's common prefix
+    if (s == B - 1 || equal_tiles(s + 1) == 0) p.pre_groups[g].s1 = s;
+  }
+  __syncthreads();
+  // (e) size the prefix work: about target_mma items in all, and at most half
+  // the partial rows of the workspace, or none at all
+  const int gper = (ng + kThreads - 1) / kThreads;
+  const int g0 = min(ng, tid * gper), g1 = min(ng, g0 + gper);
+  int rtiles = 0, rows = 0;
+  for (int g = g0; g < g1; ++g) {
+    PreGroup& pg = p.pre_groups[g];
+    pg.rows = (p.query_start_loc[pg.s1 + 1] - p.query_start_loc[pg.s0]) * p.G;
+    if (pg.s1 - pg.s0 + 1 < kMinGroupSeqs) continue;
+    rtiles += p.Hkv * ((pg.rows + kMmaRows - 1) / kMmaRows);
+    rows += p.Hkv * pg.rows;
+  }
+  {
+    int v[2] = {rtiles, rows}, tot[2];
+    block_scan<2>(v, tot);
+    if (tid == 0) {
+      int npre = tot[0] > 0 ? (p.target_mma + tot[0] - 1) / tot[0] : 0;
+      npre = min(npre, kMaxPreTiles);
+      while (npre > 0 && (int64_t)tot[1] * npre > p.part_cap / 2) --npre;
+      sh_npre = npre;
+    }
+    __syncthreads();
+  }
+  const int npre = sh_npre;
+  int nitems = 0, nrows = 0, nvalid = 0;
+  for (int g = g0; g < g1; ++g) {
+    PreGroup& pg = p.pre_groups[g];
+    pg.valid = npre > 0 && pg.s1 - pg.s0 + 1 >= kMinGroupSeqs && pg.pre_tiles >= 1;
+    if (pg.valid) {
+      const int chunk_tiles = (pg.pre_tiles + min(npre, pg.pre_tiles) - 1) / min(npre, pg.pre_tiles);
+      pg.npre = (pg.pre_tiles + chunk_tiles - 1) / chunk_tiles;
+      nitems += p.Hkv * ((pg.rows + kMmaRows - 1) / kMmaRows) * pg.npre;
+      nrows += p.Hkv * pg.rows * pg.npre;
+      ++nvalid;
+    } else {
+      pg.npre = 0;
+    }
+  }
+  {
+    int v[3] = {nitems, nrows, nvalid}, tot[3];
+    block_scan<3>(v, tot);
+    int io = v[0], ro = v[1];
+    for (int g = g0; g < g1; ++g) {
+      PreGroup& pg = p.pre_groups[g];
+      pg.item_off = io;
+      pg.part_off = ro;
+      if (pg.valid) {
+        io += p.Hkv * ((pg.rows + kMmaRows - 1) / kMmaRows) * pg.npre;
+        ro += p.Hkv * pg.rows * pg.npre;
+      }
+    }
+    if (tid == 0) {
+      sh_pre[0] = tot[0];
+      sh_pre[1] = tot[1];
+      sh_pre[2] = tot[2];
+      sh_pre[3] = ng;
+    }
+  }
+  __syncthreads();
+  // (f) each member's suffix starts after its group's prefix; where its rows'
+  // prefix partials are
+  for (int s = a0; s < a1; ++s) {
+    const PreGroup pg = p.pre_groups[p.seq_grp[s]];
+    p.seq_pre[s] = pg.valid ? pg.pre_tiles * kMmaTileKeys : 0;
+    p.seq_grp[s] = pg.valid ? pg.part_off + (p.query_start_loc[s] - p.query_start_loc[pg.s0]) * p.G : 0;
+    p.seq_tmp[s] = pg.valid ? (pg.npre << 24) | pg.rows : 0;
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   // The attention kernel may start its prologue while this plans (it waits
   // for this grid).  This grid waits for its own predecessor before reading
@@ -161,6 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   extern __shared__ int seq_off[];  // [B + 1]: first unit of each sequence (per kv head)
   const int tid = threadIdx.x;
   const int B = p.B;
+
+  // ---- shared-prefix groups
+  __shared__ int sh_pre[4];  // prefix items, prefix partial rows, groups read once, groups
+  if (tid == 0) sh_pre[0] = sh_pre[1] = sh_pre[2] = sh_pre[3] = 0;
+  __syncthreads();
+  if (p.cascade) plan_prefix_groups(p, sh_pre);
 
   // ---- units per sequence; zero the rows of invalid sequences
   for (int s = tid; s < B; s += kThreads) {
@@ -207,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   {
     UnitIter t{i0, i1, U, B, 0, 0, 0, {}};
     for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off))
-      (t.d.mma ? w_mma : w_dec) += (unsigned long long)unit_keys(t.d, t.u, p.G, p.causal);
+      (t.d.mma ? w_mma : w_dec) += (unsigned long long)(unit_keys(t.d, t.u, p.G, p.causal) - t.d.pre);
   }
   // warp sums, then one thread adds the warps' (no contended 64-bit atomics)
 #pragma unroll
@@ -251,14 +467,15 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       const SeqDesc& d = t.d;
       const int chunk = d.mma ? cm : cd;
       const int cb = d.mma ? kClasses : 0;
-      const int keys = unit_keys(d, t.u, p.G, p.causal);
+      const int keys = unit_keys(d, t.u, p.G, p.causal) - d.pre;
       int ns, per;
       split_of(keys, chunk, d.mma ? kMmaTileKeys : p.dec_tile_keys, ns, per);
       s_cnt[cb + size_class(per, chunk)][tid] += ns - 1;  // all splits but the last are full
       s_cnt[cb + size_class(keys - (ns - 1) * per, chunk)][tid] += 1;
-      if (ns > 1) {
+      if (ns > 1 || d.pre > 0) {
         s_cnt[kCntMerge][tid] += 1;
-        s_cnt[d.mma ? kCntPartMma : kCntPartDec][tid] += ns * min(d.rows - t.u * d.unit_rows, d.unit_rows);
+        if (ns > 1)
+          s_cnt[d.mma ? kCntPartMma : kCntPartDec][tid] += ns * min(d.rows - t.u * d.unit_rows, d.unit_rows);
       }
     }
 #pragma unroll
@@ -272,8 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
         nm += tot[kClasses + k];
       }
       const int pd = tot[kCntPartDec], pm = tot[kCntPartMma];
-      const bool fits = nd <= p.dec_cap && nm <= p.mma_cap && tot[kCntMerge] <= p.merge_cap &&
-                        (int64_t)pd + pm <= p.part_cap;
+      const bool fits = nd <= p.dec_cap && nm + sh_pre[0] <= p.mma_cap && tot[kCntMerge] <= p.merge_cap &&
+                        (int64_t)pd + pm + sh_pre[1] <= p.part_cap;
       sh_state = fits ? 1 : 0;
       // Once: if the decode items are mostly full chunks (long sequences
       // split) and leave a last wave less than half full, grow the chunk so
@@ -320,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       base_mma += tot[kClasses + k];
     }
   }
+  const int pre_part_base = tot[kCntPartDec] + tot[kCntPartMma];  // prefix partial rows follow the units'
   int off_grp = cnt[kCntMerge];
   int off_part = cnt[kCntPartDec] + cnt[kCntPartMma];
   {
@@ -330,16 +548,21 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       WorkItem* items = d.mma ? p.mma_items : p.dec_items;
       const int chunk = d.mma ? cm : cd;
       const int cbase = d.mma ? kClasses : 0;
-      const int keys = unit_keys(d, u, p.G, p.causal);
+      const int kend = unit_keys(d, u, p.G, p.causal);
+      const int keys = kend - d.pre;
       const int r0 = u * d.unit_rows;
       const int nr = min(d.rows - r0, d.unit_rows);
       int ns, per;
       split_of(keys, chunk, d.mma ? kMmaTileKeys : p.dec_tile_keys, ns, per);
       int grp = -1, part_base = 0;
-      if (ns > 1) {
+      if (ns > 1 || d.pre > 0) {
+        // A unit after a shared prefix always names a merge group (where its
+        // prefix partials are); unsplit, its one item folds them in itself.
         grp = off_grp++;
-        part_base = off_part;
-        off_part += ns * nr;
+        if (ns > 1) {
+          part_base = off_part;
+          off_part += ns * nr;
+        }
         MergeGroup g;
         g.seq = s;
         g.kvh = kvh;
@@ -347,7 +570,17 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
         g.nrows = nr;
         g.nsplit = ns;
         g.part_base = part_base;
-        g.pad0 = g.pad1 = 0;
+        g.pre_base = 0;
+        g.pre_n = 0;
+        g.pre_stride = 0;
+        g.pad0 = g.pad1 = g.pad2 = 0;
+        if (d.pre > 0) {
+          // this unit's rows in its group's prefix partials ([kvh][chunk][row])
+          const int nr_g = p.seq_tmp[s], npre = nr_g >> 24, grows = nr_g & 0xffffff;
+          g.pre_base = pre_part_base + p.seq_grp[s] + kvh * npre * grows + r0;
+          g.pre_n = npre;
+          g.pre_stride = grows;
+        }
         p.merges[grp] = g;
         p.tickets[grp] = 0;
       }
@@ -359,12 +592,40 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
         it.kvh = kvh;
         it.row0 = r0;
         it.nrows = nr;
-        it.kb = sp * per;
-        it.ke = min(keys, (sp + 1) * per);
+        it.kb = d.pre + sp * per;
+        it.ke = min(kend, d.pre + (sp + 1) * per);
         it.part = ns > 1 ? part_base + sp * nr : -1;
         it.grp = grp;
         items[s_cnt[sp == ns - 1 ? last_cls : full_cls][tid]++] = it;
       }
+    }
+  }
+  // ---- prefix items, after the other tensor-core items
+  if (sh_pre[0] > 0) {
+    int nm = 0;
+#pragma unroll
+    for (int k = 0; k < kClasses; ++k) nm += tot[kClasses + k];
+    const int ng = sh_pre[3];
+    for (int g = tid; g < ng; g += kThreads) {
+      const PreGroup pg = p.pre_groups[g];
+      if (!pg.valid) continue;
+      const int rt = (pg.rows + kMmaRows - 1) / kMmaRows;
+      const int per_keys = (pg.pre_tiles + pg.npre - 1) / pg.npre * kMmaTileKeys;
+      int idx = nm + pg.item_off;
+      for (int kvh = 0; kvh < p.Hkv; ++kvh)
+        for (int t = 0; t < rt; ++t)
+          for (int c = 0; c < pg.npre; ++c) {
+            WorkItem it;
+            it.seq = pg.s0;  // the group's rows are its tokens onwards
+            it.kvh = kvh;
+            it.row0 = t * kMmaRows;
+            it.nrows = min(kMmaRows, pg.rows - it.row0);
+            it.kb = c * per_keys;
+            it.ke = min(pg.pre_tiles * kMmaTileKeys, (c + 1) * per_keys);
+            it.part = pre_part_base + pg.part_off + (kvh * pg.npre + c) * pg.rows + it.row0;
+            it.grp = -1;  // merged by the decode kernel, with the members' own keys
+            p.mma_items[idx++] = it;
+          }
     }
   }
   if (tid == 0) {
@@ -375,11 +636,13 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       nm += tot[kClasses + k];
     }
     p.header->n_dec = nd;
-    p.header->n_mma = nm;
+    p.header->n_mma = nm + sh_pre[0];
+    p.header->n_pre = sh_pre[0];
+    p.header->n_groups = sh_pre[2];
     p.header->n_merge = tot[kCntMerge];
     p.header->chunk_dec = cd;
     p.header->chunk_mma = cm;
-    p.header->part_rows = tot[kCntPartDec] + tot[kCntPartMma];
+    p.header->part_rows = tot[kCntPartDec] + tot[kCntPartMma] + sh_pre[1];
     p.header->dec_counter = 0;
     p.header->mma_counter = 0;
     p.header->merge_counter = 0;

@@ -68,7 +68,7 @@ pkv_status paged_attention_forward_static_ws(const void* q, const void* k_cache,
                                              int64_t num_tokens, int32_t num_q_heads, int32_t num_kv_heads,
                                              int32_t head_dim, int64_t num_blocks, int32_t block_size,
                                              int32_t max_blocks_per_seq, int32_t max_query_len, float scale,
-                                             int32_t causal, pkv_dtype dtype, void* stream) {
+                                             int32_t causal, int32_t hints, pkv_dtype dtype, void* stream) {
   const size_t need = paged_attention_workspace_min(num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim);
   if (need > kStaticWorkspaceBytes) {
     char msg[200];
@@ -82,7 +82,7 @@ pkv_status paged_attention_forward_static_ws(const void* q, const void* k_cache,
   if (st != PKV_OK) return st;
   return paged_attention_forward(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, out, num_seqs,
                                  num_tokens, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
-                                 max_blocks_per_seq, max_query_len, scale, causal, ws, kStaticWorkspaceBytes,
+                                 max_blocks_per_seq, max_query_len, scale, causal, hints, ws, kStaticWorkspaceBytes,
                                  dtype, stream);
 }
 

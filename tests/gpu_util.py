@@ -52,13 +52,15 @@ class DeviceWorkload:
                     bt=torch.from_numpy(st.block_tables).to(d), ctx=torch.from_numpy(st.context_lens).to(d),
                     qsl=torch.from_numpy(st.query_start_loc).to(d))
 
-    def run_step(self, i: int = 0, *, workspace=None, max_query_len: int = 0) -> torch.Tensor:
+    def run_step(self, i: int = 0, *, workspace=None, max_query_len: int = 0,
+                 shared_prefix: bool = False) -> torch.Tensor:
         st = self.w.steps[i]
         t = self.step_tensors(st)
         pkv.paged_kv_write(t["k"], t["v"], t["slots"], self.kc, self.vc)
         po.kv_write(st.k_new, st.v_new, st.slot_mapping, self.kc_host, self.vc_host)
         out = pkv.paged_attention_forward(t["q"], self.kc, self.vc, t["bt"], t["ctx"], t["qsl"], self.w.scale,
-                                          self.w.causal, workspace=workspace, max_query_len=max_query_len)
+                                          self.w.causal, workspace=workspace, max_query_len=max_query_len,
+                                          shared_prefix=shared_prefix)
         torch.cuda.synchronize()
         return out
 

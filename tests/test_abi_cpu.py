@@ -49,20 +49,20 @@ def test_workspace_sizes_are_host_arithmetic(lib):
 def test_host_checks_need_no_gpu(lib):
     # num_q_heads not a multiple of num_kv_heads: rejected before any CUDA call
     st = lib.paged_attention_forward(None, None, None, None, None, None, None, 1, 1, 6, 4, 128, 4, 16, 1, 0,
-                                     ctypes.c_float(0.1), 1, None, 0, 1, None)
+                                     ctypes.c_float(0.1), 1, 0, None, 0, 1, None)
     assert st == 1 and b"num_kv_heads" in lib.pkv_last_error()
     st = lib.paged_attention_forward(None, None, None, None, None, None, None, 1, 1, 8, 4, 96, 4, 16, 1, 0,
-                                     ctypes.c_float(0.1), 1, None, 0, 1, None)
+                                     ctypes.c_float(0.1), 1, 0, None, 0, 1, None)
     assert st == 2 and b"head_dim" in lib.pkv_last_error()
     st = lib.paged_attention_forward(None, None, None, None, None, None, None, 1, 1, 8, 4, 128, 4, 24, 1, 0,
-                                     ctypes.c_float(0.1), 1, None, 0, 1, None)
+                                     ctypes.c_float(0.1), 1, 0, None, 0, 1, None)
     assert st == 2 and b"block_size" in lib.pkv_last_error()
     st = lib.paged_attention_forward(None, None, None, None, None, None, None, 1, 1, 8, 4, 128, 4, 16, 1, 0,
-                                     ctypes.c_float(0.1), 1, None, 0, 7, None)
+                                     ctypes.c_float(0.1), 1, 0, None, 0, 7, None)
     assert st == 2
     # empty batches are no-ops
     assert lib.paged_attention_forward(None, None, None, None, None, None, None, 0, 0, 8, 4, 128, 4, 16, 1, 0,
-                                       ctypes.c_float(0.1), 1, None, 0, 1, None) == 0
+                                       ctypes.c_float(0.1), 1, 0, None, 0, 1, None) == 0
     assert lib.paged_kv_write(None, None, None, None, None, 0, 4, 16, 4, 128, 0, 0, 1, None) == 0
     # bad token stride
     assert lib.paged_kv_write(None, None, None, None, None, 3, 4, 16, 4, 128, 100, 0, 1, None) == 1

@@ -30,7 +30,7 @@ def _entry():
     f = pkv.lib().paged_attention_forward_static_ws
     f.restype = c_i32
     f.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i64, c_i32, c_i32, c_i32, c_i64, c_i32, c_i32,
-                  c_i32, c_f, c_i32, c_i32, c_vp]
+                  c_i32, c_f, c_i32, c_i32, c_i32, c_vp]
     return f
 
 
@@ -38,7 +38,7 @@ def _call(f, t, kc, vc, out, w, T, max_q):
     NB, bs, Hkv, D = kc.shape
     return f(t["q"].data_ptr(), kc.data_ptr(), vc.data_ptr(), t["bt"].data_ptr(), t["ctx"].data_ptr(),
              t["qsl"].data_ptr(), out.data_ptr(), t["ctx"].shape[0], T, w.num_q_heads, Hkv, D, NB, bs,
-             t["bt"].shape[1], max_q, w.scale, 1 if w.causal else 0, 1 if w.dtype == "bf16" else 0,
+             t["bt"].shape[1], max_q, w.scale, 1 if w.causal else 0, 0, 1 if w.dtype == "bf16" else 0,
              torch.cuda.current_stream().cuda_stream)
 
 
@@ -73,7 +73,7 @@ def test_static_scratch_rejects_oversized_batch():
     assert pkv.workspace_min(4, T, 32, 8, 128) > cap()
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
     p = dummy.data_ptr()
-    status = f(p, p, p, p, p, p, p, 4, T, 32, 8, 128, 16, 16, 1, 0, 0.1, 1, 1,
+    status = f(p, p, p, p, p, p, p, 4, T, 32, 8, 128, 16, 16, 1, 0, 0.1, 1, 0, 1,
                torch.cuda.current_stream().cuda_stream)
     assert status == pkv.PKV_ERR_WORKSPACE
     assert b"static scratch" in pkv.lib().pkv_last_error()

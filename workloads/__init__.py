@@ -191,6 +191,7 @@ def build(
     dtype: str,
     seed: int,
     shared_prefix_tokens: int = 0,
+    share_groups=None,
     poison: bool = False,
     max_blocks_per_seq: int | None = None,
     causal: bool = True,
@@ -201,7 +202,10 @@ def build(
     """Build a one-step workload from per-sequence context and query lengths.
 
     ``shared_prefix_tokens`` (a multiple of ``block_size``) are held in the same
-    physical blocks by every sequence.  ``block_order`` is ``"permutation"``
+    physical blocks by every sequence.  ``share_groups``, a list of
+    ``(first_seq, last_seq, tokens)``, instead gives each listed run of
+    sequences its own shared prefix (disjoint runs; ``tokens`` a multiple of
+    ``block_size``); other sequences keep all their blocks private.  ``block_order`` is ``"permutation"``
     (a seeded random permutation of the pool) or ``"sequential"``.
     """
     L = np.asarray(context_lens, dtype=np.int64)
@@ -210,30 +214,47 @@ def build(
     bs = block_size
     if n.shape != L.shape or np.any(n < 0) or np.any(n > L):
         raise ValueError("need 0 <= q_len <= context_len per sequence")
-    if shared_prefix_tokens % bs:
-        raise ValueError("shared prefix must fill whole blocks")
-    if shared_prefix_tokens and np.any(L - n < shared_prefix_tokens):
-        raise ValueError("new tokens must lie after the shared prefix")
+    if share_groups is None:
+        share_groups = [(0, B - 1, shared_prefix_tokens)] if B and shared_prefix_tokens else []
+    elif shared_prefix_tokens:
+        raise ValueError("give shared_prefix_tokens or share_groups, not both")
+    share = np.zeros(B, dtype=np.int64)        # shared tokens of each sequence
+    share_gid = np.full(B, -1, dtype=np.int64)
+    for gi, (a, b, tok) in enumerate(share_groups):
+        if tok % bs:
+            raise ValueError("shared prefix must fill whole blocks")
+        if not (0 <= a <= b < B) or np.any(share_gid[a:b + 1] >= 0):
+            raise ValueError("share groups must be disjoint runs of sequences")
+        if np.any(L[a:b + 1] - n[a:b + 1] < tok):
+            raise ValueError("new tokens must lie after the shared prefix")
+        share[a:b + 1] = tok
+        share_gid[a:b + 1] = gi
     ss = np.random.SeedSequence(seed)
     s_layout, s_q, s_k, s_v, s_kc, s_vc = ss.spawn(6)
     g_layout = np.random.Generator(np.random.PCG64(s_layout))
 
     nblk = (L + bs - 1) // bs
-    n_shared = shared_prefix_tokens // bs
+    n_sh = share // bs  # shared blocks of each sequence
     mb = int(max_blocks_per_seq or max(1, int(nblk.max(initial=1))))
     if np.any(nblk > mb):
         raise ValueError("max_blocks_per_seq too small")
-    need = n_shared + int(np.sum(np.maximum(nblk - n_shared, 0)))
+    need = sum(tok // bs for (_, _, tok) in share_groups) + int(np.sum(np.maximum(nblk - n_sh, 0)))
     if need > num_blocks:
         raise ValueError(f"pool too small: need {need} blocks, have {num_blocks}")
     order = g_layout.permutation(num_blocks) if block_order == "permutation" else np.arange(num_blocks)
-    shared_ids = order[:n_shared]
-    cursor = n_shared
+    # the groups' shared blocks first (in group order), then private blocks in sequence order
+    group_ids = []
+    cursor = 0
+    for (_, _, tok) in share_groups:
+        group_ids.append(order[cursor:cursor + tok // bs])
+        cursor += tok // bs
     bt = np.full((B, mb), -1, dtype=np.int32)
     for s in range(B):
-        bt[s, :min(n_shared, nblk[s])] = shared_ids[:min(n_shared, nblk[s])]
-        priv = int(max(nblk[s] - n_shared, 0))
-        bt[s, n_shared:n_shared + priv] = order[cursor:cursor + priv]
+        k = int(n_sh[s])
+        if k:
+            bt[s, :min(k, nblk[s])] = group_ids[share_gid[s]][:min(k, nblk[s])]
+        priv = int(max(nblk[s] - k, 0))
+        bt[s, k:k + priv] = order[cursor:cursor + priv]
         cursor += priv
 
     Hkv, D, Hq = num_kv_heads, head_dim, num_q_heads
@@ -243,9 +264,9 @@ def build(
 
     # cached (already written) tokens: the shared prefix once, then each
     # sequence's private cached positions
-    cached_slots = [slots_of(bt[0], np.arange(shared_prefix_tokens), bs)] if B and shared_prefix_tokens else []
+    cached_slots = [slots_of(bt[a], np.arange(tok), bs) for (a, _, tok) in share_groups if tok]
     for s in range(B):
-        pos = np.arange(shared_prefix_tokens, L[s] - n[s])
+        pos = np.arange(share[s], L[s] - n[s])
         cached_slots.append(slots_of(bt[s], pos, bs))
     cached_slots = np.concatenate(cached_slots) if cached_slots else np.zeros(0, np.int64)
     nc = cached_slots.shape[0]
@@ -270,7 +291,8 @@ def build(
         name=name, dtype=dtype, num_blocks=num_blocks, block_size=bs, num_q_heads=Hq,
         num_kv_heads=Hkv, head_dim=D, k_cache=k_cache, v_cache=v_cache, steps=[step],
         scale=(1.0 / math.sqrt(D)) if scale is None else float(scale), causal=causal,
-        meta=dict(meta or {}, shared_prefix_tokens=shared_prefix_tokens, seed=seed),
+        meta=dict(meta or {}, shared_prefix_tokens=shared_prefix_tokens,
+                  share_groups=[tuple(int(x) for x in g) for g in share_groups], seed=seed),
     )
 
 
