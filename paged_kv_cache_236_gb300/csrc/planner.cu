@@ -178,7 +178,7 @@ __device__ __forceinline__ void iter_next(UnitIter& t, const PlanParams& p, cons
 // seq_grp[s] (first partial row of its rows in the group's prefix partials,
 // relative to their base) and seq_tmp[s] (npre << 24 | the group's rows); and
 // pre_groups[] for the prefix items.  Called by the whole block.
-__device__ void plan_prefix_groups(const PlanParams& p, int* sh_pre) {
+__device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre) {
   __shared__ int sh_npre;
   const int tid = threadIdx.x, B = p.B;
   const int bpt = kMmaTileKeys / p.bs;  // blocks per tile
