@@ -52,7 +52,9 @@ struct SeqDesc {
   int n, L;
   bool valid, mma;
   int rows, unit_rows, units;
-  int pre;  // leading keys read by the sequence's prefix group (0: none)
+  int pre;        // leading keys read by the sequence's prefix group (0: none)
+  int pre_rel;    // its rows' first prefix partial row, relative to the group's
+  int pre_shape;  // npre << 24 | the group's rows
 };
 
 __device__ __forceinline__ SeqDesc describe_base(const PlanParams& p, int s) {
@@ -72,7 +74,12 @@ __device__ __forceinline__ SeqDesc describe_base(const PlanParams& p, int s) {
 
 __device__ __forceinline__ SeqDesc describe(const PlanParams& p, int s) {
   SeqDesc d = describe_base(p, s);
-  if (p.cascade) d.pre = p.seq_pre[s];
+  d.pre_rel = d.pre_shape = 0;
+  if (p.cascade) {
+    d.pre = p.seq_pre[s];
+    d.pre_rel = p.seq_grp[s];
+    d.pre_shape = p.seq_tmp[s];
+  }
   return d;
 }
 
@@ -193,7 +200,7 @@ __device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre)
   __syncthreads();
   // (b) candidates: the first block equals the predecessor's.  Their equal
   // leading blocks start at the shared limit and come down to the first
-  // differing block below; listed in seq_tmp.
+  // differing block below; listed in seq_tmp as s | limit << 16.
   int nc = 0;
   for (int s = a0; s < a1; ++s) {
     int lim = 0;
@@ -208,29 +215,32 @@ __device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre)
     block_scan<1>(v, tot);  // also orders the writes above before the reads below
     int o = v[0];
     for (int s = a0; s < a1; ++s)
-      if (eqb[s] > 0) p.seq_tmp[o++] = s;
+      if (eqb[s] > 0) p.seq_tmp[o++] = s | eqb[s] << 16;
     nc = tot[0];
   }
   __syncthreads();
   // (c) compare the candidates' rows with their predecessors' in groups of
-  // four blocks, eight groups per thread and round, all loads of a round in
-  // flight together; the first differing block lowers eqb[s]
+  // four blocks: each thread a contiguous range of (candidate, group) pairs,
+  // eight per round with all their loads in flight together; the first
+  // differing block lowers eqb[s]
   {
+    static_assert(kMaxPreTiles * (kMmaTileKeys / 8) < (1 << 15) && kMaxPlanSeqs <= (1 << 16), "packed candidates");
     const int nq = (kMaxPreTiles * bpt + 3) / 4;
     const bool vec = (p.max_blocks & 3) == 0 && (reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0;
-    for (int k0 = tid; k0 < nc * nq; k0 += 8 * kThreads) {
+    const int nk = nc * nq, kper = (nk + kThreads - 1) / kThreads;
+    const int kb0 = min(nk, tid * kper), kb1 = min(nk, kb0 + kper);
+    for (int k0 = kb0; k0 < kb1; k0 += 8) {
       int sq[8], b0q[8], limq[8];
       int4 x[8], y[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int k = k0 + u * kThreads;
+        const int k = k0 + u;
         sq[u] = -1;
         b0q[u] = 0;
         limq[u] = 0;
         x[u] = y[u] = make_int4(0, 0, 0, 0);
-        if (k >= nc * nq) continue;
-        const int s = p.seq_tmp[k / nq], b0 = (k % nq) * 4;
-        const int lim = min(p.seq_pre[s], p.seq_pre[s - 1]) * bpt;
+        if (k >= kb1) continue;
+        const int e = p.seq_tmp[k / nq], s = e & 0xffff, lim = e >> 16, b0 = (k % nq) * 4;
         if (b0 >= lim) continue;
         sq[u] = s;
         b0q[u] = b0;
@@ -576,8 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
         g.pad0 = g.pad1 = g.pad2 = 0;
         if (d.pre > 0) {
           // this unit's rows in its group's prefix partials ([kvh][chunk][row])
-          const int nr_g = p.seq_tmp[s], npre = nr_g >> 24, grows = nr_g & 0xffffff;
-          g.pre_base = pre_part_base + p.seq_grp[s] + kvh * npre * grows + r0;
+          const int npre = d.pre_shape >> 24, grows = d.pre_shape & 0xffffff;
+          g.pre_base = pre_part_base + d.pre_rel + kvh * npre * grows + r0;
           g.pre_n = npre;
           g.pre_stride = grows;
         }
@@ -606,26 +616,36 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
 #pragma unroll
     for (int k = 0; k < kClasses; ++k) nm += tot[kClasses + k];
     const int ng = sh_pre[3];
-    for (int g = tid; g < ng; g += kThreads) {
-      const PreGroup pg = p.pre_groups[g];
-      if (!pg.valid) continue;
+    // item k of a group: kv head, row tile, key chunk (chunk fastest)
+    auto emit = [&](const PreGroup& pg, int k) {
       const int rt = (pg.rows + kMmaRows - 1) / kMmaRows;
       const int per_keys = (pg.pre_tiles + pg.npre - 1) / pg.npre * kMmaTileKeys;
-      int idx = nm + pg.item_off;
-      for (int kvh = 0; kvh < p.Hkv; ++kvh)
-        for (int t = 0; t < rt; ++t)
-          for (int c = 0; c < pg.npre; ++c) {
-            WorkItem it;
-            it.seq = pg.s0;  // the group's rows are its tokens onwards
-            it.kvh = kvh;
-            it.row0 = t * kMmaRows;
-            it.nrows = min(kMmaRows, pg.rows - it.row0);
-            it.kb = c * per_keys;
-            it.ke = min(pg.pre_tiles * kMmaTileKeys, (c + 1) * per_keys);
-            it.part = pre_part_base + pg.part_off + (kvh * pg.npre + c) * pg.rows + it.row0;
-            it.grp = -1;  // merged by the decode kernel, with the members' own keys
-            p.mma_items[idx++] = it;
-          }
+      const int c = k % pg.npre, t = (k / pg.npre) % rt, kvh = k / (pg.npre * rt);
+      WorkItem it;
+      it.seq = pg.s0;  // the group's rows are its tokens onwards
+      it.kvh = kvh;
+      it.row0 = t * kMmaRows;
+      it.nrows = min(kMmaRows, pg.rows - it.row0);
+      it.kb = c * per_keys;
+      it.ke = min(pg.pre_tiles * kMmaTileKeys, (c + 1) * per_keys);
+      it.part = pre_part_base + pg.part_off + (kvh * pg.npre + c) * pg.rows + it.row0;
+      it.grp = -1;  // merged by the decode kernel, with the members' own keys
+      p.mma_items[nm + pg.item_off + k] = it;
+    };
+    if (ng <= 64) {  // few groups: all threads share out each group's items
+      for (int g = 0; g < ng; ++g) {
+        const PreGroup pg = p.pre_groups[g];
+        if (!pg.valid) continue;
+        const int n = p.Hkv * ((pg.rows + kMmaRows - 1) / kMmaRows) * pg.npre;
+        for (int k = tid; k < n; k += kThreads) emit(pg, k);
+      }
+    } else {
+      for (int g = tid; g < ng; g += kThreads) {
+        const PreGroup pg = p.pre_groups[g];
+        if (!pg.valid) continue;
+        const int n = p.Hkv * ((pg.rows + kMmaRows - 1) / kMmaRows) * pg.npre;
+        for (int k = 0; k < n; ++k) emit(pg, k);
+      }
     }
   }
   if (tid == 0) {
