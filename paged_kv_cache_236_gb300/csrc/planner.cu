@@ -302,8 +302,8 @@ __device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre)
     if (s == B - 1 || equal_tiles(s + 1) == 0) p.pre_groups[g].s1 = s;
   }
   __syncthreads();
-  // (e) size the prefix work: about target_mma items in all, and at most half
-  // the partial rows of the workspace, or none at all
+  // (e) size the prefix work: about one item per SM (target_mma / 2) in all,
+  // and at most half the partial rows of the workspace, or none at all
   const int gper = (ng + kThreads - 1) / kThreads;
   const int g0 = min(ng, tid * gper), g1 = min(ng, g0 + gper);
   int rtiles = 0, rows = 0;
@@ -318,7 +318,8 @@ __device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre)
     int v[2] = {rtiles, rows}, tot[2];
     block_scan<2>(v, tot);
     if (tid == 0) {
-      int npre = tot[0] > 0 ? (p.target_mma + tot[0] - 1) / tot[0] : 0;
+      // about one wave: the prefix items run before any decode item starts
+      int npre = tot[0] > 0 ? max(1, (p.target_mma / 2) / tot[0]) : 0;
       npre = min(npre, kMaxPreTiles);
       while (npre > 0 && (int64_t)tot[1] * npre > p.part_cap / 2) --npre;
       sh_npre = npre;
