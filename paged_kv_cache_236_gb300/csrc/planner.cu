@@ -375,10 +375,13 @@ __device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre)
 
 __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   // The attention kernel may start its prologue while this plans (it waits
-  // for this grid).  This grid waits for its own predecessor before reading
-  // the metadata, which that predecessor may have produced.
+  // for this grid).  This grid may start while its predecessor runs: the
+  // only predecessor that lets it (paged_kv_write) writes neither the
+  // metadata read here nor anything written here, so the plan is computed
+  // at once and the wait for the predecessor comes before the first write
+  // that later kernels read (which also makes this grid's completion imply
+  // the predecessor's, as the attention kernels need).
   pdl_launch_dependents();
-  pdl_wait();
   extern __shared__ int seq_off[];  // [B + 1]: first unit of each sequence (per kv head)
   const int tid = threadIdx.x;
   const int B = p.B;
@@ -389,18 +392,11 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   __syncthreads();
   if (p.cascade) plan_prefix_groups(p, sh_pre);
 
-  // ---- units per sequence; zero the rows of invalid sequences
+  // ---- units per sequence (invalid sequences: none; their rows are zeroed below)
+  bool any_invalid = false;
   for (int s = tid; s < B; s += kThreads) {
     const SeqDesc d = describe(p, s);
-    if (!d.valid) {
-      raise_error(p.err, PKV_DEVERR_BAD_SEQUENCE);
-      const int a = p.query_start_loc[s], b = p.query_start_loc[s + 1];
-      if (a >= 0 && b > a && (int64_t)b <= p.T) {  // zero the rows that are addressable
-        int4* o = reinterpret_cast<int4*>(static_cast<uint8_t*>(p.out) + (int64_t)a * p.out_row_bytes);
-        const int64_t n16 = (int64_t)(b - a) * p.out_row_bytes / 16;
-        for (int64_t i = 0; i < n16; ++i) o[i] = make_int4(0, 0, 0, 0);
-      }
-    }
+    any_invalid |= !d.valid;
     seq_off[s] = d.units;  // 0 for an invalid sequence
   }
   __syncthreads();
@@ -528,12 +524,27 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
     if (sh_state) break;
   }
   if (sh_state == 2) {  // cannot happen with capacities from workspace_layout; emit nothing
+    pdl_wait();
     if (tid == 0) {
       p.header->n_dec = 0;
       p.header->n_mma = 0;
       p.header->n_merge = 0;
     }
     return;
+  }
+
+  pdl_wait();
+  if (any_invalid) {  // zero the addressable rows of this thread's invalid sequences
+    for (int s = tid; s < B; s += kThreads) {
+      if (describe_base(p, s).valid) continue;
+      raise_error(p.err, PKV_DEVERR_BAD_SEQUENCE);
+      const int a = p.query_start_loc[s], b = p.query_start_loc[s + 1];
+      if (a >= 0 && b > a && (int64_t)b <= p.T) {
+        int4* o = reinterpret_cast<int4*>(static_cast<uint8_t*>(p.out) + (int64_t)a * p.out_row_bytes);
+        const int64_t n16 = (int64_t)(b - a) * p.out_row_bytes / 16;
+        for (int64_t i = 0; i < n16; ++i) o[i] = make_int4(0, 0, 0, 0);
+      }
+    }
   }
 
   // ---- emit: class k's items start after all larger classes' (largest first)
