@@ -479,10 +479,13 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           for (int cc = 0; cc < 64; ++cc)
             if (cc >= nvis) sraw[cc] = __float_as_uint(-CUDART_INF_F);
         }
+        // this half's max (raw S): four chains of three-operand max, two values a step
         float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-        for (int cc = 0; cc < 64; ++cc) m4[cc & 3] = fmaxf(m4[cc & 3], __uint_as_float(sraw[cc]));
-        const float mloc = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));  // this half's max (raw S)
+        for (int cc = 0; cc < 64; cc += 2)
+          m4[(cc >> 1) & 3] =
+              fmax3(m4[(cc >> 1) & 3], __uint_as_float(sraw[cc]), __uint_as_float(sraw[cc + 1]));
+        const float mloc = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
         float* redm = red + sb * 256;
         redm[h * 128 + r] = mloc;
         // P of keys 64h .. 64h+63: 2^(S scale_log2 - m) packed to bf16 pairs

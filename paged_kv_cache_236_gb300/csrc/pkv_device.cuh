@@ -166,6 +166,13 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// max(a, b, c) in one instruction (three-operand max.f32, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^x with the hardware approximation (ex2.approx.ftz: relative error about
 // 2^-22; 2^-inf = 0), for softmax weights that are rounded to bf16 or
 // accumulated in fp32 afterwards.
