@@ -397,10 +397,12 @@ def run_reference(args):
 # whose hash is recorded; reported as null once those sources change.  The
 # captures and their commands are summarised under profiles/.
 NCU_TRAFFIC = {
-    "sources": "da02570d76831f93",
-    "decode": 612998656 + 5149440,       # dectc_kernel<4>, decode batch
-    "prefill": 81453824 + 10598400,      # mma_attn_kernel, prefill chunks
-    "specverify": 1076825856 + 13650688,  # mma_attn_kernel, spec-verify
+    "sources": "11604b01737b96fe",
+    "decode": 613085952 + 5081088,         # dectc_kernel<4>, decode batch
+    "prefill": 81171456 + 9745664,         # mma_attn_kernel, prefill chunks
+    "specverify": 1076737536 + 13646080,   # mma_attn_kernel, spec-verify
+    "prefix": 10557610 + 648700544 + 1399168,  # mma_attn_kernel (prefix items) + dectc_kernel<4>
+    "prefix-long": 2116698368 + 4174336,   # dectc_kernel<4>, long-context prefix-shared
 }
 
 
