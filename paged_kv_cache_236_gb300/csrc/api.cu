@@ -343,6 +343,12 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   pp.causal = causal ? 1 : 0;
   pp.mma_ok = mma_launch ? 1 : 0;
   pp.cascade = cascade ? 1 : 0;
+  // The decode kernel runs beside the tensor-core kernel, on the SMs the plan
+  // leaves it, unless it must read prefix partials that kernel writes.
+  const bool side_by_side = mma_launch && dectc && !cascade;
+  pp.side_by_side = side_by_side ? 1 : 0;
+  pp.sms = dev->sms;
+  pp.kv_key_bytes = 2 * D * elem_bytes(dtype);
   pp.block_tables = block_tables;
   pp.dec_rows_max = dec_rows_max;
   pp.dec_unit_rows = dectc ? tc_rows : kDecRows;
@@ -427,6 +433,7 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   }
   ap.counter = &header->dec_counter;
   ap.items = dec_items;
+  ap.no_wait = side_by_side ? 1 : 0;
   if (dectc) {
     CUtensorMap qmap16, kmap_sw, vmap_sw;
     if ((st = encode_q_map(&qmap16, q, T, Hq, D, 64, G, kTcDecRows / G)) != PKV_OK) return st;

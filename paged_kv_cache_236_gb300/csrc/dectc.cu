@@ -106,6 +106,18 @@ struct alignas(16) EpSlot {
 static_assert(sizeof(EpSlot) == 256, "epilogue slot");
 static_assert(sizeof(Bars) == kNumBars * 8, "barrier block");
 
+// A merge group as the planner wrote it, read from L2 (see no_wait).
+__device__ __forceinline__ MergeGroup load_group(const MergeGroup* g) {
+  static_assert(sizeof(MergeGroup) == 48, "merge group");
+  const int4* src = reinterpret_cast<const int4*>(g);
+  const int4 a = __ldcg(src), b = __ldcg(src + 1), c = __ldcg(src + 2);
+  MergeGroup m;
+  m.seq = a.x; m.kvh = a.y; m.row0 = a.z; m.nrows = a.w;
+  m.nsplit = b.x; m.part_base = b.y; m.pre_base = b.z; m.pre_n = b.w;
+  m.pre_stride = c.x; m.pad0 = c.y; m.pad1 = c.z; m.pad2 = c.w;
+  return m;
+}
+
 // All 128 softmax threads (warps 2-5) wait for the same phase; exit together.
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* err) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
@@ -198,8 +210,12 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  pdl_wait();  // the plan and the K/V write are complete and visible from here on
-  const int n_items = p.header->n_dec;
+  // The plan and the K/V write are complete and visible from here on: after
+  // the wait for the preceding grid, or, beside the tensor-core kernel, from
+  // launch (that kernel lets this one start only after seeing the plan); the
+  // plan is then read from L2 (__ldcg), past any stale L1 line.
+  if (!p.no_wait) pdl_wait();
+  const int n_items = __ldcg(&p.header->n_dec);
   const uint32_t tmem = *tmem_slot;
   const uint32_t smem_base = smem_u32(smem);
 
@@ -330,7 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
         mbar_arrive(&bars->islot_full[qb]);  // every lane: count 32
         break;
       }
-      const WorkItem it = p.items[idx];
+      WorkItem it;
+      {
+        const int4* src = reinterpret_cast<const int4*>(p.items + idx);
+        const int4 a = __ldcg(src), b = __ldcg(src + 1);
+        it.seq = a.x; it.kvh = a.y; it.row0 = a.z; it.nrows = a.w;
+        it.kb = b.x; it.ke = b.y; it.part = b.z; it.grp = b.w;
+      }
       const int L = p.context_lens[it.seq];
       const int qstart = p.query_start_loc[it.seq];
       const int n = p.query_start_loc[it.seq + 1] - qstart;
@@ -590,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
           // started) are folded in: m = max, weights 2^(m_p - m).
           int pre_base = 0, pre_n = 0, pre_stride = 0;
           if (mt.grp >= 0) {
-            const MergeGroup gr = p.groups[mt.grp];
+            const MergeGroup gr = load_group(p.groups + mt.grp);
             pre_base = gr.pre_base;
             pre_n = gr.pre_n;
             pre_stride = gr.pre_stride;
@@ -641,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
           *flag_last = atomicAdd(p.tickets + mt.grp, 1);
         }
         named_barrier(2, 128);
-        const MergeGroup gr = p.groups[mt.grp];
+        const MergeGroup gr = load_group(p.groups + mt.grp);
         if (*flag_last == gr.nsplit - 1) {
           if (d == 0) __threadfence();
           named_barrier(2, 128);

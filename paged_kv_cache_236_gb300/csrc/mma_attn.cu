@@ -201,6 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
   tc_fence_after();
   pdl_wait();  // the plan and the K/V write are complete and visible from here on
   const int n_items = p.header->n_mma;
+  // CTAs past the plan's mma_ctas leave their SMs to the decode kernel, which
+  // may start once every CTA here has seen the plan (signalled just below)
+  const bool active = blockIdx.x < p.header->mma_ctas;
+  pdl_launch_dependents();
   const uint32_t tmem = *tmem_slot;
   const uint32_t smem_base = smem_u32(smem);
 
@@ -225,7 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
 
   // The branches below are per warpgroup first (the register split is a
   // warpgroup-wide instruction), then per warp.
-  if (warp < 4 || warp >= 12) {
+  if (!active) {
+    // nothing: straight to the teardown
+  } else if (warp < 4 || warp >= 12) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLight));
     if (warp == 14) {
       // ================================================================ item fetch, Q, output stores

@@ -41,7 +41,8 @@ struct alignas(16) PlanHeader {
   int merge_counter;
   int n_pre;        // of the tensor-core items, those over shared prefixes (the last n_pre)
   int n_groups;     // prefix groups read once
-  int pad[5];
+  int mma_ctas;     // CTAs of the tensor-core kernel that take items (the rest leave their SMs to decode)
+  int pad[4];
 };
 
 // One unit of attention work: `nrows` rows of sequence `seq`, kv head `kvh`,
@@ -99,6 +100,9 @@ struct PlanParams {
   int dec_tile_keys;  // key tile of the decode-shaped kernel (splits are multiples)
   int target_dec, target_mma;  // desired item counts
   int dec_ctas;     // CTAs of the decode-shaped kernel (one wave of items)
+  int sms;          // SMs of the device (CTAs of the tensor-core kernel)
+  int side_by_side;  // the decode kernel may run beside the tensor-core kernel (no prefix items)
+  int kv_key_bytes;  // K+V bytes per key of one kv head (2 * head_dim * element size)
   int min_chunk_dec, min_chunk_mma;
   int dec_cap, mma_cap, merge_cap, part_cap;
   PlanHeader* header;
@@ -134,6 +138,11 @@ struct AttnParams {
   float scale_log2;  // scale * log2(e)
   int causal;
   int out_al32;      // out is 32-byte aligned (256-bit stores)
+  // The decode kernel launches beside the tensor-core kernel, after every
+  // CTA of that kernel has seen the plan complete (they signal dependents
+  // only then): it skips the grid-dependency wait, which would also wait for
+  // the tensor-core kernel, and reads the plan from L2.
+  int no_wait;
   int* err;
 };
 

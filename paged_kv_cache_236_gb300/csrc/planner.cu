@@ -425,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   // ---- total keys per path, for the chunk sizes
   __shared__ unsigned long long sh_wsum[kWarps][2];
   __shared__ int sh_chunk[2];
+  __shared__ int sh_mma_ctas;
   __shared__ int sh_state;
   unsigned long long w_dec = 0, w_mma = 0;
   {
@@ -450,8 +451,38 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       wd += sh_wsum[w][0];
       wm += sh_wsum[w][1];
     }
-    unsigned long long cd = (wd + p.target_dec - 1) / (unsigned long long)max(1, p.target_dec);
-    unsigned long long cm = (wm + p.target_mma - 1) / (unsigned long long)max(1, p.target_mma);
+    // Side by side: the tensor-core items (compute-bound) on mma_ctas SMs,
+    // the decode items (HBM-bound) on the rest, both at once, the split
+    // balancing a time model measured on this GPU: ~10 ns per (128-row unit,
+    // key) on one SM for the former (x1.15 for its coarse items' tail); for
+    // the latter the K+V bytes at 6.5 TB/s in all, at most 60 GB/s per SM.
+    int mma_ctas = p.sms;
+    if (p.side_by_side && wd > 0 && wm > 0) {
+      const float tm1 = (float)wm * 1.0e-2f * 1.15f;  // µs on one SM
+      const float db = (float)wd * (float)p.kv_key_bytes;
+      const float btot = 6.5e6f, bsm = 6.0e4f;  // bytes per µs
+      auto dec_us = [&](int n) { return db / fminf(btot, (float)n * bsm); };
+      auto total = [&](int k) { return fmaxf(tm1 / (float)k, dec_us(p.sms - k)); };
+      float best = tm1 / (float)p.sms + dec_us(p.sms);  // one after the other
+      // the optimum balances the two sides: where the decode side is
+      // HBM-bound (k1) or bound by its SMs (k2); try the integers around both
+      const int k1 = (int)ceilf(tm1 * btot / db);
+      const int k2 = (int)(tm1 * (float)p.sms * bsm / (db + tm1 * bsm));
+      const int cand[5] = {k1 - 1, k1, k2, k2 + 1, k2 + 2};
+      for (int c = 0; c < 5; ++c) {
+        const int k = min(max(cand[c], 1), p.sms - 1);
+        const float t = total(k);
+        if (t < best) {
+          best = t;
+          mma_ctas = k;
+        }
+      }
+    }
+    sh_mma_ctas = mma_ctas;
+    const int tgt_dec = mma_ctas < p.sms ? max(1, p.target_dec * (p.sms - mma_ctas) / p.sms) : p.target_dec;
+    const int tgt_mma = max(1, p.target_mma * mma_ctas / max(1, p.sms));
+    unsigned long long cd = (wd + tgt_dec - 1) / (unsigned long long)tgt_dec;
+    unsigned long long cm = (wm + tgt_mma - 1) / (unsigned long long)tgt_mma;
     cd = max(cd, (unsigned long long)p.min_chunk_dec);
     cm = max(cm, (unsigned long long)p.min_chunk_mma);
     cd = (cd + p.dec_tile_keys - 1) / p.dec_tile_keys * p.dec_tile_keys;
@@ -503,7 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       // split) and leave a last wave less than half full, grow the chunk so
       // that the count drops to whole waves.  Items of mixed sizes are left
       // to the largest-first order.
-      const int P = max(1, p.dec_ctas), extra = nd % P;
+      const int P = max(1, sh_mma_ctas < p.sms ? p.dec_ctas * (p.sms - sh_mma_ctas) / p.sms : p.dec_ctas);
+      const int extra = nd % P;
       if (fits && iter == 0 && nd > P && extra > 0 && 2 * extra <= P && 4 * tot[0] >= 3 * nd) {
         const long long grown = ((long long)cd * nd + (nd - extra) - 1) / (nd - extra);
         sh_chunk[0] = (int)min((grown + p.dec_tile_keys - 1) / p.dec_tile_keys * p.dec_tile_keys, (long long)(1 << 30));
@@ -528,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
     if (tid == 0) {
       p.header->n_dec = 0;
       p.header->n_mma = 0;
+      p.header->mma_ctas = p.sms;
       p.header->n_merge = 0;
     }
     return;
@@ -678,6 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
     p.header->dec_counter = 0;
     p.header->mma_counter = 0;
     p.header->merge_counter = 0;
+    p.header->mma_ctas = sh_mma_ctas;
   }
 }
 
