@@ -382,6 +382,7 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   pp.out = out;
   pp.out_row_bytes = Hq * D * elem_bytes(dtype);
   pp.err = dev->err;
+  if (cascade && (e = launch_prefix_search(pp, s)) != cudaSuccess) return cuda_fail(e, "prefix search launch");
   if ((e = launch_planner(pp, s)) != cudaSuccess) return cuda_fail(e, "planner launch");
 
   CUtensorMap kmap, vmap;

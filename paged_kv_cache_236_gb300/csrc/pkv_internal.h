@@ -170,6 +170,8 @@ cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slots, 
                             int64_t T, int64_t num_slots, int row_elems, int elem_bytes,
                             int64_t k_stride, int64_t v_stride, int* err, cudaStream_t s);
 cudaError_t launch_planner(const PlanParams& p, cudaStream_t s);
+// shared-prefix search for the planner (before it, on the same stream)
+cudaError_t launch_prefix_search(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_mma(const AttnParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,

@@ -179,7 +179,61 @@ __device__ __forceinline__ void iter_next(UnitIter& t, const PlanParams& p, cons
   t.d = describe(p, s);
 }
 
-// Finds the runs of sequences sharing a prefix and sizes their prefix work:
+constexpr int kSearchWarps = 8;  // sequences per CTA of the prefix search
+
+// Shared-prefix search, one warp per sequence s: seq_pre[s] = whole 128-key
+// tiles every query of s sees (decode-shaped sequences only, at most
+// kMaxPreTiles), and seq_mask[s] = how many leading blocks of s equal those of
+// s-1 within both sequences' visible tiles.  The warp compares the two rows
+// 32 blocks at a time, all loads in flight together, and takes the first
+// difference with a ballot.  Many CTAs, so the rows of all sequences are read
+// in about one round trip; it reads only the caller's metadata.
+__global__ void __launch_bounds__(kSearchWarps * 32) prefix_search_kernel(PlanParams p) {
+  pdl_launch_dependents();  // the planner may start; it waits for this grid before reading its results
+  const int lane = threadIdx.x & 31;
+  const int s = blockIdx.x * kSearchWarps + (threadIdx.x >> 5);
+  if (s < p.B) {
+    const int bpt = kMmaTileKeys / p.bs;
+    auto vis_tiles = [&](int q) {
+      const SeqDesc d = describe_base(p, q);
+      return (d.valid && !d.mma && d.n > 0) ? min(kMaxPreTiles, (d.L - d.n) / kMmaTileKeys) : 0;
+    };
+    const int v = vis_tiles(s);
+    const int vp = s >= 1 ? vis_tiles(s - 1) : 0;
+    const int lim = min(v, vp) * bpt;  // blocks to compare
+    int eq = 0;
+    if (lim > 0) {
+      const int32_t* prev = p.block_tables + (int64_t)(s - 1) * p.max_blocks;
+      const int32_t* cur = prev + p.max_blocks;
+      constexpr int kMaxChunks = (kMaxPreTiles * kMmaTileKeys / 8 + 31) / 32;  // block_size >= 8
+      int x[kMaxChunks], y[kMaxChunks];
+#pragma unroll
+      for (int c = 0; c < kMaxChunks; ++c) {
+        const int j = c * 32 + lane;
+        x[c] = j < lim ? __ldg(prev + j) : 0;
+        y[c] = j < lim ? __ldg(cur + j) : 0;
+      }
+      eq = lim;
+#pragma unroll
+      for (int c = kMaxChunks - 1; c >= 0; --c) {  // the lowest differing block wins
+        const unsigned m = __ballot_sync(0xffffffffu, x[c] != y[c]);
+        if (m) eq = c * 32 + __ffs(m) - 1;
+      }
+      eq = min(eq, lim);
+    }
+    if (lane == 0) {
+      p.seq_pre[s] = v;
+      p.seq_mask[s] = (uint32_t)eq;
+    }
+  }
+  // The planner waits for this grid, and the attention kernels for the
+  // planner; wait for the predecessor (the K/V write) so that the chain holds.
+  pdl_wait();
+}
+
+// From the leading blocks each sequence shares with its predecessor
+// (prefix_search_kernel), finds the runs of sequences sharing a prefix and
+// sizes their prefix work:
 // sh_pre = {prefix items, prefix partial rows, groups read once, groups}.
 // Leaves, per sequence s: seq_pre[s] (keys read by its group, 0 if none),
 // seq_grp[s] (first partial row of its rows in the group's prefix partials,
@@ -191,88 +245,9 @@ __device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre)
   const int bpt = kMmaTileKeys / p.bs;  // blocks per tile
   const int per = (B + kThreads - 1) / kThreads;
   const int a0 = min(B, tid * per), a1 = min(B, a0 + per);
-  int* eqb = reinterpret_cast<int*>(p.seq_mask);  // leading blocks equal to the predecessor's
-  // (a) whole tiles visible to every query of each decode-shaped sequence
-  for (int s = a0; s < a1; ++s) {
-    const SeqDesc d = describe_base(p, s);
-    p.seq_pre[s] = (d.valid && !d.mma && d.n > 0) ? min(kMaxPreTiles, (d.L - d.n) / kMmaTileKeys) : 0;
-  }
-  __syncthreads();
-  // (b) candidates: the first block equals the predecessor's.  Their equal
-  // leading blocks start at the shared limit and come down to the first
-  // differing block below; listed in seq_tmp as s | limit << 16.
-  int nc = 0;
-  for (int s = a0; s < a1; ++s) {
-    int lim = 0;
-    if (s >= 1 && p.seq_pre[s] > 0 && p.seq_pre[s - 1] > 0 &&
-        __ldg(p.block_tables + (int64_t)s * p.max_blocks) == __ldg(p.block_tables + (int64_t)(s - 1) * p.max_blocks))
-      lim = min(p.seq_pre[s], p.seq_pre[s - 1]) * bpt;
-    eqb[s] = lim;
-    nc += lim > 0;
-  }
-  {
-    int v[1] = {nc}, tot[1];
-    block_scan<1>(v, tot);  // also orders the writes above before the reads below
-    int o = v[0];
-    for (int s = a0; s < a1; ++s)
-      if (eqb[s] > 0) p.seq_tmp[o++] = s | eqb[s] << 16;
-    nc = tot[0];
-  }
-  __syncthreads();
-  // (c) compare the candidates' rows with their predecessors' in groups of
-  // four blocks: each thread a contiguous range of (candidate, group) pairs,
-  // eight per round with all their loads in flight together; the first
-  // differing block lowers eqb[s]
-  {
-    static_assert(kMaxPreTiles * (kMmaTileKeys / 8) < (1 << 15) && kMaxPlanSeqs <= (1 << 16), "packed candidates");
-    const int nq = (kMaxPreTiles * bpt + 3) / 4;
-    const bool vec = (p.max_blocks & 3) == 0 && (reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0;
-    const int nk = nc * nq, kper = (nk + kThreads - 1) / kThreads;
-    const int kb0 = min(nk, tid * kper), kb1 = min(nk, kb0 + kper);
-    for (int k0 = kb0; k0 < kb1; k0 += 8) {
-      int sq[8], b0q[8], limq[8];
-      int4 x[8], y[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int k = k0 + u;
-        sq[u] = -1;
-        b0q[u] = 0;
-        limq[u] = 0;
-        x[u] = y[u] = make_int4(0, 0, 0, 0);
-        if (k >= kb1) continue;
-        const int e = p.seq_tmp[k / nq], s = e & 0xffff, lim = e >> 16, b0 = (k % nq) * 4;
-        if (b0 >= lim) continue;
-        sq[u] = s;
-        b0q[u] = b0;
-        limq[u] = lim;
-        const int32_t* prev = p.block_tables + (int64_t)(s - 1) * p.max_blocks + b0;
-        const int32_t* cur = prev + p.max_blocks;
-        if (vec) {
-          x[u] = __ldg(reinterpret_cast<const int4*>(prev));
-          y[u] = __ldg(reinterpret_cast<const int4*>(cur));
-        } else {
-          const int m = min(4, lim - b0);
-          x[u].x = __ldg(prev);
-          y[u].x = __ldg(cur);
-          if (m > 1) { x[u].y = __ldg(prev + 1); y[u].y = __ldg(cur + 1); }
-          if (m > 2) { x[u].z = __ldg(prev + 2); y[u].z = __ldg(cur + 2); }
-          if (m > 3) { x[u].w = __ldg(prev + 3); y[u].w = __ldg(cur + 3); }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (sq[u] < 0) continue;
-        const int m = min(4, limq[u] - b0q[u]);
-        int j = m;  // first differing block of the group (m: none)
-        if (m > 3 && x[u].w != y[u].w) j = 3;
-        if (m > 2 && x[u].z != y[u].z) j = 2;
-        if (m > 1 && x[u].y != y[u].y) j = 1;
-        if (x[u].x != y[u].x) j = 0;
-        if (j < m) atomicMin(&eqb[sq[u]], b0q[u] + j);
-      }
-    }
-  }
-  __syncthreads();
+  // seq_pre[s]: whole tiles visible to every query of s; seq_mask[s]: leading
+  // blocks of s equal to its predecessor's (both from prefix_search_kernel)
+  const int* eqb = reinterpret_cast<const int*>(p.seq_mask);
   // (d) runs: a sequence with no leading tile equal to its predecessor's starts one
   auto equal_tiles = [&](int s) { return eqb[s] / bpt; };
   int ng = 0;
@@ -390,7 +365,10 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   __shared__ int sh_pre[4];  // prefix items, prefix partial rows, groups read once, groups
   if (tid == 0) sh_pre[0] = sh_pre[1] = sh_pre[2] = sh_pre[3] = 0;
   __syncthreads();
-  if (p.cascade) plan_prefix_groups(p, sh_pre);
+  if (p.cascade) {
+    pdl_wait();  // the shared-prefix search (the predecessor) is complete
+    plan_prefix_groups(p, sh_pre);
+  }
 
   // ---- units per sequence (invalid sequences: none; their rows are zeroed below)
   bool any_invalid = false;
@@ -716,6 +694,13 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
 }
 
 }  // namespace
+
+cudaError_t launch_prefix_search(const PlanParams& p, cudaStream_t s) {
+  if (p.B <= 0) return cudaSuccess;
+  const cudaError_t e = launch_pdl(prefix_search_kernel, dim3((p.B + kSearchWarps - 1) / kSearchWarps),
+                                   dim3(kSearchWarps * 32), 0, s, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 cudaError_t launch_planner(const PlanParams& p, cudaStream_t s) {
   const size_t smem = (size_t)(p.B + 1) * sizeof(int);
