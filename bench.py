@@ -397,12 +397,12 @@ def run_reference(args):
 # whose hash is recorded; reported as null once those sources change.  The
 # captures and their commands are summarised under profiles/.
 NCU_TRAFFIC = {
-    "sources": "11604b01737b96fe",
-    "decode": 613085952 + 5081088,         # dectc_kernel<4>, decode batch
-    "prefill": 81171456 + 9745664,         # mma_attn_kernel, prefill chunks
-    "specverify": 1076737536 + 13646080,   # mma_attn_kernel, spec-verify
-    "prefix": 10557610 + 648700544 + 1399168,  # mma_attn_kernel (prefix items) + dectc_kernel<4>
-    "prefix-long": 2116698368 + 4174336,   # dectc_kernel<4>, long-context prefix-shared
+    "sources": "3347f1dcc6847019",
+    "decode": 613111808 + 4718336,         # dectc_kernel<4>, decode batch
+    "prefill": 81036544 + 9203712,         # mma_attn_kernel, prefill chunks
+    "specverify": 1076745472 + 13745920,   # mma_attn_kernel, spec-verify
+    "prefix": 10558549 + 648700138 + 1369152,  # mma_attn_kernel (prefix items) + dectc_kernel<4>
+    "prefix-long": 2116707584 + 4223232,   # dectc_kernel<4>, long-context prefix-shared
 }
 
 
