@@ -6,6 +6,7 @@ inside a 128-key tile, suffixes long enough to be split, prefill chunks in
 the same batch, and paths that ignore the hint."""
 import numpy as np
 import pytest
+import torch
 
 import paged_kv_cache_236_gb300 as pkv
 import workloads as wl
@@ -83,4 +84,31 @@ def test_prefix_config_with_hint_sampled():
     B = w.step.num_seqs
     seqs = sorted({0, 1, 2, 3, B - 1} | set(g.choice(B, size=8, replace=False).tolist()))
     check_step(dw, out, seqs=seqs, what="prefix config, shared-prefix hint")
+    assert pkv.device_errors() == 0
+
+
+def test_many_short_runs():
+    # 600 sequences in runs of 5 on their own 256-token prefixes: more groups
+    # than the planner shares out cooperatively, one item list per group
+    g = np.random.Generator(np.random.PCG64(41))
+    B, run, tok = 600, 5, 256
+    groups = [(a, a + run - 1, tok) for a in range(0, B, run)]
+    n = np.ones(B, np.int64)
+    L = tok + n + g.integers(1, 300, size=B, endpoint=True)
+    nblk = int(np.sum((L + 15) // 16))
+    w = wl.build("many-runs", context_lens=L, q_lens=n, num_blocks=nblk + 64, block_size=16, num_q_heads=32,
+                 num_kv_heads=8, head_dim=128, dtype="bf16", seed=43, share_groups=groups, poison=True)
+    _check_both(w)
+
+
+def test_prefix_rows_beyond_a_small_workspace():
+    # with the smallest workspace the prefix partial rows may not fit: the call
+    # then reads every key per sequence (or fewer prefix chunks), same result
+    w = _runs_case(233)
+    st = w.step
+    ws = torch.empty(pkv.workspace_min(st.num_seqs, st.num_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim),
+                     dtype=torch.uint8, device="cuda")
+    dw = DeviceWorkload(w)
+    out = dw.run_step(0, shared_prefix=True, workspace=ws)
+    check_step(dw, out, what="shared-prefix hint, minimum workspace")
     assert pkv.device_errors() == 0
