@@ -47,9 +47,9 @@ WORKLOAD_DESC = {
     "specverify": "speculative verify: 32 seqs x 5 query tokens on 8192-token contexts, 64q/8kv heads, head_dim "
                   "128, block_size 32, 10240-block pool, bf16",
     "prefix": "prefix-shared decode: 256 seqs sharing a 2048-token prefix (128 blocks) + private U[128,1024] "
-              "suffixes, 1 query token, 32q/8kv, head_dim 128, block_size 16, bf16",
+              "suffixes, 1 query token, 32q/8kv, head_dim 128, block_size 16, bf16; shared-prefix hint set",
     "prefix-long": "long-context prefix-shared decode: 4 seqs x 131072 tokens (2048 shared), 1 query token, "
-                   "32q/8kv, head_dim 128, block_size 16, bf16",
+                   "32q/8kv, head_dim 128, block_size 16, bf16; shared-prefix hint set",
 }
 
 
