@@ -39,6 +39,11 @@
 //             global reads.
 // Shared memory: 3 stages of K+V (192 KB), 2 Q tiles and 2 P tiles (4 KB
 // each).  TMEM: S^T double-buffered in columns [0,32), O^T in [32,48).
+//
+// An unsplit item after a shared prefix (part < 0, merge group >= 0) folds
+// the prefix's partial rows, written by the tensor-core kernel before this
+// one ran, into its own rows in the epilogue; a split one leaves that to its
+// group's merge, which folds in the splits and the prefix partials alike.
 #include <math_constants.h>
 
 #include "pkv_device.cuh"

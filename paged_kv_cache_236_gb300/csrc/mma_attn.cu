@@ -61,6 +61,16 @@
 // The running max used for the exponentials is only raised when a tile's row
 // maximum exceeds it by more than 8 (log2 units), so O is rescaled in TMEM
 // rarely; P stays <= 2^8 and the result is exact up to rounding.
+//
+// Beside the decode kernel: every CTA signals its dependent (the decode
+// kernel of the same call) as soon as it has seen the plan, and CTAs at or
+// past the plan's mma_ctas take no items, so that the decode kernel's CTAs
+// take their SMs and both kernels run at once on disjoint SMs.
+//
+// Shared-prefix items: an item whose rows are those of a run of sequences
+// sharing leading blocks (their tokens are contiguous in q, from the run's
+// first sequence) over keys of that prefix.  It writes partial rows and no
+// merge; the decode kernel folds them into each member's rows.
 #include <math_constants.h>
 
 #include "pkv_device.cuh"
