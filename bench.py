@@ -276,10 +276,25 @@ def run_gpu(args, rank, world, local_rank):
     st = w.step
     pin = lambda a: (torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
                      if a.dtype == np.uint16 else torch.from_numpy(np.ascontiguousarray(a))).pin_memory()
-    host_in = dict(q=pin(st.q), k=pin(st.k_new), v=pin(st.v_new), slots=pin(st.slot_mapping),
-                   bt=pin(st.block_tables), ctx=pin(st.context_lens), qsl=pin(st.query_start_loc))
+    host_parts = dict(q=pin(st.q), k=pin(st.k_new), v=pin(st.v_new), slots=pin(st.slot_mapping),
+                      bt=pin(st.block_tables), ctx=pin(st.context_lens), qsl=pin(st.query_start_loc))
+    # As a serving loop would: the step's inputs staged in one pinned buffer
+    # (each part 256-byte aligned), sent with one host-to-device copy into a
+    # device buffer of the same layout, and read through views of it.
+    offs, nbytes = {}, 0
+    for k2, x in host_parts.items():
+        offs[k2] = nbytes
+        nbytes += (x.numel() * x.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d = {}
+    for k2, x in host_parts.items():
+        n = x.numel() * x.element_size()
+        host_buf[offs[k2]:offs[k2] + n].copy_(x.reshape(-1).view(torch.uint8))
+        d[k2] = dev_buf[offs[k2]:offs[k2] + n].view(x.dtype).view(x.shape)
     host_out = torch.empty(tuple(st.q.shape), dtype=t["q"].dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+    out_dev = torch.empty_like(t["q"])
+    h2d = nbytes
     d2h = host_out.numel() * host_out.element_size()
     ws = torch.empty(pkv.workspace_size(st.num_seqs, st.num_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim),
                      dtype=torch.uint8, device=dev)
@@ -288,10 +303,11 @@ def run_gpu(args, rank, world, local_rank):
         flush.fill_(1)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        d = {k2: x.to(dev, non_blocking=True) for k2, x in host_in.items()}
+        dev_buf.copy_(host_buf, non_blocking=True)
         pkv.paged_kv_write(d["k"], d["v"], d["slots"], t["kc"], t["vc"])
         o = pkv.paged_attention_forward(d["q"], t["kc"], t["vc"], d["bt"], d["ctx"], d["qsl"], w.scale, w.causal,
-                                        workspace=ws, max_query_len=t["mql"], shared_prefix=t["sp"])
+                                        out=out_dev, workspace=ws, max_query_len=t["mql"],
+                                        shared_prefix=t["sp"])
         host_out.copy_(o, non_blocking=True)
         b.record()
         b.synchronize()
