@@ -248,7 +248,7 @@ __device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre)
   // seq_pre[s]: whole tiles visible to every query of s; seq_mask[s]: leading
   // blocks of s equal to its predecessor's (both from prefix_search_kernel)
   const int* eqb = reinterpret_cast<const int*>(p.seq_mask);
-  // (d) runs: a sequence with no leading tile equal to its predecessor's starts one
+  // (a) runs: a sequence with no leading tile equal to its predecessor's starts one
   auto equal_tiles = [&](int s) { return eqb[s] / bpt; };
   int ng = 0;
   {
@@ -277,7 +277,7 @@ __device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre)
     if (s == B - 1 || equal_tiles(s + 1) == 0) p.pre_groups[g].s1 = s;
   }
   __syncthreads();
-  // (e) size the prefix work: about one item per SM (target_mma / 2) in all,
+  // (b) size the prefix work: about one item per SM (target_mma / 2) in all,
   // and at most half the partial rows of the workspace, or none at all
   const int gper = (ng + kThreads - 1) / kThreads;
   const int g0 = min(ng, tid * gper), g1 = min(ng, g0 + gper);
@@ -337,7 +337,7 @@ __device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre)
     }
   }
   __syncthreads();
-  // (f) each member's suffix starts after its group's prefix; where its rows'
+  // (c) each member's suffix starts after its group's prefix; where its rows'
   // prefix partials are
   for (int s = a0; s < a1; ++s) {
     const PreGroup pg = p.pre_groups[p.seq_grp[s]];
