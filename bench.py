@@ -102,10 +102,17 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def launches_per_step(w, max_q_len: int) -> int:
-    """Our kernels per step: write, planner, [tensor-core kernel], CUDA-core kernel, merge."""
+def launches_per_step(w, max_q_len: int, shared_prefix: bool) -> int:
+    """Our kernels per step, as paged_attention_forward chooses them: the K/V
+    write, [the shared-prefix search], the planner, [the tensor-core kernel],
+    the decode-shaped kernel (split merges run inside the attention kernels)."""
     g = w.num_q_heads // w.num_kv_heads
-    return 4 + (1 if max_q_len * g > 4 else 0)
+    tc = w.dtype == "bf16" and w.head_dim == 128 and g & (g - 1) == 0
+    dectc = tc and g <= 16
+    dec_rows = 16 if dectc else 4
+    cascade = shared_prefix and dectc
+    mma = tc and (cascade or not (max_q_len > 0 and max_q_len * g <= dec_rows))
+    return 3 + int(cascade) + int(mma)
 
 
 class ClockSampler:
@@ -330,7 +337,7 @@ def run_gpu(args, rank, world, local_rank):
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_tot / args.steps, 5)},
-        "gpu_launches": launches_per_step(w, t["mql"]) * args.steps,
+        "gpu_launches": launches_per_step(w, t["mql"], t["sp"]) * args.steps,
         "clocks": clocks,
     }
 
@@ -347,7 +354,7 @@ def run_gpu(args, rank, world, local_rank):
             "bytes_per_step": algorithmic_bytes(wm)["step"],
             "hbm_frac": round(algorithmic_bytes(wm)["step"] / (avg * 1e-3) / 1e9 / hbm_peak, 4),
             "prefill_unmasked_tflop": round(fl / 1e12, 4)}
-        result["gpu_launches"] += launches_per_step(wm, tm["mql"]) * len(ms_m)
+        result["gpu_launches"] += launches_per_step(wm, tm["mql"], tm["sp"]) * len(ms_m)
         del tm
 
     if rank == 0 and not args.no_cpu_baseline:
