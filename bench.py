@@ -357,9 +357,46 @@ def run_gpu(args, rank, world, local_rank):
         result["gpu_launches"] += launches_per_step(wm, tm["mql"], tm["sp"]) * len(ms_m)
         del tm
 
+    if rank == 0:
+        result["block_manager"] = block_manager_timing(w, with_oracle=not args.no_cpu_baseline)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     return result
+
+
+def block_manager_timing(w, reps: int = 50, with_oracle: bool = True) -> dict:
+    """Host cost of one step's metadata through the library's C++ block
+    manager (slots, block tables, context lengths, query offsets,
+    copy-on-write pairs) for the workload's batch: each repetition allocates
+    the sequences to their cached lengths (untimed), then times the step that
+    appends every sequence's query tokens.  The reference model of the same
+    manager is timed beside it (the oracle side, fewer repetitions)."""
+    import paged_kv_cache_236_gb300 as pkv
+    st = w.step
+    B = st.num_seqs
+    n_new = np.diff(st.query_start_loc).astype(np.int32)
+    cached = (st.context_lens - n_new).astype(np.int32)
+    width = st.block_tables.shape[1]
+    ids = np.arange(B, dtype=np.int64)
+
+    def run(make, k):
+        tot = 0.0
+        for _ in range(k):
+            m = make(w.num_blocks, w.block_size, width)
+            m.step(ids, cached)
+            t0 = time.perf_counter()
+            m.step(ids, n_new)
+            tot += time.perf_counter() - t0
+        return tot / k * 1e6
+
+    out = {"value": round(run(pkv.BlockManager, reps), 2), "unit": "us per step (host)", "reps": reps,
+           "what": f"BlockManager.step for the workload's {B} sequences ({int(n_new.sum())} new tokens, "
+                   f"{width}-block tables), through the Python binding"}
+    if with_oracle:
+        from oracle.block_manager import BlockManagerModel
+        out["oracle_us_per_step"] = round(run(BlockManagerModel, 3), 2)
+        out["oracle_reps"] = 3
+    return out
 
 
 def cpu_baseline(w, budget_s: float = 15.0) -> dict:
@@ -453,12 +490,16 @@ def _code_only(text: str) -> str:
     return " ".join("".join(out).split())
 
 
+# The sources of the write and attention path: its kernels, their launches and
+# the plan.  The block manager and the block copy are not on it.
+FORWARD_SOURCES = ("api.cu", "decode.cu", "dectc.cu", "kv_write.cu", "mma_attn.cu", "planner.cu", "static_ws.cu",
+                   "pkv_device.cuh", "pkv_tc.cuh", "pkv_internal.h")
+
+
 def _kernel_sources_hash() -> str:
-    import glob
     import hashlib
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_kv_cache_236_gb300", "csrc")
-    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
-                   glob.glob(os.path.join(csrc, "*.h")))
+    files = sorted(os.path.join(csrc, f) for f in FORWARD_SOURCES)
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.basename(f).encode())

@@ -65,7 +65,8 @@ typedef enum {
   PKV_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or shape */
   PKV_ERR_UNSUPPORTED = 2,  /* valid but not implemented (dtype, head_dim, block_size, GPU) */
   PKV_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a launch failed */
-  PKV_ERR_WORKSPACE = 4     /* workspace missing or smaller than required */
+  PKV_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required */
+  PKV_ERR_OUT_OF_BLOCKS = 5 /* block manager: free and evictable blocks do not cover the request */
 } pkv_status;
 
 typedef enum {

@@ -9,6 +9,8 @@ tensors are not on a CUDA device, the calls raise.
     paged_kv_write(k, v, slot_mapping, k_cache, v_cache)
     paged_attention_forward(q, k_cache, v_cache, block_tables, context_lens,
                             query_start_loc, scale, causal)
+    BlockManager(num_blocks, block_size, max_blocks_per_seq)   (host, C++)
+    copy_blocks(k_cache, v_cache, copies)                      (copy-on-write)
 
 Block pool per layer: ``[num_blocks, block_size, num_kv_heads, head_dim]``
 ("ADR 004: Paged Attention Serving Integration", Decision 4 - a per-layer
@@ -21,17 +23,19 @@ import ctypes
 import os
 import threading
 
+import numpy as np
 import torch
 
 __all__ = [
     "paged_kv_write", "paged_attention_forward", "workspace_size", "workspace_min",
     "device_errors", "set_profile_events", "profile_elapsed_ms", "lib", "LibraryError", "DEVERR",
+    "BlockManager", "OutOfBlocks", "copy_blocks",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpaged_kv.so")
 
-PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_WORKSPACE = range(5)
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_WORKSPACE, PKV_ERR_OUT_OF_BLOCKS = range(6)
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
 HINT_SHARED_PREFIX = 0x1  # PKV_HINT_SHARED_PREFIX
 DEVERR = {
@@ -50,6 +54,11 @@ class LibraryError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"paged_kv status {status}: {message}")
         self.status = status
+
+
+class OutOfBlocks(LibraryError):
+    """The block manager's free and evictable blocks do not cover a request
+    (``PKV_ERR_OUT_OF_BLOCKS``); the manager is unchanged."""
 
 
 _lib = None
@@ -91,13 +100,31 @@ def lib() -> ctypes.CDLL:
             L.pkv_event_elapsed_ms.argtypes = [c_vp, c_vp, ctypes.POINTER(c_f)]
             L.pkv_version.restype = ctypes.c_char_p
             L.pkv_version.argtypes = []
+            c_p32 = ctypes.POINTER(c_i32)
+            for name, args in (
+                    ("pkv_bm_create", [c_i32, c_i32, c_i32, ctypes.POINTER(c_vp)]),
+                    ("pkv_bm_update", [c_vp, c_i64, c_i32, c_vp, c_p32, c_p32]),
+                    ("pkv_bm_step", [c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_p32]),
+                    ("pkv_bm_free", [c_vp, c_i64]),
+                    ("pkv_bm_fork", [c_vp, c_i64, c_i64]),
+                    ("pkv_bm_add_prefix", [c_vp, c_i64, c_vp, c_i32]),
+                    ("pkv_bm_try_get_prefix_blocks", [c_vp, c_i64, c_vp, c_i32, c_p32]),
+                    ("pkv_bm_block_table", [c_vp, c_i64, c_vp, c_p32, c_p32]),
+                    ("pkv_bm_stats", [c_vp, c_p32, c_p32, c_p32, c_p32]),
+                    ("paged_kv_copy_blocks", [c_vp, c_vp, c_vp, c_i32, c_i32, c_i64, c_i64, c_i32, c_i32, c_i32,
+                                              c_i32, c_vp])):
+                getattr(L, name).restype = c_i32
+                getattr(L, name).argtypes = args
+            L.pkv_bm_destroy.restype = None
+            L.pkv_bm_destroy.argtypes = [c_vp]
             _lib = L
     return _lib
 
 
 def _check(status: int) -> None:
     if status != PKV_OK:
-        raise LibraryError(status, lib().pkv_last_error().decode(errors="replace"))
+        msg = lib().pkv_last_error().decode(errors="replace")
+        raise (OutOfBlocks if status == PKV_ERR_OUT_OF_BLOCKS else LibraryError)(status, msg)
 
 
 def _stream(device: torch.device) -> int:
@@ -234,3 +261,128 @@ def device_errors(clear: bool = True) -> int:
     flags = c_i32(0)
     _check(lib().pkv_device_errors(ctypes.byref(flags), 1 if clear else 0))
     return int(flags.value)
+
+
+# ----------------------------------------------------------------------------
+# host block manager (include/paged_kv_blocks.h)
+# ----------------------------------------------------------------------------
+
+def _host(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=dtype))
+
+
+class BlockManager:
+    """The library's host block manager: block ids, slots and tables for a
+    pool of ``num_blocks`` blocks of ``block_size`` tokens ("Paged Attention
+    基础", section 3.1 C; "ADR 004", Decision 5 and Consequences).
+
+    ``update(seq, n)`` -> (slots int64 [n], copies int32 [c, 2]);
+    ``step(seq_ids, n_new)`` -> dict of the call metadata (host numpy
+    arrays: slot_mapping, block_tables, context_lens, query_start_loc,
+    copies); ``free``, ``fork``, ``add_prefix``, ``try_get_prefix_blocks``,
+    ``block_table``, ``stats``.  Refused requests raise ``OutOfBlocks`` or
+    ``LibraryError`` and change nothing.
+    """
+
+    def __init__(self, num_blocks: int, block_size: int, max_blocks_per_seq: int):
+        h = c_vp()
+        _check(lib().pkv_bm_create(num_blocks, block_size, max_blocks_per_seq, ctypes.byref(h)))
+        self._h = h
+        self.num_blocks, self.block_size, self.max_blocks = num_blocks, block_size, max_blocks_per_seq
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            lib().pkv_bm_destroy(h)
+            self._h = None
+
+    def update(self, seq: int, n: int):
+        slots = np.empty(max(n, 0), dtype=np.int64)
+        pair = (c_i32 * 2)()
+        nc = c_i32(0)
+        _check(lib().pkv_bm_update(self._h, int(seq), int(n), slots.ctypes.data if n > 0 else None, pair,
+                                   ctypes.byref(nc)))
+        return slots, np.asarray(list(pair)[:2 * nc.value], dtype=np.int32).reshape(-1, 2)
+
+    def step(self, seq_ids, n_new) -> dict:
+        ids = _host(seq_ids, np.int64)
+        n = _host(n_new, np.int32)
+        B = len(ids)
+        if len(n) != B:
+            raise ValueError("seq_ids and n_new differ in length")
+        total = int(n.astype(np.int64).sum()) if B else 0
+        out = {
+            "slot_mapping": np.empty(max(total, 0), dtype=np.int64),
+            "block_tables": np.empty((B, self.max_blocks), dtype=np.int32),
+            "context_lens": np.empty(B, dtype=np.int32),
+            "query_start_loc": np.empty(B + 1, dtype=np.int32),
+            "copies": np.empty((max(B, 1), 2), dtype=np.int32),
+        }
+        nc = c_i32(0)
+        ptr = lambda a: a.ctypes.data if a.size else None
+        _check(lib().pkv_bm_step(self._h, ptr(ids), ptr(n), B, ptr(out["slot_mapping"]), ptr(out["block_tables"]),
+                                 ptr(out["context_lens"]), out["query_start_loc"].ctypes.data,
+                                 out["copies"].ctypes.data, ctypes.byref(nc)))
+        out["copies"] = out["copies"][:nc.value]
+        return out
+
+    def free(self, seq: int) -> None:
+        _check(lib().pkv_bm_free(self._h, int(seq)))
+
+    def fork(self, parent: int, child: int) -> None:
+        _check(lib().pkv_bm_fork(self._h, int(parent), int(child)))
+
+    def add_prefix(self, seq: int, tokens) -> None:
+        t = _host(tokens, np.int64)
+        _check(lib().pkv_bm_add_prefix(self._h, int(seq), t.ctypes.data if t.size else None, len(t)))
+
+    def try_get_prefix_blocks(self, seq: int, tokens) -> int:
+        t = _host(tokens, np.int64)
+        got = c_i32(0)
+        _check(lib().pkv_bm_try_get_prefix_blocks(self._h, int(seq), t.ctypes.data if t.size else None, len(t),
+                                                  ctypes.byref(got)))
+        return int(got.value)
+
+    def block_table(self, seq: int) -> list:
+        table = np.empty(self.max_blocks, dtype=np.int32)
+        nb, nt = c_i32(0), c_i32(0)
+        _check(lib().pkv_bm_block_table(self._h, int(seq), table.ctypes.data, ctypes.byref(nb), ctypes.byref(nt)))
+        return table[:nb.value].tolist()
+
+    def num_tokens(self, seq: int) -> int:
+        nt = c_i32(0)
+        _check(lib().pkv_bm_block_table(self._h, int(seq), None, None, ctypes.byref(nt)))
+        return int(nt.value)
+
+    def stats(self) -> dict:
+        f, i, u, c = c_i32(0), c_i32(0), c_i32(0), c_i32(0)
+        _check(lib().pkv_bm_stats(self._h, ctypes.byref(f), ctypes.byref(i), ctypes.byref(u), ctypes.byref(c)))
+        return {"free": f.value, "idle": i.value, "in_use": u.value, "cached": c.value}
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, copies) -> None:
+    """Copy-on-write on the device pool: block ``dst`` of every layer's K and
+    V pool becomes a copy of block ``src`` for each host pair (src, dst) of
+    ``copies`` (int32 [n, 2], as ``BlockManager.update`` / ``step`` return).
+    Caches are ``[NB, bs, Hkv, D]`` or ``[layers, NB, bs, Hkv, D]`` (each
+    layer's pool contiguous).  Runs on the current stream."""
+    dev = _need_cuda(k_cache, v_cache)
+    pairs = _host(copies, np.int32).reshape(-1, 2)
+    if k_cache.dtype not in DTYPE or v_cache.dtype != k_cache.dtype or v_cache.shape != k_cache.shape or \
+            v_cache.stride() != k_cache.stride():
+        raise ValueError("k_cache and v_cache must share dtype (bfloat16 or float32), shape and strides")
+    if k_cache.dim() == 4:
+        layers, stride = 1, 0
+        pool = k_cache
+    elif k_cache.dim() == 5:
+        layers, stride = k_cache.shape[0], k_cache.stride(0)
+        pool = k_cache[0]
+    else:
+        raise ValueError("caches must be [NB, bs, Hkv, D] or [layers, NB, bs, Hkv, D]")
+    if not pool.is_contiguous():
+        raise ValueError("each layer's pool must be contiguous")
+    NB, bs, Hkv, D = pool.shape
+    with torch.cuda.device(dev):
+        _check(lib().paged_kv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(),
+                                          pairs.ctypes.data if len(pairs) else None, len(pairs), layers, stride,
+                                          NB, bs, Hkv, D, DTYPE[k_cache.dtype], _stream(dev)))

@@ -1,6 +1,7 @@
 """Build the C-ABI shared library ``libpaged_kv.so`` in-tree for sm_103a.
 
-Each ``csrc/*.cu`` translation unit is compiled in parallel with nvcc, then
+Each ``csrc/*.cu`` (device code) and ``csrc/*.cpp`` (host-only code, the
+block manager) translation unit is compiled in parallel with nvcc, then
 linked with ``nvcc -shared``.  Objects go to ``<repo>/_build/<machine>/``;
 the library lands next to this file.  A rebuild happens when the library is
 missing, older than a source, or was built on another machine type.
@@ -37,7 +38,7 @@ def nvcc() -> str:
 
 
 def sources() -> list[str]:
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _inputs() -> list[str]:
@@ -63,7 +64,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     cc = nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [cc, *ARCH_FLAGS, *NVCC_FLAGS, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

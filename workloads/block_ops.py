@@ -37,7 +37,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["op_stream", "kv_row", "kv_rows"]
+__all__ = ["op_stream", "kv_row", "kv_rows", "kv_rows_normal"]
 
 _P = (1 << 61) - 1
 
@@ -65,6 +65,17 @@ def kv_rows(tokens, width: int, salt: int = 0) -> np.ndarray:
     for p, t in enumerate(tokens):
         h = (h * 1099511628211 + int(t) + 7) % _P
         out[p] = _expand(h, width)
+    return out
+
+
+def kv_rows_normal(tokens, width: int, salt: int = 0) -> np.ndarray:
+    """Rows of N(0, 1) fp32 values, row p drawn from a generator seeded by the
+    hash of ``tokens[:p + 1]`` (and ``salt``: K and V use different ones)."""
+    h = 1469598103934665603
+    out = np.empty((len(tokens), width), dtype=np.float32)
+    for p, t in enumerate(tokens):
+        h = (h * 1099511628211 + int(t) + 7) % _P
+        out[p] = np.random.default_rng([h, salt]).standard_normal(width, dtype=np.float32)
     return out
 
 
