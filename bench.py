@@ -357,11 +357,45 @@ def run_gpu(args, rank, world, local_rank):
         result["gpu_launches"] += launches_per_step(wm, tm["mql"], tm["sp"]) * len(ms_m)
         del tm
 
+    # ---------------- copy-on-write block copy (HBM-bound) ----------------
+    if rank == 0:
+        result["copy_blocks"] = copy_blocks_timing(pkv, torch, dev, flush, hbm_peak, args.warmup)
+        result["gpu_launches"] += result["copy_blocks"]["launches"]
     if rank == 0:
         result["block_manager"] = block_manager_timing(w, with_oracle=not args.no_cpu_baseline)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     return result
+
+
+def copy_blocks_timing(pkv, torch, dev, flush, hbm_peak, warmup, reps: int = 10) -> dict:
+    """paged_kv_copy_blocks on 2048 (src, dst) pairs of a 4096-block bf16 pool
+    (block_size 16, 8 kv heads, head_dim 128: 32 KB per block and pool), one
+    layer: 2048 x 2 pools x 32 KB read and as much written (268 MB, above L2),
+    L2 flushed before each call; CUDA events on the current stream."""
+    nb, pairs_n = 4096, 2048
+    kc = torch.zeros((nb, 16, 8, 128), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    perm = np.random.default_rng(9).permutation(nb).astype(np.int32)
+    pairs = np.stack([perm[:pairs_n], perm[pairs_n:]], axis=1)
+    block_bytes = 16 * 8 * 128 * 2
+    moved = pairs_n * 2 * block_bytes * 2
+    ms = []
+    for i in range(warmup + reps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        pkv.copy_blocks(kc, vc, pairs)
+        b.record()
+        b.synchronize()
+        if i >= warmup:
+            ms.append(a.elapsed_time(b))
+    med = statistics.median(ms)
+    gbs = moved / (med * 1e-3) / 1e9
+    del kc, vc
+    return {"value": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "ms": round(med, 5),
+            "bytes": moved, "pairs": pairs_n, "launches": reps * -(-pairs_n // 480),
+            "what": "copy-on-write of 2048 blocks (K and V, 32 KB each), read + write bytes / median call time"}
 
 
 def block_manager_timing(w, reps: int = 50, with_oracle: bool = True) -> dict:
