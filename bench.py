@@ -394,7 +394,7 @@ def copy_blocks_timing(pkv, torch, dev, flush, hbm_peak, warmup, reps: int = 10)
     gbs = moved / (med * 1e-3) / 1e9
     del kc, vc
     return {"value": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "ms": round(med, 5),
-            "bytes": moved, "pairs": pairs_n, "launches": reps * -(-pairs_n // 480),
+            "bytes": moved, "pairs": pairs_n, "launches": reps * -(-pairs_n // 4000),
             "what": "copy-on-write of 2048 blocks (K and V, 32 KB each), read + write bytes / median call time"}
 
 
@@ -487,16 +487,16 @@ def run_reference(args):
 
 
 # DRAM bytes per launch of each workload's dominant kernel (dram__bytes_read.sum +
-# dram__bytes_write.sum) from one ncu capture, valid only for the kernel sources
-# whose hash is recorded; reported as null once those sources change.  The
-# captures and their commands are summarised under profiles/.
+# dram__bytes_write.sum) from one ncu capture, each valid only for the sources
+# whose hash is recorded with it (the shared launch path plus the kernels that
+# workload runs); reported as null once those sources change.  The captures
+# and their commands are summarised under profiles/.
 NCU_TRAFFIC = {
-    "sources": "e924c785b8c3e31b",  # kernel sources without comments (_code_only)
-    "decode": 613111808 + 4718336,         # dectc_kernel<4>, decode batch
-    "prefill": 81036544 + 9203712,         # mma_attn_kernel, prefill chunks
-    "specverify": 1076745472 + 13745920,   # mma_attn_kernel, spec-verify
-    "prefix": 10558549 + 648700138 + 1369152,  # mma_attn_kernel (prefix items) + dectc_kernel<4>
-    "prefix-long": 2116707584 + 4223232,   # dectc_kernel<4>, long-context prefix-shared
+    "decode": ("50f7603394c6a898", 613111808 + 4718336),        # dectc_kernel<4>, decode batch
+    "prefill": ("73b1c3cd24fdc664", 81036544 + 9203712),        # mma_attn_kernel, prefill chunks
+    "specverify": ("73b1c3cd24fdc664", 1076745472 + 13745920),  # mma_attn_kernel, spec-verify
+    "prefix": ("e924c785b8c3e31b", 10558549 + 648700138 + 1369152),  # mma_attn_kernel + dectc_kernel<4>
+    "prefix-long": ("50f7603394c6a898", 2116707584 + 4223232),  # dectc_kernel<4>, long-context prefix-shared
 }
 
 
@@ -524,16 +524,20 @@ def _code_only(text: str) -> str:
     return " ".join("".join(out).split())
 
 
-# The sources of the write and attention path: its kernels, their launches and
-# the plan.  The block manager and the block copy are not on it.
-FORWARD_SOURCES = ("api.cu", "decode.cu", "dectc.cu", "kv_write.cu", "mma_attn.cu", "planner.cu", "static_ws.cu",
-                   "pkv_device.cuh", "pkv_tc.cuh", "pkv_internal.h")
+# The sources of the write and attention path: the launch path and plan shared
+# by every workload, and the attention kernels each workload runs.  The block
+# manager and the block copy are not on it.
+FORWARD_SOURCES = ("api.cu", "kv_write.cu", "planner.cu", "static_ws.cu", "pkv_device.cuh", "pkv_tc.cuh",
+                   "pkv_internal.h")
+WORKLOAD_KERNELS = {"decode": ("decode.cu", "dectc.cu"), "prefix-long": ("decode.cu", "dectc.cu"),
+                    "prefill": ("mma_attn.cu",), "specverify": ("mma_attn.cu",),
+                    "prefix": ("decode.cu", "dectc.cu", "mma_attn.cu")}
 
 
-def _kernel_sources_hash() -> str:
+def _kernel_sources_hash(workload: str) -> str:
     import hashlib
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_kv_cache_236_gb300", "csrc")
-    files = sorted(os.path.join(csrc, f) for f in FORWARD_SOURCES)
+    files = sorted(os.path.join(csrc, f) for f in FORWARD_SOURCES + WORKLOAD_KERNELS[workload])
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.basename(f).encode())
@@ -543,9 +547,9 @@ def _kernel_sources_hash() -> str:
 
 
 def ncu_traffic(workload: str):
-    if workload not in NCU_TRAFFIC or _kernel_sources_hash() != NCU_TRAFFIC["sources"]:
+    if workload not in NCU_TRAFFIC or _kernel_sources_hash(workload) != NCU_TRAFFIC[workload][0]:
         return None
-    return NCU_TRAFFIC[workload]
+    return NCU_TRAFFIC[workload][1]
 
 
 def main():

@@ -172,7 +172,7 @@ pkv_status pkv_bm_stats(const pkv_block_manager* bm, int32_t* free_blocks, int32
  *                     num_kv_heads * head_dim, i.e. dense)
  *   copies            HOST int32 [num_copies, 2] (src, dst), as pkv_bm_update and
  *                     pkv_bm_step return them; read before the call returns (the
- *                     pairs travel in the launch parameters, 480 per launch)
+ *                     pairs travel in the launch parameters, 4000 per launch)
  * Checked on the host before any launch (PKV_ERR_INVALID_ARG): every id in
  * [0, num_blocks), no destination twice, no destination that is also a
  * source (the block manager never produces either).  Pool bases, the block's

@@ -25,7 +25,7 @@
 
 namespace {
 
-constexpr int kPairsPerLaunch = 480;  // parameters stay under 4 KB
+constexpr int kPairsPerLaunch = 4000;  // 32 000 bytes: parameters stay under the 32 764-byte limit
 constexpr int kMaxGrid = 1024;
 
 struct CopyList {
@@ -110,7 +110,7 @@ extern "C" pkv_status paged_kv_copy_blocks(void* k_cache, void* v_cache, const i
     if (dsts.count(copies[2 * i])) return fail(PKV_ERR_INVALID_ARG, "block %lld is a source and a destination",
                                                copies[2 * i]);
   const int block_chunks = (int)(block_elems * eb / 16);
-  CopyList list;
+  static thread_local CopyList list;  // 32 KB: off the stack
   for (int32_t first = 0; first < num_copies; first += kPairsPerLaunch) {
     const int n = num_copies - first < kPairsPerLaunch ? num_copies - first : kPairsPerLaunch;
     list.n = n;

@@ -36,10 +36,10 @@ def _host_bits(t: torch.Tensor) -> np.ndarray:
 
 
 @pytest.mark.parametrize("dtype,layered,n_pairs", [("bf16", False, 7), ("f32", False, 5), ("bf16", True, 9),
-                                                   ("bf16", False, 600)])
+                                                   ("bf16", False, 600), ("bf16", False, 4100)])
 def test_copy_blocks_bit_exact(dtype, layered, n_pairs):
     rng = np.random.default_rng(40 + n_pairs)
-    NB, bs, H, D, layers = 1400, 16, 4, 64 if dtype == "f32" else 128, 3
+    NB, bs, H, D, layers = max(1400, 2 * n_pairs + 8), 16, 4, 64 if dtype == "f32" else 128, 3
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     shape = (layers, NB + 5, bs, H, D) if layered else (NB, bs, H, D)
     k = torch.randn(shape, dtype=torch.float32).to(tdt).cuda()
