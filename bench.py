@@ -413,10 +413,14 @@ def block_manager_timing(w, reps: int = 50, with_oracle: bool = True) -> dict:
     width = st.block_tables.shape[1]
     ids = np.arange(B, dtype=np.int64)
 
+    # the manager gives every sequence its own blocks (the workload's shared
+    # prefixes are not registered with it): a pool with room for all of them
+    nb = int(sum(-(-int(L) // w.block_size) for L in st.context_lens)) + B
+
     def run(make, k):
         tot = 0.0
         for _ in range(k):
-            m = make(w.num_blocks, w.block_size, width)
+            m = make(nb, w.block_size, width)
             m.step(ids, cached)
             t0 = time.perf_counter()
             m.step(ids, n_new)
