@@ -36,7 +36,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged-attn decode KV GB/s (% HBM peak); mixed-batch query tokens/s"
-BASE_SEED = {"decode": 1002, "mixed": 1003, "prefill": 1003, "specverify": 1004, "prefix": 1005, "prefix-long": 1006}
+BASE_SEED = {"decode": 1002, "mixed": 1003, "prefill": 1003, "specverify": 1004, "prefix": 1005, "prefix-long": 1006,
+             "decode-fp8": 1002}
+# The FP8 (E4M3) cache workload: the decode batch with both pools encoded with
+# one scale each, chosen so that N(0, 1) values span the E4M3 range.
+FP8_SCALE = 4.5 / 448
 WORKLOAD_DESC = {
     "decode": "decode batch: 64 seqs, context U[512,4096], 1 query token, 32q/8kv heads, head_dim 128, "
               "block_size 16, 20000-block pool, random block permutation, bf16",
@@ -50,7 +54,15 @@ WORKLOAD_DESC = {
               "suffixes, 1 query token, 32q/8kv, head_dim 128, block_size 16, bf16; shared-prefix hint set",
     "prefix-long": "long-context prefix-shared decode: 4 seqs x 131072 tokens (2048 shared), 1 query token, "
                    "32q/8kv, head_dim 128, block_size 16, bf16; shared-prefix hint set",
+    "decode-fp8": "decode batch with FP8 (E4M3) K/V pools: 64 seqs, context U[512,4096], 1 query token, 32q/8kv "
+                  "heads, head_dim 128, block_size 16, 20000-block pool, q/out bf16, one scale per pool "
+                  "(4.5/448)",
 }
+
+
+def workload_of(name: str, seed: int):
+    import workloads as wl
+    return wl.decode_batch(seed=seed) if name == "decode-fp8" else wl.CONFIGS[name](seed=seed)
 
 
 def _peaks():
@@ -61,19 +73,21 @@ def _peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def algorithmic_bytes(w) -> dict:
-    """Bytes a perfect implementation must move for one step of workload w."""
+def algorithmic_bytes(w, fp8: bool = False) -> dict:
+    """Bytes a perfect implementation must move for one step of workload w
+    (fp8: the pools hold one-byte codes; q, out and the new rows stay bf16)."""
     st = w.step
     es = 2 if w.dtype == "bf16" else 4
+    kv_es = 1 if fp8 else es
     Hkv, D, Hq = w.num_kv_heads, w.head_dim, w.num_q_heads
     L = st.context_lens.astype(np.int64)
     shared = int(w.meta.get("shared_prefix_tokens", 0))
     # unique KV tokens: a shared prefix is read from HBM once
     uniq_tokens = int(L.sum()) - (shared * (len(L) - 1) if shared else 0)
-    kv = uniq_tokens * Hkv * D * es * 2
+    kv = uniq_tokens * Hkv * D * kv_es * 2
     T = st.num_tokens
     qo = 2 * T * Hq * D * es
-    write = 4 * T * Hkv * D * es + 8 * T
+    write = 2 * T * Hkv * D * (es + kv_es) + 8 * T
     bt = int(((L + w.block_size - 1) // w.block_size).sum()) * 4 + 8 * len(L) + 4
     attn = kv + qo
     return {"step": attn + write + bt, "attn_kernel": kv + qo, "kv": kv, "write": write}
@@ -102,10 +116,13 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def launches_per_step(w, max_q_len: int, shared_prefix: bool) -> int:
+def launches_per_step(w, max_q_len: int, shared_prefix: bool, fp8: bool = False) -> int:
     """Our kernels per step, as paged_attention_forward chooses them: the K/V
     write, [the shared-prefix search], the planner, [the tensor-core kernel],
-    the decode-shaped kernel (split merges run inside the attention kernels)."""
+    the decode-shaped kernel (split merges run inside the attention kernels).
+    FP8 pools: the write, the planner and the CUDA-core kernel."""
+    if fp8:
+        return 3
     g = w.num_q_heads // w.num_kv_heads
     tc = w.dtype == "bf16" and w.head_dim == 128 and g & (g - 1) == 0
     dectc = tc and g <= 16
@@ -189,9 +206,21 @@ def run_gpu(args, rank, world, local_rank):
             return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
         return torch.from_numpy(a).to(dev)
 
-    def prepare(w):
+    def prepare(w, fp8=False):
         st = w.step
-        return dict(kc=to_dev(w.k_cache), vc=to_dev(w.v_cache), q=to_dev(st.q), k=to_dev(st.k_new),
+        kc, vc = to_dev(w.k_cache), to_dev(w.v_cache)
+        if fp8:
+            # the pools' bf16 rows encoded on the device by the library's FP8 write
+            NB, bs = kc.shape[0], kc.shape[1]
+            kc8 = torch.empty(kc.shape, dtype=torch.uint8, device=dev)
+            vc8 = torch.empty_like(kc8)
+            slots = torch.arange(NB * bs, dtype=torch.int64, device=dev)
+            pkv.paged_kv_write_fp8(kc.view(NB * bs, kc.shape[2], kc.shape[3]), vc.view(NB * bs, kc.shape[2], kc.shape[3]),
+                                   slots, kc8, vc8, FP8_SCALE, FP8_SCALE)
+            torch.cuda.synchronize()
+            del kc, vc, slots
+            kc, vc = kc8, vc8
+        return dict(kc=kc, vc=vc, fp8=fp8, q=to_dev(st.q), k=to_dev(st.k_new),
                     v=to_dev(st.v_new), slots=torch.from_numpy(st.slot_mapping).to(dev),
                     bt=torch.from_numpy(st.block_tables).to(dev), ctx=torch.from_numpy(st.context_lens).to(dev),
                     qsl=torch.from_numpy(st.query_start_loc).to(dev), mql=int(st.q_lens.max(initial=0)),
@@ -206,6 +235,12 @@ def run_gpu(args, rank, world, local_rank):
                                             w.head_dim), dtype=torch.uint8, device=dev)
 
         def one():
+            if t["fp8"]:
+                pkv.paged_kv_write_fp8(t["k"], t["v"], t["slots"], t["kc"], t["vc"], FP8_SCALE, FP8_SCALE)
+                pkv.paged_attention_forward_fp8kv(t["q"], t["kc"], t["vc"], t["bt"], t["ctx"], t["qsl"], w.scale,
+                                                  FP8_SCALE, FP8_SCALE, w.causal, out=out, workspace=ws,
+                                                  max_query_len=t["mql"])
+                return
             pkv.paged_kv_write(t["k"], t["v"], t["slots"], t["kc"], t["vc"])
             pkv.paged_attention_forward(t["q"], t["kc"], t["vc"], t["bt"], t["ctx"], t["qsl"], w.scale, w.causal,
                                         out=out, workspace=ws, max_query_len=t["mql"], shared_prefix=t["sp"])
@@ -247,8 +282,9 @@ def run_gpu(args, rank, world, local_rank):
         return step_ms, kern_ms, out
 
     # ---------------- headline workload ----------------
-    w = wl.CONFIGS[args.workload](seed=BASE_SEED[args.workload] + rank)
-    t = prepare(w)
+    fp8 = args.workload == "decode-fp8"
+    w = workload_of(args.workload, BASE_SEED[args.workload] + rank)
+    t = prepare(w, fp8)
     sampler = ClockSampler(_gpu_id(torch, dev))
     time.sleep(0.3)
     step_ms, kern_ms, out = timed(w, t, args.steps, args.warmup)
@@ -256,7 +292,7 @@ def run_gpu(args, rank, world, local_rank):
     flags = pkv.device_errors()
     if flags:
         raise SystemExit(f"device error word set: {flags:#x}")
-    ab = algorithmic_bytes(w)
+    ab = algorithmic_bytes(w, fp8)
     tot_ms = max_over_ranks(sum(step_ms), world, dev)
     value = ab["step"] * args.steps * world / (tot_ms * 1e-3) / 1e9
     kern_avg_ms = sum(kern_ms) / len(kern_ms)
@@ -272,7 +308,8 @@ def run_gpu(args, rank, world, local_rank):
         # bf16 head_dim-128 batches run on the tensor-core kernels (the CUDA-core
         # decode_kernel serves the other shapes)
         kname = "mma_attn_kernel (tcgen05)" if args.workload == "specverify" else (
-            "mma_attn_kernel + dectc_kernel" if args.workload == "mixed" else "dectc_kernel (tcgen05 decode)")
+            "mma_attn_kernel + dectc_kernel" if args.workload == "mixed" else
+            "decode_kernel (CUDA cores, FP8 E4M3 K/V)" if fp8 else "dectc_kernel (tcgen05 decode)")
         roof = {"bound": "hbm", "kernel": kname + ", attention kernels per launch", "achieved": round(achieved, 1),
                 "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                 "peak_kind": peak_kind + " HBM copy", "traffic": ncu_traffic(args.workload),
@@ -311,10 +348,16 @@ def run_gpu(args, rank, world, local_rank):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         dev_buf.copy_(host_buf, non_blocking=True)
-        pkv.paged_kv_write(d["k"], d["v"], d["slots"], t["kc"], t["vc"])
-        o = pkv.paged_attention_forward(d["q"], t["kc"], t["vc"], d["bt"], d["ctx"], d["qsl"], w.scale, w.causal,
-                                        out=out_dev, workspace=ws, max_query_len=t["mql"],
-                                        shared_prefix=t["sp"])
+        if fp8:
+            pkv.paged_kv_write_fp8(d["k"], d["v"], d["slots"], t["kc"], t["vc"], FP8_SCALE, FP8_SCALE)
+            o = pkv.paged_attention_forward_fp8kv(d["q"], t["kc"], t["vc"], d["bt"], d["ctx"], d["qsl"], w.scale,
+                                                  FP8_SCALE, FP8_SCALE, w.causal, out=out_dev, workspace=ws,
+                                                  max_query_len=t["mql"])
+        else:
+            pkv.paged_kv_write(d["k"], d["v"], d["slots"], t["kc"], t["vc"])
+            o = pkv.paged_attention_forward(d["q"], t["kc"], t["vc"], d["bt"], d["ctx"], d["qsl"], w.scale,
+                                            w.causal, out=out_dev, workspace=ws, max_query_len=t["mql"],
+                                            shared_prefix=t["sp"])
         host_out.copy_(o, non_blocking=True)
         b.record()
         b.synchronize()
@@ -337,7 +380,7 @@ def run_gpu(args, rank, world, local_rank):
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_tot / args.steps, 5)},
-        "gpu_launches": launches_per_step(w, t["mql"], t["sp"]) * args.steps,
+        "gpu_launches": launches_per_step(w, t["mql"], t["sp"], fp8) * args.steps,
         "clocks": clocks,
     }
 
@@ -364,7 +407,7 @@ def run_gpu(args, rank, world, local_rank):
     if rank == 0:
         result["block_manager"] = block_manager_timing(w, with_oracle=not args.no_cpu_baseline)
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds, fp8=fp8)
     return result
 
 
@@ -437,14 +480,17 @@ def block_manager_timing(w, reps: int = 50, with_oracle: bool = True) -> dict:
     return out
 
 
-def cpu_baseline(w, budget_s: float = 15.0) -> dict:
+def cpu_baseline(w, budget_s: float = 15.0, fp8: bool = False) -> dict:
     """The fp64 oracle, as it stands, on sequences of the same workload until
     the time budget is spent; GB/s over the algorithmic bytes of the rows it
-    produced."""
+    produced.  fp8: the oracle's E4M3 encoding of each gathered row, decoded,
+    then the same attention (bytes counted at one per cached element)."""
     import workloads as wl
+    from oracle import fp8 as ofp8
     from oracle import paged_oracle as po
     st = w.step
     es = 2 if w.dtype == "bf16" else 4
+    kv_es = 1 if fp8 else es
     kc, vc = w.k_cache, w.v_cache
     done, nbytes = 0, 0
     t0 = time.perf_counter()
@@ -453,9 +499,12 @@ def cpu_baseline(w, budget_s: float = 15.0) -> dict:
         L = int(st.context_lens[s])
         K = wl.to_f64(po.gather(kc, st.block_tables[s], L), w.dtype)
         V = wl.to_f64(po.gather(vc, st.block_tables[s], L), w.dtype)
+        if fp8:
+            K = ofp8.dequantize(ofp8.quantize(K.astype(np.float32), FP8_SCALE), FP8_SCALE)
+            V = ofp8.dequantize(ofp8.quantize(V.astype(np.float32), FP8_SCALE), FP8_SCALE)
         po.attend(wl.to_f64(st.q[a:b], w.dtype), K, V, w.scale, w.causal)
         done += 1
-        nbytes += L * w.num_kv_heads * w.head_dim * es * 2 + 2 * (b - a) * w.num_q_heads * w.head_dim * es
+        nbytes += L * w.num_kv_heads * w.head_dim * kv_es * 2 + 2 * (b - a) * w.num_q_heads * w.head_dim * es
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
@@ -470,11 +519,12 @@ def run_reference(args):
     same workload (the oracle on its sequences for about a budget's worth of
     seconds), timed on the host cores."""
     import workloads as wl
-    w = wl.CONFIGS[args.workload](seed=BASE_SEED[args.workload])
+    w = workload_of(args.workload, BASE_SEED[args.workload])
     vals, secs = [], []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        r = cpu_baseline(w, budget_s=max(1.0, args.cpu_seconds / max(1, args.steps)))
+        r = cpu_baseline(w, budget_s=max(1.0, args.cpu_seconds / max(1, args.steps)),
+                         fp8=args.workload == "decode-fp8")
         if i >= args.warmup:
             vals.append(r)
             secs.append(time.perf_counter() - t0)
@@ -534,6 +584,7 @@ def _code_only(text: str) -> str:
 FORWARD_SOURCES = ("api.cu", "kv_write.cu", "planner.cu", "static_ws.cu", "pkv_device.cuh", "pkv_tc.cuh",
                    "pkv_internal.h")
 WORKLOAD_KERNELS = {"decode": ("decode.cu", "dectc.cu"), "prefix-long": ("decode.cu", "dectc.cu"),
+                    "decode-fp8": ("decode.cu",),
                     "prefill": ("mma_attn.cu",), "specverify": ("mma_attn.cu",),
                     "prefix": ("decode.cu", "dectc.cu", "mma_attn.cu")}
 

@@ -71,7 +71,8 @@ typedef enum {
 
 typedef enum {
   PKV_DTYPE_F32 = 0,
-  PKV_DTYPE_BF16 = 1
+  PKV_DTYPE_BF16 = 1,
+  PKV_DTYPE_FP8_E4M3 = 2  /* cache codes only: see paged_kv_write_fp8 */
 } pkv_dtype;
 
 /*
@@ -203,6 +204,50 @@ pkv_status paged_attention_forward_static_ws(const void* q, const void* k_cache,
                                              int32_t block_size, int32_t max_blocks_per_seq,
                                              int32_t max_query_len, float scale, int32_t causal,
                                              int32_t hints, pkv_dtype dtype, void* stream);
+
+/*
+ * FP8 KV cache (the library's own format; the source pages name no cache
+ * precision).  Each pool element is an 8-bit E4M3 code (OCP "e4m3fn": 1 sign,
+ * 4 exponent bits with bias 7, 3 mantissa bits, largest finite value 448, no
+ * infinities), with one fp32 scale for the K pool and one for the V pool,
+ * chosen by the caller (e.g. per layer):
+ *   code = E4M3(RNE(x / scale)), x / scale an IEEE fp32 division, magnitudes
+ *          beyond 448 saturated to +-448
+ *   value read = code * scale.
+ * Pools are [num_blocks, block_size, num_kv_heads, head_dim] bytes: half the
+ * bytes of bf16, so decode, which reads every cached row once per step,
+ * moves half the memory.
+ *
+ * paged_kv_write_fp8 - paged_kv_write into FP8 pools: rows k, v of `dtype`
+ * (bf16 or f32; token strides in elements, multiples of 16 bytes; 0 means
+ * dense) are encoded with k_scale / v_scale and scattered by slot_mapping
+ * (slots < 0 skipped).  num_kv_heads * head_dim must be a multiple of 16.
+ */
+pkv_status paged_kv_write_fp8(const void* k, const void* v, const int64_t* slot_mapping,
+                              void* k_cache, void* v_cache,
+                              int64_t num_tokens, int64_t num_blocks, int32_t block_size,
+                              int32_t num_kv_heads, int32_t head_dim,
+                              int64_t k_token_stride, int64_t v_token_stride,
+                              pkv_dtype dtype, float k_scale, float v_scale, void* stream);
+
+/*
+ * paged_attention_forward_fp8kv - paged_attention_forward with FP8 pools:
+ * q and out bf16, k_cache / v_cache E4M3 codes read as code * k_scale and
+ * code * v_scale; the same metadata, workspace and results otherwise
+ * (softmax(scale q k^T) v, fp32 accumulation).  head_dim 128 (other head
+ * sizes: PKV_ERR_UNSUPPORTED); any block_size, GQA group and query count of
+ * paged_attention_forward.  Every row runs on the CUDA-core kernel (K and V
+ * converted to fp32 in registers); PKV_HINT_SHARED_PREFIX is ignored.
+ */
+pkv_status paged_attention_forward_fp8kv(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, const int32_t* context_lens,
+                                         const int32_t* query_start_loc, void* out,
+                                         int32_t num_seqs, int64_t num_tokens, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                                         int32_t block_size, int32_t max_blocks_per_seq,
+                                         int32_t max_query_len, float scale, int32_t causal,
+                                         float k_scale, float v_scale, int32_t hints, void* workspace,
+                                         size_t workspace_bytes, void* stream);
 
 /* Bytes of the static scratch used by paged_attention_forward_static_ws. */
 size_t paged_attention_static_workspace_bytes(void);

@@ -67,9 +67,16 @@ def e4m3_encode(x) -> np.ndarray:
 
 
 def quantize(x, scale: float) -> np.ndarray:
-    """Codes of x / scale (the division in fp32, as the kernel does)."""
-    q = (np.asarray(x, dtype=np.float32) / np.float32(scale)).astype(np.float32)
-    return e4m3_encode(q)
+    """Codes of x / scale (the division in fp32, as the kernel does).
+    Large arrays are encoded in slices (memory only; every element is
+    independent)."""
+    x = np.asarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    flat, res = x.reshape(-1), out.reshape(-1)
+    step = 1 << 22
+    for a in range(0, flat.size, step):
+        res[a:a + step] = e4m3_encode((flat[a:a + step] / np.float32(scale)).astype(np.float32))
+    return out
 
 
 def dequantize(codes, scale: float) -> np.ndarray:

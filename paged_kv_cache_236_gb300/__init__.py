@@ -9,6 +9,8 @@ tensors are not on a CUDA device, the calls raise.
     paged_kv_write(k, v, slot_mapping, k_cache, v_cache)
     paged_attention_forward(q, k_cache, v_cache, block_tables, context_lens,
                             query_start_loc, scale, causal)
+    paged_kv_write_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale)
+    paged_attention_forward_fp8kv(q, k_cache, v_cache, ..., scale, k_scale, v_scale)
     BlockManager(num_blocks, block_size, max_blocks_per_seq)   (host, C++)
     copy_blocks(k_cache, v_cache, copies)                      (copy-on-write)
 
@@ -29,7 +31,7 @@ import torch
 __all__ = [
     "paged_kv_write", "paged_attention_forward", "workspace_size", "workspace_min",
     "device_errors", "set_profile_events", "profile_elapsed_ms", "lib", "LibraryError", "DEVERR",
-    "BlockManager", "OutOfBlocks", "copy_blocks",
+    "BlockManager", "OutOfBlocks", "copy_blocks", "paged_kv_write_fp8", "paged_attention_forward_fp8kv",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -112,7 +114,12 @@ def lib() -> ctypes.CDLL:
                     ("pkv_bm_block_table", [c_vp, c_i64, c_vp, c_p32, c_p32]),
                     ("pkv_bm_stats", [c_vp, c_p32, c_p32, c_p32, c_p32]),
                     ("paged_kv_copy_blocks", [c_vp, c_vp, c_vp, c_i32, c_i32, c_i64, c_i64, c_i32, c_i32, c_i32,
-                                              c_i32, c_vp])):
+                                              c_i32, c_vp]),
+                    ("paged_kv_write_fp8", [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i32, c_i32, c_i32, c_i64,
+                                            c_i64, c_i32, c_f, c_f, c_vp]),
+                    ("paged_attention_forward_fp8kv", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i64, c_i32,
+                                                       c_i32, c_i32, c_i64, c_i32, c_i32, c_i32, c_f, c_i32, c_f,
+                                                       c_f, c_i32, c_vp, c_sz, c_vp])):
                 getattr(L, name).restype = c_i32
                 getattr(L, name).argtypes = args
             L.pkv_bm_destroy.restype = None
@@ -386,3 +393,84 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, copies) -> None:
         _check(lib().paged_kv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(),
                                           pairs.ctypes.data if len(pairs) else None, len(pairs), layers, stride,
                                           NB, bs, Hkv, D, DTYPE[k_cache.dtype], _stream(dev)))
+
+
+# ----------------------------------------------------------------------------
+# FP8 (E4M3) pools (include/paged_kv.h: paged_kv_write_fp8,
+# paged_attention_forward_fp8kv)
+# ----------------------------------------------------------------------------
+
+_FP8_TYPES = {torch.uint8} | ({torch.float8_e4m3fn} if hasattr(torch, "float8_e4m3fn") else set())
+
+
+def _check_fp8_pools(k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
+    if k_cache.dtype not in _FP8_TYPES or v_cache.dtype != k_cache.dtype:
+        raise ValueError("FP8 pools must be uint8 (E4M3 codes) or float8_e4m3fn tensors")
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape or not k_cache.is_contiguous() or \
+            not v_cache.is_contiguous():
+        raise ValueError("caches must be contiguous [num_blocks, block_size, num_kv_heads, head_dim]")
+
+
+def paged_kv_write_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                       v_cache: torch.Tensor, k_scale: float, v_scale: float) -> None:
+    """Encode ``k, v [T, Hkv, D]`` (bf16 or f32) as E4M3 codes of x / scale
+    and scatter them into the FP8 pools at ``slot_mapping`` (< 0 skips)."""
+    dev = _need_cuda(k, v, slot_mapping, k_cache, v_cache)
+    _check_fp8_pools(k_cache, v_cache)
+    if k.dtype not in DTYPE or v.dtype != k.dtype:
+        raise ValueError("k and v must share dtype bfloat16 or float32")
+    NB, bs, Hkv, D = k_cache.shape
+    T = k.shape[0]
+    for name, t in (("k", k), ("v", v)):
+        if t.dim() != 3 or tuple(t.shape[1:]) != (Hkv, D) or t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError(f"{name} must be [T, {Hkv}, {D}] with contiguous heads")
+    if v.shape[0] != T or slot_mapping.shape != (T,) or slot_mapping.dtype != torch.int64 or \
+            not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous int64 [T]")
+    with torch.cuda.device(dev):
+        _check(lib().paged_kv_write_fp8(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), k_cache.data_ptr(),
+                                        v_cache.data_ptr(), T, NB, bs, Hkv, D, k.stride(0) if T else 0,
+                                        v.stride(0) if T else 0, DTYPE[k.dtype], float(k_scale), float(v_scale),
+                                        _stream(dev)))
+
+
+def paged_attention_forward_fp8kv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                  block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                  query_start_loc: torch.Tensor, scale: float, k_scale: float, v_scale: float,
+                                  causal: bool = True, *, out: torch.Tensor | None = None,
+                                  workspace: torch.Tensor | None = None, max_query_len: int = 0) -> torch.Tensor:
+    """``paged_attention_forward`` over FP8 pools read as code * k_scale and
+    code * v_scale; q and the result are bf16, head_dim 128."""
+    dev = _need_cuda(q, k_cache, v_cache, block_tables, context_lens, query_start_loc)
+    _check_fp8_pools(k_cache, v_cache)
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or not q.is_contiguous():
+        raise ValueError("q must be contiguous bfloat16 [T, Hq, D]")
+    T, Hq, D = q.shape
+    NB, bs, Hkv, Dk = k_cache.shape
+    if Dk != D:
+        raise ValueError("head_dim of q and the caches differ")
+    B = context_lens.shape[0]
+    for name, t, shape in (("block_tables", block_tables, None), ("context_lens", context_lens, (B,)),
+                           ("query_start_loc", query_start_loc, (B + 1,))):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous int32")
+        if shape is not None and tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or (B > 0 and block_tables.shape[1] == 0):
+        raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq] with max_blocks_per_seq > 0")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.device != dev:
+        raise ValueError("out must match q")
+    with torch.cuda.device(dev):
+        need = workspace_min(B, T, Hq, Hkv, D)
+        if workspace is None:
+            workspace = _workspace(dev, workspace_size(B, T, Hq, Hkv, D))
+        if workspace.dtype != torch.uint8 or workspace.device != dev or workspace.numel() < need:
+            raise ValueError(f"workspace must be a uint8 CUDA tensor of at least {need} bytes")
+        _check(lib().paged_attention_forward_fp8kv(
+            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
+            query_start_loc.data_ptr(), out.data_ptr(), B, T, Hq, Hkv, D, NB, bs, max(1, block_tables.shape[1]),
+            int(max_query_len), float(scale), 1 if causal else 0, float(k_scale), float(v_scale), 0,
+            workspace.data_ptr(), workspace.numel(), _stream(dev)))
+    return out

@@ -84,7 +84,7 @@ pkv_status device_info(DeviceInfo** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int elem_bytes(pkv_dtype dt) { return dt == PKV_DTYPE_BF16 ? 2 : 4; }
+int elem_bytes(pkv_dtype dt) { return dt == PKV_DTYPE_BF16 ? 2 : dt == PKV_DTYPE_FP8_E4M3 ? 1 : 4; }
 
 // 4-D map of a block pool [NB, bs, Hkv, D] with a box of one block of one kv head.
 pkv_status encode_pool_map(CUtensorMap* map, const void* base, pkv_dtype dt, int64_t NB, int bs, int Hkv, int D,
@@ -94,7 +94,10 @@ pkv_status encode_pool_map(CUtensorMap* map, const void* base, pkv_dtype dt, int
   cuuint64_t strides[3] = {(cuuint64_t)D * es, (cuuint64_t)Hkv * D * es, (cuuint64_t)bs * Hkv * D * es};
   cuuint32_t box[4] = {(cuuint32_t)box_d, 1, (cuuint32_t)bs, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = g_encode(map, dt == PKV_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+  const CUtensorMapDataType ty = dt == PKV_DTYPE_BF16        ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dt == PKV_DTYPE_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r = g_encode(map, ty,
                         4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (pool) failed: %d", (int)r);
@@ -244,6 +247,40 @@ pkv_status paged_kv_write(const void* k, const void* v, const int64_t* slot_mapp
   return PKV_OK;
 }
 
+pkv_status paged_kv_write_fp8(const void* k, const void* v, const int64_t* slot_mapping, void* k_cache,
+                              void* v_cache, int64_t num_tokens, int64_t num_blocks, int32_t block_size,
+                              int32_t num_kv_heads, int32_t head_dim, int64_t k_token_stride, int64_t v_token_stride,
+                              pkv_dtype dtype, float k_scale, float v_scale, void* stream) {
+  g_msg[0] = 0;
+  if (dtype != PKV_DTYPE_BF16 && dtype != PKV_DTYPE_F32) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", (int)dtype);
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "sizes must be positive (num_tokens >= 0)");
+  if (!(k_scale > 0.f) || !isfinite(k_scale) || !(v_scale > 0.f) || !isfinite(v_scale))
+    return fail(PKV_ERR_INVALID_ARG, "k_scale and v_scale must be positive and finite");
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  if (row > (1 << 24)) return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads * head_dim too large");
+  if (row % 16 != 0) return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads * head_dim not a multiple of 16");
+  if (k_token_stride == 0) k_token_stride = row;
+  if (v_token_stride == 0) v_token_stride = row;
+  if (k_token_stride < row || v_token_stride < row)
+    return fail(PKV_ERR_INVALID_ARG, "token stride smaller than num_kv_heads * head_dim");
+  const int es = elem_bytes(dtype);
+  if ((k_token_stride * es) % 16 != 0 || (v_token_stride * es) % 16 != 0)
+    return fail(PKV_ERR_UNSUPPORTED, "token strides must be multiples of 16 bytes");
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PKV_ERR_INVALID_ARG, "rows and caches must be 16-byte aligned");
+  DeviceInfo* d = nullptr;
+  pkv_status st = device_info(&d);
+  if (st != PKV_OK) return st;
+  cudaError_t e = launch_kv_write_fp8(k, v, slot_mapping, k_cache, v_cache, num_tokens, num_blocks * block_size,
+                                      (int)row, es, k_token_stride, v_token_stride, k_scale, v_scale, d->err,
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "paged_kv_write_fp8 launch");
+  return PKV_OK;
+}
+
 size_t paged_attention_workspace_size(int32_t num_seqs, int64_t num_tokens, int32_t num_q_heads,
                                       int32_t num_kv_heads, int32_t head_dim) {
   if (num_seqs < 0 || num_tokens < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
@@ -256,13 +293,15 @@ size_t paged_attention_workspace_min(int32_t num_seqs, int64_t num_tokens, int32
   return workspace_layout(num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, 0, 0, false).total;
 }
 
-pkv_status paged_attention_forward(const void* q, const void* k_cache, const void* v_cache,
-                                   const int32_t* block_tables, const int32_t* context_lens,
-                                   const int32_t* query_start_loc, void* out, int32_t num_seqs, int64_t num_tokens,
-                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
-                                   int32_t block_size, int32_t max_blocks_per_seq, int32_t max_query_len,
-                                   float scale, int32_t causal, int32_t hints, void* workspace,
-                                   size_t workspace_bytes, pkv_dtype dtype, void* stream) {
+// The forward call; kv_fp8: the pools hold E4M3 codes (q and out bf16), read
+// as code * k_scale and code * v_scale.
+static pkv_status forward_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                               const int32_t* context_lens, const int32_t* query_start_loc, void* out,
+                               int32_t num_seqs, int64_t num_tokens, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int64_t num_blocks, int32_t block_size, int32_t max_blocks_per_seq,
+                               int32_t max_query_len, float scale, int32_t causal, int32_t hints, void* workspace,
+                               size_t workspace_bytes, pkv_dtype dtype, bool kv_fp8, float k_scale, float v_scale,
+                               void* stream) {
   g_msg[0] = 0;
   const int B = num_seqs, Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim, bs = block_size;
   const int64_t T = num_tokens;
@@ -297,7 +336,7 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   const int G = Hq / Hkv;
 
   int dec_ctas = 1;
-  cudaError_t e = decode_ctas_per_sm(bf16, D, &dec_ctas);
+  cudaError_t e = kv_fp8 ? decode_fp8_ctas_per_sm(&dec_ctas) : decode_ctas_per_sm(bf16, D, &dec_ctas);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel set-up");
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -311,7 +350,7 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
 
   // tensor-core path: bf16, head_dim 128, G a power of two (a 128-row tile is
   // 128/G whole tokens)
-  const bool mma_ok = bf16 && D == 128 && (G & (G - 1)) == 0 && G <= 128;
+  const bool mma_ok = !kv_fp8 && bf16 && D == 128 && (G & (G - 1)) == 0 && G <= 128;
   // decode-shaped rows: tensor-core kernel (keys on M, rows on N) for bf16,
   // head_dim 128 and G dividing 16; the CUDA-core kernel otherwise
   const bool dectc = mma_ok && G <= kTcDecRows;
@@ -348,7 +387,8 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   const bool side_by_side = mma_launch && dectc && !cascade;
   pp.side_by_side = side_by_side ? 1 : 0;
   pp.sms = dev->sms;
-  pp.kv_key_bytes = 2 * D * elem_bytes(dtype);
+  const pkv_dtype kv_dtype = kv_fp8 ? PKV_DTYPE_FP8_E4M3 : dtype;
+  pp.kv_key_bytes = 2 * D * elem_bytes(kv_dtype);
   pp.block_tables = block_tables;
   pp.dec_rows_max = dec_rows_max;
   pp.dec_unit_rows = dectc ? tc_rows : kDecRows;
@@ -386,9 +426,11 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   if ((e = launch_planner(pp, s)) != cudaSuccess) return cuda_fail(e, "planner launch");
 
   CUtensorMap kmap, vmap;
-  if ((st = encode_pool_map(&kmap, k_cache, dtype, num_blocks, bs, Hkv, D, D, CU_TENSOR_MAP_SWIZZLE_NONE)) != PKV_OK)
+  if ((st = encode_pool_map(&kmap, k_cache, kv_dtype, num_blocks, bs, Hkv, D, D, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+      PKV_OK)
     return st;
-  if ((st = encode_pool_map(&vmap, v_cache, dtype, num_blocks, bs, Hkv, D, D, CU_TENSOR_MAP_SWIZZLE_NONE)) != PKV_OK)
+  if ((st = encode_pool_map(&vmap, v_cache, kv_dtype, num_blocks, bs, Hkv, D, D, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+      PKV_OK)
     return st;
 
   AttnParams ap{};
@@ -409,7 +451,8 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   ap.bs = bs;
   ap.max_blocks = max_blocks_per_seq;
   ap.num_blocks = num_blocks;
-  ap.scale_log2 = scale * 1.4426950408889634f;
+  ap.scale_log2 = (kv_fp8 ? scale * k_scale : scale) * 1.4426950408889634f;
+  ap.v_scale = kv_fp8 ? v_scale : 1.f;
   ap.causal = causal ? 1 : 0;
   ap.out_al32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   ap.err = dev->err;
@@ -446,12 +489,44 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
       return st;
     if ((e = launch_dectc(ap, tc_rows, qmap16, kmap_sw, vmap_sw, dev->sms, s)) != cudaSuccess)
       return cuda_fail(e, "decode (tensor-core) launch");
+  } else if (kv_fp8) {
+    if ((e = launch_decode_fp8(ap, kmap, vmap, dec_grid, s)) != cudaSuccess) return cuda_fail(e, "decode launch");
   } else if ((e = launch_decode(ap, kmap, vmap, bf16, dec_grid, s)) != cudaSuccess) {
     return cuda_fail(e, "decode launch");
   }
   if (g_prof_stop && (e = cudaEventRecord(g_prof_stop, s)) != cudaSuccess) return cuda_fail(e, "profile event");
 
   return PKV_OK;
+}
+
+pkv_status paged_attention_forward(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, const int32_t* context_lens,
+                                   const int32_t* query_start_loc, void* out, int32_t num_seqs, int64_t num_tokens,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                                   int32_t block_size, int32_t max_blocks_per_seq, int32_t max_query_len,
+                                   float scale, int32_t causal, int32_t hints, void* workspace,
+                                   size_t workspace_bytes, pkv_dtype dtype, void* stream) {
+  return forward_impl(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, out, num_seqs, num_tokens,
+                      num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq, max_query_len,
+                      scale, causal, hints, workspace, workspace_bytes, dtype, false, 1.f, 1.f, stream);
+}
+
+pkv_status paged_attention_forward_fp8kv(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, const int32_t* context_lens,
+                                         const int32_t* query_start_loc, void* out, int32_t num_seqs,
+                                         int64_t num_tokens, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int64_t num_blocks, int32_t block_size,
+                                         int32_t max_blocks_per_seq, int32_t max_query_len, float scale,
+                                         int32_t causal, float k_scale, float v_scale, int32_t hints,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+  g_msg[0] = 0;
+  if (!(k_scale > 0.f) || !isfinite(k_scale) || !(v_scale > 0.f) || !isfinite(v_scale))
+    return fail(PKV_ERR_INVALID_ARG, "k_scale and v_scale must be positive and finite");
+  if (head_dim != 128) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d with an FP8 cache (supported: 128)", head_dim);
+  return forward_impl(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, out, num_seqs, num_tokens,
+                      num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq, max_query_len,
+                      scale, causal, hints, workspace, workspace_bytes, PKV_DTYPE_BF16, true, k_scale, v_scale,
+                      stream);
 }
 
 }  // extern "C"

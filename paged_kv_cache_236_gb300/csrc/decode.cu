@@ -29,6 +29,7 @@
 //    shuffles per 8 scores), warp-level online softmax, then P.V with each
 //    lane owning head_dim/32 output columns of all 4 rows (packed FMAs); the
 //    4 warp states are merged at the end of an item through shared memory.
+#include <cuda_fp8.h>
 #include <math_constants.h>
 
 #include "pkv_device.cuh"
@@ -48,18 +49,24 @@ constexpr int kRounds = kWarpKeys / kKeysPerRound;        // 2
 constexpr int kMetaDone = 2, kMetaLast = 1, kMetaFirst = 4;
 static_assert(kRP == 4 && kLPT == 8, "butterfly below is written for 8 partials per lane");
 
-template <typename T, int D>
+// T: the element of q and out; KV: the element of the K and V pools (T, or
+// E4M3 codes for the FP8 cache, read as fp32 code values; the scales are
+// folded into the logit scale and applied to the output).
+template <typename T, typename KV, int D>
 struct Cfg {
   static constexpr int kEs = sizeof(T);
-  static constexpr int kRowBytes = D * kEs;
+  static constexpr int kKvEs = sizeof(KV);
+  static constexpr int kQRowBytes = D * kEs;
+  static constexpr int kRowBytes = D * kKvEs;  // one K or V row
   static constexpr int kChunks = kRowBytes / 16;
-  static constexpr int kCPL = kChunks / kLPT;  // 16-byte chunks per lane per key
-  static constexpr int kEPC = 16 / kEs;        // elements per chunk
+  static constexpr int kCPL = kChunks / kLPT;  // 16-byte K chunks per lane per key
+  static constexpr int kEPC = 16 / kKvEs;      // K elements per chunk
   static constexpr int kEPL = kCPL * kEPC;     // q elements per lane
+  static constexpr int kQCPC = kEPC * kEs / 16;  // 16-byte q chunks per K chunk
   static constexpr int kDPL = D / 32;          // output columns per lane
   static constexpr int kTileBytes = kDecTileKeys * kRowBytes;
   static constexpr int kQSlotOff = 2 * kTileBytes;  // an item's q rows, in its first tile's stage
-  static constexpr int kStageBytes = (2 * kTileBytes + kRP * kRowBytes + 1023) / 1024 * 1024;
+  static constexpr int kStageBytes = (2 * kTileBytes + kRP * kQRowBytes + 1023) / 1024 * 1024;
   static constexpr int kStages =
       (98304 / kStageBytes) < 2 ? 2 : ((98304 / kStageBytes) > 4 ? 4 : (98304 / kStageBytes));
   // shared memory carve-up
@@ -74,6 +81,7 @@ struct Cfg {
   static constexpr int kBarOff = kMetaOff + kMetaBytes;
   static constexpr int kSmem = kBarOff + 2 * kStages * 8 + 16 + 1024;  // + slack to align the base to 1 KB
   static_assert(kCPL >= 1 && kChunks % kLPT == 0, "row must split into 8 lanes of 16-byte chunks");
+  static_assert(kQCPC >= 1, "q elements of a K chunk fill whole 16-byte chunks");
 };
 
 // What a stage carries besides K and V: which item and key tile, and the
@@ -101,11 +109,35 @@ __device__ __forceinline__ void chunk_to_pairs<float>(const uint4 raw, f32x2* f)
   f[0] = pk2(__uint_as_float(raw.x), __uint_as_float(raw.y));
   f[1] = pk2(__uint_as_float(raw.z), __uint_as_float(raw.w));
 }
+// Two E4M3 codes (low byte first) as their fp32 values (exact: E4M3 values
+// are fp16 values).
+__device__ __forceinline__ f32x2 e4m3x2_to_pair(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  return pk2(f.x, f.y);
+}
+template <>
+__device__ __forceinline__ void chunk_to_pairs<__nv_fp8_e4m3>(const uint4 raw, f32x2* f) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = e4m3x2_to_pair(w[i] & 0xFFFFu);
+    f[2 * i + 1] = e4m3x2_to_pair(w[i] >> 16);
+  }
+}
 
 // This lane's kDPL V columns of one key row as fp32 pairs.
 template <typename T, int DPL>
 __device__ __forceinline__ void load_v_pairs(const uint8_t* p, f32x2* f) {
-  if constexpr (sizeof(T) == 2) {
+  if constexpr (sizeof(T) == 1) {
+    if constexpr (DPL == 4) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+      f[0] = e4m3x2_to_pair(w & 0xFFFFu);
+      f[1] = e4m3x2_to_pair(w >> 16);
+    } else {
+      f[0] = e4m3x2_to_pair(*reinterpret_cast<const uint16_t*>(p));
+    }
+  } else if constexpr (sizeof(T) == 2) {
     if constexpr (DPL == 4) {
       const uint2 w = *reinterpret_cast<const uint2*>(p);
       f[0] = pk2(bf16_lo(w.x), bf16_hi(w.x));
@@ -154,11 +186,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
-template <typename T, int D>
+template <typename T, typename KV, int D>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
                                                              const __grid_constant__ CUtensorMap kmap,
                                                              const __grid_constant__ CUtensorMap vmap) {
-  using C = Cfg<T, D>;
+  using C = Cfg<T, KV, D>;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   f32x2* pbuf = reinterpret_cast<f32x2*>(smem + C::kPOff);
@@ -246,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
           m.L = L;
           m.n = n;
           m.qstart = qstart;
-          mbar_arrive_expect_tx(&full[stage], 2 * C::kTileBytes + (first ? it.nrows * C::kRowBytes : 0));
+          mbar_arrive_expect_tx(&full[stage], 2 * C::kTileBytes + (first ? it.nrows * C::kQRowBytes : 0));
         }
         __syncwarp();
         if (lane < nb_per_tile) {
@@ -259,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
           const int tok = row / p.G, g = row - tok * p.G;
           const T* qrow =
               reinterpret_cast<const T*>(p.q) + ((int64_t)(qstart + tok) * p.Hq + (int64_t)it.kvh * p.G + g) * D;
-          bulk_load(sbase + C::kQSlotOff + lane * C::kRowBytes, qrow, C::kRowBytes, &full[stage]);
+          bulk_load(sbase + C::kQSlotOff + lane * C::kQRowBytes, qrow, C::kQRowBytes, &full[stage]);
         }
         phys = next_phys;
         ++tile;
@@ -294,14 +326,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
 #pragma unroll
         for (int e = 0; e < C::kDPL / 2; ++e) acc[r][e] = 0ull;
         if (r < mt.nrows) {
-          const uint8_t* qrow = sbase + C::kQSlotOff + r * C::kRowBytes;
+          const uint8_t* qrow = sbase + C::kQSlotOff + r * C::kQRowBytes;
+          // this lane's q elements: the kEPC elements of each of its K chunks
 #pragma unroll
           for (int m = 0; m < C::kCPL; ++m) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(qrow + (j + 8 * m) * 16);
-            f32x2 f[C::kEPC / 2];
-            chunk_to_pairs<T>(raw, f);
 #pragma unroll
-            for (int e = 0; e < C::kEPC / 2; ++e) qf[r][m * (C::kEPC / 2) + e] = mul2(f[e], sc2);
+            for (int u = 0; u < C::kQCPC; ++u) {
+              const uint4 raw = *reinterpret_cast<const uint4*>(qrow + ((j + 8 * m) * C::kQCPC + u) * 16);
+              constexpr int kQP = 8 / C::kEs;  // fp32 pairs in a 16-byte q chunk
+              f32x2 f[kQP];
+              chunk_to_pairs<T>(raw, f);
+#pragma unroll
+              for (int e = 0; e < kQP; ++e) qf[r][m * (C::kEPC / 2) + u * kQP + e] = mul2(f[e], sc2);
+            }
           }
         } else {
 #pragma unroll
@@ -330,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
         for (int m = 0; m < C::kCPL; ++m) {
           const uint4 raw = *reinterpret_cast<const uint4*>(krow + (j + 8 * m) * 16);
           f32x2 f[C::kEPC / 2];
-          chunk_to_pairs<T>(raw, f);
+          chunk_to_pairs<KV>(raw, f);
 #pragma unroll
           for (int r = 0; r < kRP; ++r)
 #pragma unroll
@@ -389,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
         const ulonglong2 p23 = *reinterpret_cast<const ulonglong2*>(pw + kk * kRP + 2);
         const f32x2 pp[4] = {p01.x, p01.y, p23.x, p23.y};
         f32x2 vf[C::kDPL / 2];
-        load_v_pairs<T, C::kDPL>(vs + kk * C::kRowBytes + lane * C::kDPL * C::kEs, vf);
+        load_v_pairs<KV, C::kDPL>(vs + kk * C::kRowBytes + lane * C::kDPL * C::kKvEs, vf);
 #pragma unroll
         for (int r = 0; r < kRP; ++r)
 #pragma unroll
@@ -434,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
           const int tok = row / p.G, g = row - tok * p.G;
           T* orow =
               reinterpret_cast<T*>(p.out) + ((int64_t)(mt.qstart + tok) * p.Hq + (int64_t)mt.kvh * p.G + g) * D;
-          orow[d] = Elem<T>::to_out(o / lsum);
+          orow[d] = Elem<T>::to_out(o / lsum * p.v_scale);
         } else {
           p.part_acc[(int64_t)(mt.part + r) * D + d] = o;
           if (d == 0) p.part_ml[mt.part + r] = make_float2(M, lsum);
@@ -469,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
             const int tok = row / p.G, gh = row - tok * p.G;
             T* orow =
                 reinterpret_cast<T*>(p.out) + ((int64_t)(mt.qstart + tok) * p.Hq + (int64_t)g.kvh * p.G + gh) * D;
-            orow[d] = Elem<T>::to_out(o / lsum);
+            orow[d] = Elem<T>::to_out(o / lsum * p.v_scale);
           }
         }
       }
@@ -479,9 +516,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
 }
 
 // The dynamic shared-memory opt-in is a per-device function attribute.
-template <typename T, int D>
+template <typename T, typename KV, int D>
 cudaError_t prepare_decode(int* ctas_per_sm) {
-  using C = Cfg<T, D>;
+  using C = Cfg<T, KV, D>;
   static unsigned long long done_mask = 0;  // one bit per device ordinal (< 64)
   static int occupancy[64];
   int dev = 0;
@@ -489,10 +526,10 @@ cudaError_t prepare_decode(int* ctas_per_sm) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-    e = cudaFuncSetAttribute(decode_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    e = cudaFuncSetAttribute(decode_kernel<T, KV, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<T, D>, kThreads, C::kSmem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<T, KV, D>, kThreads, C::kSmem);
     if (e != cudaSuccess) return e;
     occupancy[dev] = occ < 1 ? 1 : occ;
     __atomic_fetch_or(&done_mask, 1ull << dev, __ATOMIC_RELEASE);
@@ -501,36 +538,46 @@ cudaError_t prepare_decode(int* ctas_per_sm) {
   return cudaSuccess;
 }
 
-template <typename T, int D>
+template <typename T, typename KV, int D>
 cudaError_t launch_decode_t(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
                             cudaStream_t s) {
-  using C = Cfg<T, D>;
-  cudaError_t e = prepare_decode<T, D>(nullptr);
+  using C = Cfg<T, KV, D>;
+  cudaError_t e = prepare_decode<T, KV, D>(nullptr);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_kernel<T, D>, dim3(grid), dim3(kThreads), C::kSmem, s, p, kmap, vmap);
+  e = launch_pdl(decode_kernel<T, KV, D>, dim3(grid), dim3(kThreads), C::kSmem, s, p, kmap, vmap);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
+
+using bf16_t = __nv_bfloat16;
+using e4m3_t = __nv_fp8_e4m3;
 
 }  // namespace
 
 cudaError_t decode_ctas_per_sm(bool bf16, int D, int* ctas) {
-  if (bf16) return D == 128 ? prepare_decode<__nv_bfloat16, 128>(ctas) : prepare_decode<__nv_bfloat16, 64>(ctas);
-  return D == 128 ? prepare_decode<float, 128>(ctas) : prepare_decode<float, 64>(ctas);
+  if (bf16) return D == 128 ? prepare_decode<bf16_t, bf16_t, 128>(ctas) : prepare_decode<bf16_t, bf16_t, 64>(ctas);
+  return D == 128 ? prepare_decode<float, float, 128>(ctas) : prepare_decode<float, float, 64>(ctas);
 }
 
+cudaError_t decode_fp8_ctas_per_sm(int* ctas) { return prepare_decode<bf16_t, e4m3_t, 128>(ctas); }
+
 int decode_smem_bytes(int D, int elem_bytes) {
-  if (elem_bytes == 2) return D == 128 ? Cfg<__nv_bfloat16, 128>::kSmem : Cfg<__nv_bfloat16, 64>::kSmem;
-  return D == 128 ? Cfg<float, 128>::kSmem : Cfg<float, 64>::kSmem;
+  if (elem_bytes == 2) return D == 128 ? Cfg<bf16_t, bf16_t, 128>::kSmem : Cfg<bf16_t, bf16_t, 64>::kSmem;
+  return D == 128 ? Cfg<float, float, 128>::kSmem : Cfg<float, float, 64>::kSmem;
 }
 
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, bool bf16, int grid,
                           cudaStream_t s) {
   if (bf16) {
-    return p.D == 128 ? launch_decode_t<__nv_bfloat16, 128>(p, kmap, vmap, grid, s)
-                      : launch_decode_t<__nv_bfloat16, 64>(p, kmap, vmap, grid, s);
+    return p.D == 128 ? launch_decode_t<bf16_t, bf16_t, 128>(p, kmap, vmap, grid, s)
+                      : launch_decode_t<bf16_t, bf16_t, 64>(p, kmap, vmap, grid, s);
   }
-  return p.D == 128 ? launch_decode_t<float, 128>(p, kmap, vmap, grid, s)
-                    : launch_decode_t<float, 64>(p, kmap, vmap, grid, s);
+  return p.D == 128 ? launch_decode_t<float, float, 128>(p, kmap, vmap, grid, s)
+                    : launch_decode_t<float, float, 64>(p, kmap, vmap, grid, s);
+}
+
+cudaError_t launch_decode_fp8(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
+                              cudaStream_t s) {
+  return launch_decode_t<bf16_t, e4m3_t, 128>(p, kmap, vmap, grid, s);
 }
 
 }  // namespace pkv

@@ -135,7 +135,8 @@ struct AttnParams {
   int* tickets;      // arrivals per merge group
   int Hq, Hkv, G, D, bs, max_blocks;
   int64_t num_blocks;
-  float scale_log2;  // scale * log2(e)
+  float scale_log2;  // scale * log2(e) (times the K scale for an FP8 cache)
+  float v_scale;     // output factor: the V scale for an FP8 cache, else 1
   int causal;
   int out_al32;      // out is 32-byte aligned (256-bit stores)
   // The decode kernel launches beside the tensor-core kernel, after every
@@ -169,6 +170,14 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slots, void* kc, void* vc,
                             int64_t T, int64_t num_slots, int row_elems, int elem_bytes,
                             int64_t k_stride, int64_t v_stride, int* err, cudaStream_t s);
+// FP8 (E4M3) cache: the quantising write (rows of bf16 or fp32, es bytes per
+// element) and the CUDA-core decode kernel for bf16 q with head_dim 128
+cudaError_t launch_kv_write_fp8(const void* k, const void* v, const int64_t* slots, void* kc, void* vc, int64_t T,
+                                int64_t num_slots, int row_elems, int es, int64_t k_stride, int64_t v_stride,
+                                float k_scale, float v_scale, int* err, cudaStream_t s);
+cudaError_t launch_decode_fp8(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
+                              cudaStream_t s);
+cudaError_t decode_fp8_ctas_per_sm(int* ctas);
 cudaError_t launch_planner(const PlanParams& p, cudaStream_t s);
 // shared-prefix search for the planner (before it, on the same stream)
 cudaError_t launch_prefix_search(const PlanParams& p, cudaStream_t s);
