@@ -68,3 +68,23 @@ def test_host_checks_need_no_gpu(lib):
     assert lib.paged_kv_write(None, None, None, None, None, 3, 4, 16, 4, 128, 100, 0, 1, None) == 1
     # null pointers with work to do
     assert lib.paged_kv_write(None, None, None, None, None, 3, 4, 16, 4, 128, 0, 0, 1, None) == 1
+
+
+def test_fp8_host_checks_need_no_gpu(lib):
+    import ctypes as C
+    f = C.c_float
+    # FP8 attention: scales must be positive, head_dim 128 only
+    st = lib.paged_attention_forward_fp8kv(None, None, None, None, None, None, None, 1, 1, 8, 4, 128, 4, 16, 1, 0,
+                                           f(0.1), 1, f(0.0), f(1.0), 0, None, 0, None)
+    assert st == 1 and b"scale" in lib.pkv_last_error()
+    st = lib.paged_attention_forward_fp8kv(None, None, None, None, None, None, None, 1, 1, 8, 4, 64, 4, 16, 1, 0,
+                                           f(0.1), 1, f(1.0), f(1.0), 0, None, 0, None)
+    assert st == 2 and b"head_dim" in lib.pkv_last_error()
+    # an empty batch is a no-op
+    assert lib.paged_attention_forward_fp8kv(None, None, None, None, None, None, None, 0, 0, 8, 4, 128, 4, 16, 1, 0,
+                                             f(0.1), 1, f(1.0), f(1.0), 0, None, 0, None) == 0
+    # FP8 write: scales, row multiple of 16, source dtype
+    assert lib.paged_kv_write_fp8(None, None, None, None, None, 3, 4, 16, 4, 128, 0, 0, 1, f(-1.0), f(1.0), None) == 1
+    assert lib.paged_kv_write_fp8(None, None, None, None, None, 3, 4, 16, 1, 8, 0, 0, 1, f(1.0), f(1.0), None) == 2
+    assert lib.paged_kv_write_fp8(None, None, None, None, None, 3, 4, 16, 4, 128, 0, 0, 2, f(1.0), f(1.0), None) == 2
+    assert lib.paged_kv_write_fp8(None, None, None, None, None, 0, 4, 16, 4, 128, 0, 0, 1, f(1.0), f(1.0), None) == 0
