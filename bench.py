@@ -546,11 +546,12 @@ def run_reference(args):
 # workload runs); reported as null once those sources change.  The captures
 # and their commands are summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": ("50f7603394c6a898", 613111808 + 4718336),        # dectc_kernel<4>, decode batch
-    "prefill": ("73b1c3cd24fdc664", 81036544 + 9203712),        # mma_attn_kernel, prefill chunks
-    "specverify": ("73b1c3cd24fdc664", 1076745472 + 13745920),  # mma_attn_kernel, spec-verify
-    "prefix": ("e924c785b8c3e31b", 10558549 + 648700138 + 1369152),  # mma_attn_kernel + dectc_kernel<4>
-    "prefix-long": ("50f7603394c6a898", 2116707584 + 4223232),  # dectc_kernel<4>, long-context prefix-shared
+    "decode": ("1adb8e998b5a55d2", 613144320 + 4362496),  # dectc_kernel<4>, decode batch
+    "prefill": ("8e3322af5452efde", 80956160 + 7931136),  # mma_attn_kernel, prefill chunks
+    "specverify": ("8e3322af5452efde", 1076848896 + 13777664),  # mma_attn_kernel, spec-verify
+    "prefix": ("e4fd585a2c78aab2", 10567680 + 0 + 648704000 + 1501952),  # mma_attn_kernel + dectc_kernel<4>
+    "prefix-long": ("1adb8e998b5a55d2", 2116702464 + 4256256),  # dectc_kernel<4>, long-context prefix-shared
+    "decode-fp8": ("d9642064cc5de4e1", 307352576 + 4703232),  # decode_kernel<bf16, e4m3>, decode batch with FP8 pools
 }
 
 
