@@ -299,8 +299,11 @@ class BlockManager:
 
     def __del__(self):
         h = getattr(self, "_h", None)
-        if h is not None and h.value:
-            lib().pkv_bm_destroy(h)
+        if h is not None and h.value and _lib is not None:
+            try:
+                _lib.pkv_bm_destroy(h)
+            except Exception:  # interpreter shutdown: the library may be gone already
+                pass
             self._h = None
 
     def update(self, seq: int, n: int):
