@@ -120,7 +120,7 @@ def launches_per_step(w, max_q_len: int, shared_prefix: bool, fp8: bool = False)
     """Our kernels per step, as paged_attention_forward chooses them: the K/V
     write, [the shared-prefix search], the planner, [the tensor-core kernel],
     the decode-shaped kernel (split merges run inside the attention kernels).
-    FP8 pools: the write, the planner and the CUDA-core kernel."""
+    FP8 pools: the write, the planner and one decode kernel."""
     if fp8:
         return 3
     g = w.num_q_heads // w.num_kv_heads
@@ -309,7 +309,8 @@ def run_gpu(args, rank, world, local_rank):
         # decode_kernel serves the other shapes)
         kname = "mma_attn_kernel (tcgen05)" if args.workload == "specverify" else (
             "mma_attn_kernel + dectc_kernel" if args.workload == "mixed" else
-            "decode_kernel (CUDA cores, FP8 E4M3 K/V)" if fp8 else "dectc_kernel (tcgen05 decode)")
+            "dectc_kernel (tcgen05 decode, fp16 MMAs on E4M3 tiles converted in shared memory)" if fp8 else
+            "dectc_kernel (tcgen05 decode)")
         roof = {"bound": "hbm", "kernel": kname + ", attention kernels per launch", "achieved": round(achieved, 1),
                 "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                 "peak_kind": peak_kind + " HBM copy", "traffic": ncu_traffic(args.workload),
@@ -546,12 +547,12 @@ def run_reference(args):
 # workload runs); reported as null once those sources change.  The captures
 # and their commands are summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": ("1adb8e998b5a55d2", 613144320 + 4362496),  # dectc_kernel<4>, decode batch
-    "prefill": ("8e3322af5452efde", 80956160 + 7931136),  # mma_attn_kernel, prefill chunks
-    "specverify": ("8e3322af5452efde", 1076848896 + 13777664),  # mma_attn_kernel, spec-verify
-    "prefix": ("e4fd585a2c78aab2", 10567680 + 0 + 648704000 + 1501952),  # mma_attn_kernel + dectc_kernel<4>
-    "prefix-long": ("1adb8e998b5a55d2", 2116702464 + 4256256),  # dectc_kernel<4>, long-context prefix-shared
-    "decode-fp8": ("d9642064cc5de4e1", 307352576 + 4703232),  # decode_kernel<bf16, e4m3>, decode batch with FP8 pools
+    "decode": ("1df0dd060c35cc39", 613120000 + 4368640),  # dectc_kernel<4>, decode batch
+    "prefill": ("cecd99cff8111ed8", 81004800 + 8169728),  # mma_attn_kernel, prefill chunks
+    "specverify": ("cecd99cff8111ed8", 1076760576 + 13708288),  # mma_attn_kernel, spec-verify
+    "prefix": ("ffe453f953418479", 10567680 + 0 + 648741632 + 1411328),  # mma_attn_kernel + dectc_kernel<4>
+    "prefix-long": ("1df0dd060c35cc39", 2116710912 + 4214784),  # dectc_kernel<4>, long-context prefix-shared
+    "decode-fp8": ("1df0dd060c35cc39", 309542656 + 4083712),  # dectc_kernel<4, FP8>, decode batch with FP8 pools
 }
 
 
@@ -585,7 +586,7 @@ def _code_only(text: str) -> str:
 FORWARD_SOURCES = ("api.cu", "kv_write.cu", "planner.cu", "static_ws.cu", "pkv_device.cuh", "pkv_tc.cuh",
                    "pkv_internal.h")
 WORKLOAD_KERNELS = {"decode": ("decode.cu", "dectc.cu"), "prefix-long": ("decode.cu", "dectc.cu"),
-                    "decode-fp8": ("decode.cu",),
+                    "decode-fp8": ("decode.cu", "dectc.cu"),
                     "prefill": ("mma_attn.cu",), "specverify": ("mma_attn.cu",),
                     "prefix": ("decode.cu", "dectc.cu", "mma_attn.cu")}
 

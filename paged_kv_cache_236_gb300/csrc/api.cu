@@ -353,7 +353,11 @@ static pkv_status forward_impl(const void* q, const void* k_cache, const void* v
   const bool mma_ok = !kv_fp8 && bf16 && D == 128 && (G & (G - 1)) == 0 && G <= 128;
   // decode-shaped rows: tensor-core kernel (keys on M, rows on N) for bf16,
   // head_dim 128 and G dividing 16; the CUDA-core kernel otherwise
-  const bool dectc = mma_ok && G <= kTcDecRows;
+  // FP8 pools: the same kernel on fp16 MMAs over converted tiles when the
+  // host hint bounds every sequence's rows by 8, the CUDA-core kernel otherwise
+  const bool f8tc = kv_fp8 && D == 128 && (G & (G - 1)) == 0 && max_query_len > 0 &&
+                    (int64_t)max_query_len * G <= 8;
+  const bool dectc = (mma_ok && G <= kTcDecRows) || f8tc;
   const int dec_rows_max = dectc ? kTcDecRows : kDecRows;
   // rows of softmax per key in that kernel: a power of two >= G (so items hold
   // whole tokens) covering the hinted query length; 16 when there is no hint
@@ -364,7 +368,7 @@ static pkv_status forward_impl(const void* q, const void* k_cache, const void* v
   }
   // shared prefixes are read once per group by the tensor-core kernel, and
   // the rest of each member's keys by the tensor-core decode kernel
-  const bool cascade = (hints & PKV_HINT_SHARED_PREFIX) != 0 && dectc;
+  const bool cascade = (hints & PKV_HINT_SHARED_PREFIX) != 0 && dectc && !kv_fp8;
   // with a host hint that no sequence has more rows than that, skip the launch
   const bool mma_launch =
       mma_ok && (cascade || !(max_query_len > 0 && (int64_t)max_query_len * G <= dec_rows_max));
@@ -478,7 +482,13 @@ static pkv_status forward_impl(const void* q, const void* k_cache, const void* v
   ap.counter = &header->dec_counter;
   ap.items = dec_items;
   ap.no_wait = side_by_side ? 1 : 0;
-  if (dectc) {
+  if (dectc && kv_fp8) {
+    CUtensorMap qmap16;
+    if ((st = encode_q_map(&qmap16, q, T, Hq, D, 64, G, kTcDecRows / G)) != PKV_OK) return st;
+    // kmap / vmap (uint8, one {128, 1, bs, 1} box of codes per block) were encoded above
+    if ((e = launch_dectc_fp8(ap, tc_rows, qmap16, kmap, vmap, dev->sms, s)) != cudaSuccess)
+      return cuda_fail(e, "decode (tensor-core, FP8) launch");
+  } else if (dectc) {
     CUtensorMap qmap16, kmap_sw, vmap_sw;
     if ((st = encode_q_map(&qmap16, q, T, Hq, D, 64, G, kTcDecRows / G)) != PKV_OK) return st;
     if ((st = encode_pool_map(&kmap_sw, k_cache, dtype, num_blocks, bs, Hkv, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) !=

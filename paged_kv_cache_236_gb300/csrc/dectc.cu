@@ -40,10 +40,22 @@
 // Shared memory: 3 stages of K+V (192 KB), 2 Q tiles and 2 P tiles (4 KB
 // each).  TMEM: S^T double-buffered in columns [0,32), O^T in [32,48).
 //
+// FP8 pools (E4M3 codes, one scale per pool), items of up to 8 rows: 512
+// threads.  The producers load each tile's codes (one {128, 1, block_size,
+// 1} box per block, 16 KB of K and 16 KB of V) into a 2-slot staging ring and
+// run ahead of the MMAs; warps 12-15 convert a staged tile into the fp16 tile
+// the MMAs read (E4M3 -> fp16 is exact, one instruction per two codes; the
+// same 128-byte swizzle), and an item's Q tile from bf16 to fp16 in place.
+// The MMAs then run on fp16 A and B; P is written as fp16.  Two fp16 stages,
+// 4 Q tiles and 4 metadata slots (the producers are up to two tiles ahead).
+// The K scale is in the logit scale, the V scale multiplies the output.
+//
 // An unsplit item after a shared prefix (part < 0, merge group >= 0) folds
 // the prefix's partial rows, written by the tensor-core kernel before this
 // one ran, into its own rows in the epilogue; a split one leaves that to its
 // group's merge, which folds in the splits and the prefix partials alike.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math_constants.h>
 
 #include "pkv_device.cuh"
@@ -53,22 +65,39 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int kStages = 3;
+constexpr int kMaxStages = 3;
 constexpr int kKeys = kMmaTileKeys;            // 128 keys per tile
 constexpr int kN = kTcDecRows;                 // 16 rows (MMA N)
 constexpr int kTileBytes = kKeys * 128 * 2;    // one of K or V: 32 KB
 constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kCodeTile = kKeys * 128;         // one of K or V as E4M3 codes: 16 KB
 constexpr int kQHalf = kN * 128;               // one 64-column half of the Q / P tiles (2 KB)
-constexpr int kQOff = kStages * kStageBytes;
-constexpr int kPOff = kQOff + 2 * 2 * kQHalf;
-constexpr int kMetaOff = kPOff + 2 * 2 * kQHalf;
-constexpr int kRedOff = kMetaOff + kStages * 64;
-constexpr int kSlotOff = kRedOff + 2 * 4 * kN * 4;
-constexpr int kISlotOff = kSlotOff + 2 * 256;  // 2 item slots
-constexpr int kBarOff = kISlotOff + 2 * 192;
-constexpr int kNumBars = 3 * kStages + 2 * 8 + 4;
-constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
+constexpr int kNumBars = 5 * kMaxStages + 2 * 8 + 4 + 2;
+
+// Shared-memory layout.  bf16 pools: 3 stages of K+V.  FP8 pools: 2 stages
+// of fp16 K+V (what the MMAs read) and 2 stages of staged codes (what TMA
+// writes), and 4 more warps that convert the one into the other.
+template <bool F8>
+struct Lay {
+  static constexpr int kThreads = F8 ? 512 : 384;
+  static constexpr int kStages = F8 ? 2 : 3;
+  // FP8: the producers run ahead of the fp16 stages on the staging ring, so
+  // tile metadata and Q tiles live in 4 slots (a slot is rewritten only
+  // after every reader of its previous tile is done with it)
+  static constexpr int kMetaSlots = F8 ? 4 : kStages;
+  static constexpr int kQBufs = F8 ? 4 : 2;
+  static constexpr int kQOff = kStages * kStageBytes;
+  static constexpr int kPOff = kQOff + kQBufs * 2 * kQHalf;
+  static constexpr int kMetaOff = kPOff + 2 * 2 * kQHalf;
+  static constexpr int kRedOff = kMetaOff + kMetaSlots * 64;
+  static constexpr int kSlotOff = kRedOff + 2 * 4 * kN * 4;
+  static constexpr int kISlotOff = kSlotOff + 2 * 256;  // 2 item slots
+  static constexpr int kStgOff = (kISlotOff + 2 * 192 + 1023) & ~1023;
+  static constexpr int kStgBytes = F8 ? kStages * 2 * kCodeTile : 0;
+  static constexpr int kBarOff = F8 ? kStgOff + kStgBytes : kISlotOff + 2 * 192;
+  static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
+};
+static_assert(Lay<true>::kSmem <= 232448 && Lay<false>::kSmem <= 232448, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 64;
 constexpr uint32_t kSCol = 0, kOCol = 32;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -76,6 +105,9 @@ constexpr int kMetaDone = 2, kMetaLast = 1, kMetaFirst = 4;
 
 constexpr uint32_t kIdescS = idesc_bf16(128, kN, false, false);
 constexpr uint32_t kIdescO = idesc_bf16(128, kN, true, false);
+// fp16 A and B (FP8 pools decode to fp16 exactly): the format fields are 0
+constexpr uint32_t kIdescS16 = kIdescS & ~((7u << 7) | (7u << 10));
+constexpr uint32_t kIdescO16 = kIdescO & ~((7u << 7) | (7u << 10));
 
 struct alignas(16) Meta {
   int item, kbase, flags, seq;
@@ -86,10 +118,12 @@ struct alignas(16) Meta {
 static_assert(sizeof(Meta) == 64, "meta slot");
 
 struct Bars {
-  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
+  uint64_t kc_full[kMaxStages], vc_full[kMaxStages];  // FP8: fp16 K / V of the stage converted
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t o_full[2], o_empty[2], ml_full[2], ml_empty[2];
   uint64_t islot_full[2], islot_free[2];
+  uint64_t stage_empty[2];  // FP8: a staging slot's codes converted (the producers may refill it)
 };
 
 // An item as the item-fetch warp hands it to the producer.
@@ -172,25 +206,73 @@ struct AddOp {
   __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
 };
 
+// Two E4M3 codes (low byte first) as an fp16 pair, exactly (every E4M3
+// value is an fp16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// One tile of codes (128 keys x 128 bytes, row-major) as the fp16 tile the
+// MMAs read: two 64-column halves kHalf apart, key r's 16-byte chunk j at
+// chunk j ^ (r & 7) of its 128-byte row (the 128-byte swizzle).  Thread c of
+// the 128 converter threads takes 16-code chunks c, c + 128, ...
+__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int c) {
+#pragma unroll 2
+  for (int u = c; u < kKeys * 8; u += 128) {
+    const int key = u >> 3, ch = u & 7;
+    const uint4 raw = *reinterpret_cast<const uint4*>(src + key * 128 + ch * 16);
+    const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[2 * i] = e4m3x2_to_f16x2(in[i] & 0xFFFFu);
+      w[2 * i + 1] = e4m3x2_to_f16x2(in[i] >> 16);
+    }
+    uint8_t* row = dst + (ch >> 2) * kHalf + key * 128;
+    const int j0 = (ch & 3) * 2;
+    *reinterpret_cast<uint4*>(row + ((j0 ^ (key & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(row + (((j0 + 1) ^ (key & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// Eight bf16 values as eight fp16 values (round to nearest; magnitudes above
+// 65504 become infinite).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h = __floats2half2_rn(__uint_as_float(in[i] << 16), __uint_as_float(in[i] & 0xFFFF0000u));
+    out[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 // NR: rows per item (4, 8 or 16; the MMA's N stays 16, extra columns unused).
-template <int NR>
-__global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
+// F8: the pools hold E4M3 codes (q bf16): staged codes are converted to fp16
+// tiles and the MMAs run on fp16 operands.
+template <int NR, bool F8>
+__global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnParams p,
                                                             const __grid_constant__ CUtensorMap qmap,
                                                             const __grid_constant__ CUtensorMap kmap,
                                                             const __grid_constant__ CUtensorMap vmap) {
+  using Y = Lay<F8>;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNumBars * 8);
-  Meta* meta = reinterpret_cast<Meta*>(smem + kMetaOff);
-  float* red = reinterpret_cast<float*>(smem + kRedOff);  // [2][4 warps][NR rows]
+  Bars* bars = reinterpret_cast<Bars*>(smem + Y::kBarOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Y::kBarOff + kNumBars * 8);
+  Meta* meta = reinterpret_cast<Meta*>(smem + Y::kMetaOff);
+  float* red = reinterpret_cast<float*>(smem + Y::kRedOff);  // [2][4 warps][NR rows]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < Y::kStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->kc_full[s], 128);  // the 128 converter threads (FP8)
+      mbar_init(&bars->vc_full[s], 128);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
@@ -205,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
       mbar_init(&bars->ml_empty[b], 128);
       mbar_init(&bars->islot_full[b], 32);
       mbar_init(&bars->islot_free[b], 2);  // both producers read the slot
+      mbar_init(&bars->stage_empty[b], 128);
     }
     fence_mbar_init();
   }
@@ -236,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
       }
     }
     const int nb_per_tile = kKeys / p.bs;
-    const ItemSlot* islots = reinterpret_cast<const ItemSlot*>(smem + kISlotOff);
+    const ItemSlot* islots = reinterpret_cast<const ItemSlot*>(smem + Y::kISlotOff);
     int g = 0;
     for (int it_cnt = 0;; ++it_cnt) {
       const int qb = it_cnt & 1;
@@ -250,11 +333,14 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
       if (lane == 0) mbar_arrive(&bars->islot_free[qb]);
       if (done) {
         if (vprod) break;
-        const int st = g % kStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->kv_empty[st], ((g / kStages) & 1) ^ 1, p.err))) break;
+        const int st = g % Y::kStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(F8 ? &bars->stage_empty[st] : &bars->kv_empty[st],
+                                               ((g / Y::kStages) & 1) ^ 1, p.err)))
+          break;
+        const int mi = F8 ? (g & 3) : st;
         if (lane == 0) {
-          meta[st].item = -1;
-          meta[st].flags = kMetaDone;
+          meta[mi].item = -1;
+          meta[mi].flags = kMetaDone;
           mbar_arrive(&bars->k_full[st]);
         }
         break;
@@ -275,28 +361,39 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
       };
       bool ok = true;
       for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
-        const int st = g % kStages;
+        const int st = g % Y::kStages;
         const bool first = kbase == it.kb;
         const int next_phys = (kbase + kKeys < it.ke) ? block_of(kbase + kKeys) : 0;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->kv_empty[st], ((g / kStages) & 1) ^ 1, p.err))) {
+        // bf16: the stage's K/V tiles are free once its last P.V is done.
+        // FP8: the staging slot is free once its codes are converted.
+        if (!__all_sync(0xffffffffu, mbar_wait(F8 ? &bars->stage_empty[st] : &bars->kv_empty[st],
+                                               ((g / Y::kStages) & 1) ^ 1, p.err))) {
           ok = false;
           break;
         }
         uint8_t* kd = smem + st * kStageBytes;
         uint8_t* vd = kd + kTileBytes;
+        // FP8: the codes of K and V land in the staging area (one 128-byte
+        // row per key, one box per block); the converter warps fill kd / vd
+        uint8_t* kc8 = smem + Y::kStgOff + st * 2 * kCodeTile;
+        uint8_t* vc8 = kc8 + kCodeTile;
         if (vprod) {
-          if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
+          if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[st], F8 ? kCodeTile : kTileBytes);
           __syncwarp();
           if (lane < nb_per_tile) {
             const int row_off = lane * p.bs * 128;
-            tma_load_4d(vd + row_off, &vmap, &bars->v_full[st], 0, it.kvh, 0, phys);
-            tma_load_4d(vd + kHalf + row_off, &vmap, &bars->v_full[st], 64, it.kvh, 0, phys);
+            if constexpr (F8) {
+              tma_load_4d(vc8 + row_off, &vmap, &bars->v_full[st], 0, it.kvh, 0, phys);
+            } else {
+              tma_load_4d(vd + row_off, &vmap, &bars->v_full[st], 0, it.kvh, 0, phys);
+              tma_load_4d(vd + kHalf + row_off, &vmap, &bars->v_full[st], 64, it.kvh, 0, phys);
+            }
           }
           phys = next_phys;
           continue;
         }
         if (lane == 0) {
-          Meta& m = meta[st];
+          Meta& m = meta[F8 ? (g & 3) : st];
           m.item = idx;
           m.kbase = kbase;
           m.flags = ((kbase + kKeys >= it.ke) ? kMetaLast : 0) | (first ? kMetaFirst : 0);
@@ -310,10 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
           m.L = L;
           m.n = n;
           m.qstart = qstart;
-          mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes + (first ? 2 * kQHalf : 0));
+          mbar_arrive_expect_tx(&bars->k_full[st], (F8 ? kCodeTile : kTileBytes) + (first ? 2 * kQHalf : 0));
           if (first) {
             // this item's Q rows: tokens row0/G .. of the item, G heads each
-            uint8_t* qd = smem + kQOff + (it_cnt & 1) * 2 * kQHalf;
+            uint8_t* qd = smem + Y::kQOff + (it_cnt & (Y::kQBufs - 1)) * 2 * kQHalf;
             const int tok0 = qstart + it.row0 / p.G;
             tma_load_3d(qd, &qmap, &bars->k_full[st], 0, it.kvh * p.G, tok0);
             tma_load_3d(qd + kQHalf, &qmap, &bars->k_full[st], 64, it.kvh * p.G, tok0);
@@ -322,8 +419,12 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
         __syncwarp();
         if (lane < nb_per_tile) {
           const int row_off = lane * p.bs * 128;
-          tma_load_4d(kd + row_off, &kmap, &bars->k_full[st], 0, it.kvh, 0, phys);
-          tma_load_4d(kd + kHalf + row_off, &kmap, &bars->k_full[st], 64, it.kvh, 0, phys);
+          if constexpr (F8) {
+            tma_load_4d(kc8 + row_off, &kmap, &bars->k_full[st], 0, it.kvh, 0, phys);
+          } else {
+            tma_load_4d(kd + row_off, &kmap, &bars->k_full[st], 0, it.kvh, 0, phys);
+            tma_load_4d(kd + kHalf + row_off, &kmap, &bars->k_full[st], 64, it.kvh, 0, phys);
+          }
         }
         phys = next_phys;
       }
@@ -332,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
   } else if (warp == 10) {
     // ================================================================ item fetch
     const int nb_per_tile = kKeys / p.bs;
-    ItemSlot* islots = reinterpret_cast<ItemSlot*>(smem + kISlotOff);
+    ItemSlot* islots = reinterpret_cast<ItemSlot*>(smem + Y::kISlotOff);
     for (int c = 0;; ++c) {
       const int qb = c & 1;
       // Item c is taken from the queue once the producers have taken item
@@ -390,24 +491,24 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
       // descriptors of stage 0 / buffer 0; others are offsets of these
       const uint64_t dk0 = desc_k(smem_base);
       const uint64_t dv0 = desc_mn(smem_base + kTileBytes);
-      const uint64_t dq0 = desc_k(smem_base + kQOff);
-      const uint64_t dp0 = desc_k(smem_base + kPOff);
+      const uint64_t dq0 = desc_k(smem_base + Y::kQOff);
+      const uint64_t dp0 = desc_k(smem_base + Y::kPOff);
       bool pend_first = false, pend_last = false;
       auto issue_pv = [&]() -> bool {
-        const int b = pend & 1, st = pend % kStages, ob = pend_item & 1;
+        const int b = pend & 1, st = pend % Y::kStages, ob = pend_item & 1;
         if (pend_first) {
           // O^T[ob] is about to be overwritten: the epilogue of item pend_item-2 must have read it
           if (!mbar_wait(&bars->o_empty[ob], ((pend_item >> 1) & 1) ^ 1, p.err)) return false;
         }
         if (!mbar_wait(&bars->p_full[b], (pend >> 1) & 1, p.err)) return false;
-        if (!mbar_wait(&bars->v_full[st], (pend / kStages) & 1, p.err)) return false;
+        if (!mbar_wait(F8 ? &bars->vc_full[st] : &bars->v_full[st], (pend / Y::kStages) & 1, p.err)) return false;
         tc_fence_after();
         const uint64_t dv = desc_add(dv0, st * kStageBytes);
         const uint64_t dp = desc_add(dp0, b * 2 * kQHalf);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
           umma_bf16(tmem + kOCol + ob * kN, desc_add(dv, kk * 2048), desc_add(dp, (kk >> 2) * kQHalf + (kk & 3) * 32),
-                    kIdescO, (pend_first && kk == 0) ? 0u : 1u);
+                    F8 ? kIdescO16 : kIdescO, (pend_first && kk == 0) ? 0u : 1u);
         umma_commit(&bars->pv_done[b]);
         umma_commit(&bars->kv_empty[st]);
         if (pend_last) umma_commit(&bars->o_full[ob]);
@@ -415,9 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
         return true;
       };
       for (;; ++g) {
-        const int st = g % kStages;
-        if (!mbar_wait(&bars->k_full[st], (g / kStages) & 1, p.err)) break;
-        const int flags = meta[st].flags;
+        const int st = g % Y::kStages;
+        if (!mbar_wait(F8 ? &bars->kc_full[st] : &bars->k_full[st], (g / Y::kStages) & 1, p.err)) break;
+        const int flags = meta[F8 ? (g & 3) : st].flags;
         if (flags & kMetaDone) {
           if (pend >= 0) issue_pv();
           break;
@@ -427,11 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
         if (!mbar_wait(&bars->s_free[b], ((g >> 1) & 1) ^ 1, p.err)) break;
         tc_fence_after();
         const uint64_t dk = desc_add(dk0, st * kStageBytes);
-        const uint64_t dq = desc_add(dq0, (it_cnt & 1) * 2 * kQHalf);
+        const uint64_t dq = desc_add(dq0, (it_cnt & (Y::kQBufs - 1)) * 2 * kQHalf);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk)
           umma_bf16(tmem + kSCol + b * kN, desc_add(dk, (kk >> 2) * kHalf + (kk & 3) * 32),
-                    desc_add(dq, (kk >> 2) * kQHalf + (kk & 3) * 32), kIdescS, kk > 0 ? 1u : 0u);
+                    desc_add(dq, (kk >> 2) * kQHalf + (kk & 3) * 32), F8 ? kIdescS16 : kIdescS, kk > 0 ? 1u : 0u);
         umma_commit(&bars->s_full[b]);
         if (pend >= 0 && !issue_pv()) break;
         pend = g;
@@ -441,13 +542,50 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
       }
     }
     __syncwarp();
+  } else if (warp >= 12) {
+    // ================================================================ FP8 converters (warps 12-15)
+    // Per stage: the staged K codes (and, on an item's first tile, its Q
+    // tile, bf16 -> fp16 in place) become the fp16 K tile, then kc_full;
+    // the staged V codes become the fp16 V tile, then vc_full.  The stage's
+    // fp16 tiles are free: its producer waited for kv_empty before loading.
+    if constexpr (F8) {
+      const int c = threadIdx.x - 384;
+      int it_cnt = -1;
+      for (int g = 0;; ++g) {
+        const int st = g % Y::kStages;
+        const uint32_t ph = (g / Y::kStages) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_full[st], ph, p.err))) break;
+        const int flags = meta[g & 3].flags;
+        if (flags & kMetaDone) {
+          mbar_arrive(&bars->kc_full[st]);  // the MMA and softmax warps see the end
+          break;
+        }
+        // the stage's fp16 tiles are free once the P.V of its previous tile is done
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->kv_empty[st], ph ^ 1, p.err))) break;
+        const uint8_t* codes = smem + Y::kStgOff + st * 2 * kCodeTile;
+        uint8_t* kd = smem + st * kStageBytes;
+        convert_tile(codes, kd, c);
+        if (flags & kMetaFirst) {
+          ++it_cnt;
+          uint4* q = reinterpret_cast<uint4*>(smem + Y::kQOff + (it_cnt & (Y::kQBufs - 1)) * 2 * kQHalf);
+          for (int i = c; i < 2 * kQHalf / 16; i += 128) q[i] = bf16x8_to_f16x8(q[i]);
+        }
+        fence_proxy_async_smem();  // generic-proxy writes, read by the tensor core
+        mbar_arrive(&bars->kc_full[st]);
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], ph, p.err))) break;
+        convert_tile(codes + kCodeTile, kd + kTileBytes, c);
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->vc_full[st]);
+        mbar_arrive(&bars->stage_empty[st]);  // both code tiles of the slot read
+      }
+    }
   } else {
     // ================================================================ softmax / epilogue
     constexpr int kLog = NR == 4 ? 2 : NR == 8 ? 3 : 4;
     const int q4 = warp & 3;
     const int t = q4 * 32 + lane;  // key of the tile (S^T lane) / output column (O^T lane)
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
-    EpSlot* slots = reinterpret_cast<EpSlot*>(smem + kSlotOff);
+    EpSlot* slots = reinterpret_cast<EpSlot*>(smem + Y::kSlotOff);
     if (warp < 6) {
       // ---------------------------------------------------------- softmax
       const int my_row = lane >> (5 - kLog);  // row this lane holds after a reduction
@@ -457,9 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
       Meta mt;
       int g = 0, it_cnt = -1;
       for (;; ++g) {
-        const int st = g % kStages;
-        if (!wait_all(&bars->k_full[st], (g / kStages) & 1, p.err)) break;
-        const int flags = meta[st].flags;
+        const int st = g % Y::kStages;
+        if (!wait_all(F8 ? &bars->kc_full[st] : &bars->k_full[st], (g / Y::kStages) & 1, p.err)) break;
+        const int mi = F8 ? (g & 3) : st;
+        const int flags = meta[mi].flags;
         if (flags & kMetaDone) {
           // tell the epilogue warps there are no more items
           const int ob = (it_cnt + 1) & 1;
@@ -470,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
           break;
         }
         if (flags & kMetaFirst) {
-          mt = meta[st];
+          mt = meta[mi];
           ++it_cnt;
 #pragma unroll
           for (int r = 0; r < NR; ++r) {
@@ -480,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
             vis[r] = r < mt.nrows ? min(mt.ke, p.causal ? mt.L - mt.n + tok + 1 : mt.L) : 0;
           }
         }
-        const int kbase = meta[st].kbase;
+        const int kbase = meta[mi].kbase;
         const int b = g & 1;
         float* redb = red + b * 4 * NR;  // [4 warps][NR], double-buffered by tile
         if (!wait_all(&bars->s_full[b], (g >> 1) & 1, p.err)) break;
@@ -520,14 +659,17 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
 
         // ---- P (bf16) into this tile's P buffer: row r, column t, 128-byte swizzle
         if (!wait_all(&bars->pv_done[b], ((g >> 1) & 1) ^ 1, p.err)) break;  // P.V of tile g-2 is done
-        uint8_t* pbuf = smem + kPOff + b * 2 * kQHalf + (t >> 6) * kQHalf;
+        uint8_t* pbuf = smem + Y::kPOff + b * 2 * kQHalf + (t >> 6) * kQHalf;
         const int pchunk = (t & 63) >> 3, pbyte = (t & 7) * 2;
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
           const float e = fast_exp2(fmaf(v[r], p.scale_log2, -m_use[r]));
           lsum[r] = fmaf(lsum[r], alpha[r], e);
-          *reinterpret_cast<__nv_bfloat16*>(pbuf + r * 128 + ((pchunk ^ (r & 7)) << 4) + pbyte) =
-              __float2bfloat16_rn(e);
+          if constexpr (F8)
+            *reinterpret_cast<__half*>(pbuf + r * 128 + ((pchunk ^ (r & 7)) << 4) + pbyte) = __float2half_rn(e);
+          else
+            *reinterpret_cast<__nv_bfloat16*>(pbuf + r * 128 + ((pchunk ^ (r & 7)) << 4) + pbyte) =
+                __float2bfloat16_rn(e);
         }
         if (any_rescale) {
           // O^T must hold every earlier tile's P.V before it is scaled; thread t
@@ -546,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
         if (kbase + kKeys > mt.L) {
           // keys at or past the sequence's end hold arbitrary bits: zero their V
           // rows (after the tile has landed) so that 0 * V stays 0
-          if (!wait_all(&bars->v_full[st], (g / kStages) & 1, p.err)) break;
+          if (!wait_all(F8 ? &bars->vc_full[st] : &bars->v_full[st], (g / Y::kStages) & 1, p.err)) break;
           if (key >= mt.L) {
             uint4* v0 = reinterpret_cast<uint4*>(smem + st * kStageBytes + kTileBytes + t * 128);
             uint4* v1 = reinterpret_cast<uint4*>(smem + st * kStageBytes + kTileBytes + kHalf + t * 128);
@@ -645,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
               const int tok = row / p.G, gh = row - tok * p.G;
               __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
                                     ((int64_t)(mt.qstart + tok) * p.Hq + (int64_t)mt.kvh * p.G + gh) * 128;
-              orow[d] = __float2bfloat16_rn(acc / lt);
+              orow[d] = __float2bfloat16_rn(acc / lt * p.v_scale);
             }
           }
           continue;
@@ -698,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
               const int tok = row / p.G, gh = row - tok * p.G;
               __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
                                     ((int64_t)(mt.qstart + tok) * p.Hq + (int64_t)gr.kvh * p.G + gh) * 128;
-              orow[d] = __float2bfloat16_rn(acc / lt);
+              orow[d] = __float2bfloat16_rn(acc / lt * p.v_scale);
             }
           }
         }
@@ -713,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1) dectc_kernel(const AttnParams p,
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int NR>
+template <int NR, bool F8>
 cudaError_t launch_dectc_t(const AttnParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, int grid, cudaStream_t s) {
   static unsigned long long done_mask = 0;
@@ -722,11 +864,12 @@ cudaError_t launch_dectc_t(const AttnParams& p, const CUtensorMap& qmap, const C
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-    e = cudaFuncSetAttribute(dectc_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    e = cudaFuncSetAttribute(dectc_kernel<NR, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<F8>::kSmem);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, 1ull << dev, __ATOMIC_RELEASE);
   }
-  e = launch_pdl(dectc_kernel<NR>, dim3(grid), dim3(kThreads), kSmem, s, p, qmap, kmap, vmap);
+  e = launch_pdl(dectc_kernel<NR, F8>, dim3(grid), dim3(Lay<F8>::kThreads), Lay<F8>::kSmem, s, p, qmap, kmap,
+                 vmap);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -734,9 +877,16 @@ cudaError_t launch_dectc_t(const AttnParams& p, const CUtensorMap& qmap, const C
 
 cudaError_t launch_dectc(const AttnParams& p, int rows, const CUtensorMap& qmap, const CUtensorMap& kmap,
                          const CUtensorMap& vmap, int grid, cudaStream_t s) {
-  if (rows <= 4) return launch_dectc_t<4>(p, qmap, kmap, vmap, grid, s);
-  if (rows <= 8) return launch_dectc_t<8>(p, qmap, kmap, vmap, grid, s);
-  return launch_dectc_t<16>(p, qmap, kmap, vmap, grid, s);
+  if (rows <= 4) return launch_dectc_t<4, false>(p, qmap, kmap, vmap, grid, s);
+  if (rows <= 8) return launch_dectc_t<8, false>(p, qmap, kmap, vmap, grid, s);
+  return launch_dectc_t<16, false>(p, qmap, kmap, vmap, grid, s);
+}
+
+cudaError_t launch_dectc_fp8(const AttnParams& p, int rows, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                             const CUtensorMap& vmap, int grid, cudaStream_t s) {
+  if (rows <= 4) return launch_dectc_t<4, true>(p, qmap, kmap, vmap, grid, s);
+  if (rows <= 8) return launch_dectc_t<8, true>(p, qmap, kmap, vmap, grid, s);
+  return cudaErrorInvalidValue;  // more than 8 rows per item: the CUDA-core kernel serves FP8 pools
 }
 
 }  // namespace pkv

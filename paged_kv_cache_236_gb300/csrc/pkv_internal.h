@@ -188,6 +188,10 @@ cudaError_t launch_mma(const AttnParams& p, const CUtensorMap& qmap, const CUten
 // rows: the largest item row count (4, 8 or 16 rows of softmax per key)
 cudaError_t launch_dectc(const AttnParams& p, int rows, const CUtensorMap& qmap, const CUtensorMap& kmap,
                          const CUtensorMap& vmap, int grid, cudaStream_t s);
+// The same kernel over FP8 pools (rows <= 8): staged E4M3 tiles converted to
+// fp16, fp16 MMAs; kmap / vmap are uint8 maps with {128, 1, bs, 1} boxes
+cudaError_t launch_dectc_fp8(const AttnParams& p, int rows, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                             const CUtensorMap& vmap, int grid, cudaStream_t s);
 
 // Sets the thread-local message pkv_last_error returns.
 void set_last_error(const char* msg);

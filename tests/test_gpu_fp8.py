@@ -4,7 +4,9 @@
   fp32, nearest E4M3 code with ties to even, saturation at 448), for bf16 and
   fp32 rows over the whole range: saturating, normal and subnormal codes.
 * paged_attention_forward_fp8kv equals the fp64 oracle's attention over the
-  decoded pools (code * scale), within the bf16 tolerance: decode, several
+  decoded pools (code * scale), within the bf16 tolerance, on both of its
+  kernels (the tensor-core decode kernel when a query-length hint bounds the
+  rows by 8, the CUDA-core kernel otherwise): decode, several
   query tokens, prefill chunks, GQA groups 1 to 16, block sizes 8 to 64,
   non-causal, a long split context, and the decode batch at full size on
   sampled sequences.  Unused pool slots hold the NaN code, so a read outside
@@ -100,8 +102,12 @@ class Fp8Run:
         return check_close(np.concatenate(g), np.concatenate(r), "bf16", what)
 
 
+# With a query-length hint that bounds every sequence's rows (tokens x G) by 8
+# the tensor-core decode kernel runs (fp16 MMAs over converted tiles): seeds
+# 1, 3, 7, 8, 9; the others take the CUDA-core kernel.
 @pytest.mark.parametrize("seed,hq,hkv,bs,max_q", [(1, 8, 2, 16, 1), (2, 8, 2, 16, 5), (3, 16, 16, 8, 3),
-                                                  (4, 32, 2, 32, 1), (5, 16, 1, 64, 7), (6, 32, 8, 16, 40)])
+                                                  (4, 32, 2, 32, 1), (5, 16, 1, 64, 7), (6, 32, 8, 16, 40),
+                                                  (7, 16, 8, 64, 4), (8, 32, 8, 32, 2), (9, 8, 8, 16, 1)])
 def test_attention_fp8_parity(seed, hq, hkv, bs, max_q):
     w = wl.random_small(seed, batch=6, max_ctx=700, max_q=max_q, num_q_heads=hq, num_kv_heads=hkv,
                         block_size=bs, poison=True)
