@@ -236,8 +236,13 @@ pkv_status paged_kv_write_fp8(const void* k, const void* v, const int64_t* slot_
  * code * v_scale; the same metadata, workspace and results otherwise
  * (softmax(scale q k^T) v, fp32 accumulation).  head_dim 128 (other head
  * sizes: PKV_ERR_UNSUPPORTED); any block_size, GQA group and query count of
- * paged_attention_forward.  Every row runs on the CUDA-core kernel (K and V
- * converted to fp32 in registers); PKV_HINT_SHARED_PREFIX is ignored.
+ * paged_attention_forward.  When max_query_len > 0, the group size
+ * num_q_heads / num_kv_heads is a power of two and max_query_len times it is
+ * at most 8, the tensor-core decode kernel runs: staged code tiles are
+ * converted to fp16 in shared memory, q is rounded to fp16 (|q| must stay
+ * below 65504) and the MMAs take fp16 operands.  Otherwise the CUDA-core
+ * kernel runs, K and V converted to fp32 in registers.
+ * PKV_HINT_SHARED_PREFIX is ignored.
  */
 pkv_status paged_attention_forward_fp8kv(const void* q, const void* k_cache, const void* v_cache,
                                          const int32_t* block_tables, const int32_t* context_lens,
