@@ -76,6 +76,9 @@ struct pkv_block_manager {
   std::unordered_map<int64_t, Seq> seqs_;
   int64_t next_entry_ = 1;
   int32_t used_ = 0;
+  // per-call scratch of pkv_bm_step, kept to avoid allocations
+  std::vector<int64_t> ids_scratch_;
+  std::vector<std::pair<int32_t, int32_t>> dropped_;  // (shared last block, copies made of it)
 
   pkv_block_manager(int32_t n, int32_t b, int32_t m)
       : nb(n), bs(b), max_blocks(m), ref_(n, 0), idle_pos_(n), is_idle_(n, 0), block_key_(n), block_entry_(n, 0) {
@@ -216,12 +219,20 @@ pkv_status pkv_bm_step(pkv_block_manager* bm, const int64_t* seq_ids, const int3
   // checks: distinct ids, sizes, and the blocks the whole step takes, with
   // the copy-on-write of a block shared by several members counted as the
   // sequential updates would (each copy drops the shared block's count)
-  std::unordered_set<int64_t> ids;
-  std::unordered_map<int32_t, int32_t> dropped;
+  std::vector<int64_t>& ids = bm->ids_scratch_;
+  ids.assign(seq_ids, seq_ids + num_seqs);
+  std::sort(ids.begin(), ids.end());
+  const auto dup = std::adjacent_find(ids.begin(), ids.end());
+  if (dup != ids.end()) return fail(PKV_ERR_INVALID_ARG, "sequence %lld twice in one step", (long long)*dup);
+  std::vector<std::pair<int32_t, int32_t>>& dropped = bm->dropped_;
+  dropped.clear();
+  auto dropped_of = [&](int32_t b) -> int32_t {
+    for (const auto& d : dropped)
+      if (d.first == b) return d.second;
+    return 0;
+  };
   int64_t total = 0, need = 0;
   for (int32_t i = 0; i < num_seqs; ++i) {
-    if (!ids.insert(seq_ids[i]).second)
-      return fail(PKV_ERR_INVALID_ARG, "sequence %lld twice in one step", (long long)seq_ids[i]);
     const int64_t n = num_new_tokens[i];
     if (n < 0) return fail(PKV_ERR_INVALID_ARG, "num_new_tokens[%lld] < 0", i);
     total += n;
@@ -238,14 +249,19 @@ pkv_status pkv_bm_step(pkv_block_manager* bm, const int64_t* seq_ids, const int3
       return fail(PKV_ERR_INVALID_ARG, "sequence %lld would need more than %lld blocks", (long long)seq_ids[i],
                   bm->max_blocks);
     int32_t named = 0;
-    if (!s.table.empty()) {
-      const int32_t last = s.table.back();
-      auto d = dropped.find(last);
-      named = bm->ref_[last] - (d == dropped.end() ? 0 : d->second);
-    }
+    if (!s.table.empty()) named = bm->ref_[s.table.back()] - dropped_of(s.table.back());
     bool cow;
     need += bm->need(s, n, named, &cow);
-    if (cow) ++dropped[s.table.back()];
+    if (cow) {
+      const int32_t last = s.table.back();
+      bool found = false;
+      for (auto& d : dropped)
+        if (d.first == last) {
+          ++d.second;
+          found = true;
+        }
+      if (!found) dropped.emplace_back(last, 1);
+    }
   }
   if (total > ((int64_t)1 << 31) - 1) return fail(PKV_ERR_INVALID_ARG, "more than 2^31 - 1 new tokens");
   if (total > 0 && !slot_mapping) return fail(PKV_ERR_INVALID_ARG, "null slot_mapping");
