@@ -314,13 +314,28 @@ class BlockManager:
                                    ctypes.byref(nc)))
         return slots, np.asarray(list(pair)[:2 * nc.value], dtype=np.int32).reshape(-1, 2)
 
-    def step(self, seq_ids, n_new) -> dict:
+    def step(self, seq_ids, n_new, reuse: bool = False) -> dict:
+        """One batch step (``pkv_bm_step``): the call metadata as host numpy
+        arrays.  With ``reuse=True`` they are views into buffers the manager
+        keeps, valid until its next ``step(..., reuse=True)``; this saves the
+        per-call allocations of a serving loop."""
         ids = _host(seq_ids, np.int64)
         n = _host(n_new, np.int32)
         B = len(ids)
         if len(n) != B:
             raise ValueError("seq_ids and n_new differ in length")
-        total = int(n.astype(np.int64).sum()) if B else 0
+        total = int(n.sum(dtype=np.int64)) if B else 0
+        if reuse:
+            bufs = self._buffers(B, total)
+            out = {k: v for k, v in bufs["arrays"].items()}
+            ptr = bufs["ptr"]
+            nc = bufs["nc"]
+            _check(lib().pkv_bm_step(self._h, ids.ctypes.data if B else None, n.ctypes.data if B else None, B,
+                                     ptr["slot_mapping"], ptr["block_tables"], ptr["context_lens"],
+                                     ptr["query_start_loc"], ptr["copies"], ctypes.byref(nc)))
+            return {"slot_mapping": out["slot_mapping"][:total], "block_tables": out["block_tables"][:B],
+                    "context_lens": out["context_lens"][:B], "query_start_loc": out["query_start_loc"][:B + 1],
+                    "copies": out["copies"][:nc.value]}
         out = {
             "slot_mapping": np.empty(max(total, 0), dtype=np.int64),
             "block_tables": np.empty((B, self.max_blocks), dtype=np.int32),
@@ -335,6 +350,25 @@ class BlockManager:
                                  out["copies"].ctypes.data, ctypes.byref(nc)))
         out["copies"] = out["copies"][:nc.value]
         return out
+
+    def _buffers(self, B: int, total: int) -> dict:
+        """Output buffers of at least B sequences and `total` new tokens,
+        grown geometrically, with their addresses computed once."""
+        b = getattr(self, "_bufs", None)
+        if b is None or b["B"] < B or b["T"] < total:
+            cb = max(B, 2 * b["B"] if b else 64, 1)
+            ct = max(total, 2 * b["T"] if b else 256, 1)
+            arrays = {
+                "slot_mapping": np.empty(ct, dtype=np.int64),
+                "block_tables": np.empty((cb, self.max_blocks), dtype=np.int32),
+                "context_lens": np.empty(cb, dtype=np.int32),
+                "query_start_loc": np.empty(cb + 1, dtype=np.int32),
+                "copies": np.empty((cb, 2), dtype=np.int32),
+            }
+            b = {"B": cb, "T": ct, "arrays": arrays, "nc": c_i32(0),
+                 "ptr": {k: a.ctypes.data for k, a in arrays.items()}}
+            self._bufs = b
+        return b
 
     def free(self, seq: int) -> None:
         _check(lib().pkv_bm_free(self._h, int(seq)))

@@ -143,3 +143,24 @@ def test_large_pool_is_fast(pkv):
         m.step(ids, [1] * 512)
     dt = (time.perf_counter() - t0) / 50
     assert dt < 0.05, dt
+
+
+def test_step_with_reused_buffers_matches(pkv):
+    """step(..., reuse=True) returns the same metadata (views into buffers
+    the manager keeps, grown as batches grow)."""
+    a, b = pkv.BlockManager(3000, 16, 64), pkv.BlockManager(3000, 16, 64)
+    rng = np.random.default_rng(3)
+    live = []
+    for it in range(60):
+        new = [1000 + it] if rng.random() < 0.5 or not live else []
+        live += new
+        ids = np.asarray(sorted(rng.choice(live, size=min(len(live), int(rng.integers(1, 40))), replace=False)),
+                         dtype=np.int64)
+        n = rng.integers(0, 40, size=len(ids)).astype(np.int32)
+        ra, rb = a.step(ids, n), b.step(ids, n, reuse=True)
+        for k in ra:
+            assert np.array_equal(ra[k], rb[k]), (it, k)
+        if it % 7 == 3 and len(live) > 3:
+            s = live.pop(int(rng.integers(0, len(live))))
+            a.free(s)
+            b.free(s)
