@@ -152,7 +152,8 @@ size_t paged_attention_workspace_min(int32_t num_seqs, int64_t num_tokens, int32
  *   out             device [num_tokens, num_q_heads, head_dim], dtype; every row of
  *                   every sequence is written
  *   max_query_len   host hint: an upper bound of every sequence's query count, or
- *                   0 if unknown (only used to skip launching kernels with no work)
+ *                   0 if unknown (used to pick the kernels; a smaller value still
+ *                   gives the right rows, possibly slower)
  *   scale           logit scale (e.g. 1/sqrt(head_dim))
  *   causal          non-zero: bottom-right aligned causal mask
  *   hints           PKV_HINT_* bits (0: none)
