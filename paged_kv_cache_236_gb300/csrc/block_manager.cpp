@@ -25,7 +25,6 @@
 #include <list>
 #include <new>
 #include <unordered_map>
-#include <unordered_set>
 #include <vector>
 
 #include "paged_kv_blocks.h"
@@ -226,10 +225,11 @@ pkv_status pkv_bm_step(pkv_block_manager* bm, const int64_t* seq_ids, const int3
   if (dup != ids.end()) return fail(PKV_ERR_INVALID_ARG, "sequence %lld twice in one step", (long long)*dup);
   std::vector<std::pair<int32_t, int32_t>>& dropped = bm->dropped_;
   dropped.clear();
-  auto dropped_of = [&](int32_t b) -> int32_t {
-    for (const auto& d : dropped)
-      if (d.first == b) return d.second;
-    return 0;
+  // copies already counted of shared block b (few: a linear scan)
+  auto dropped_of = [&](int32_t b) -> int32_t* {
+    for (auto& d : dropped)
+      if (d.first == b) return &d.second;
+    return nullptr;
   };
   int64_t total = 0, need = 0;
   for (int32_t i = 0; i < num_seqs; ++i) {
@@ -249,18 +249,18 @@ pkv_status pkv_bm_step(pkv_block_manager* bm, const int64_t* seq_ids, const int3
       return fail(PKV_ERR_INVALID_ARG, "sequence %lld would need more than %lld blocks", (long long)seq_ids[i],
                   bm->max_blocks);
     int32_t named = 0;
-    if (!s.table.empty()) named = bm->ref_[s.table.back()] - dropped_of(s.table.back());
+    int32_t* seen = nullptr;
+    if (!s.table.empty()) {
+      seen = dropped_of(s.table.back());
+      named = bm->ref_[s.table.back()] - (seen ? *seen : 0);
+    }
     bool cow;
     need += bm->need(s, n, named, &cow);
     if (cow) {
-      const int32_t last = s.table.back();
-      bool found = false;
-      for (auto& d : dropped)
-        if (d.first == last) {
-          ++d.second;
-          found = true;
-        }
-      if (!found) dropped.emplace_back(last, 1);
+      if (seen)
+        ++*seen;
+      else
+        dropped.emplace_back(s.table.back(), 1);
     }
   }
   if (total > ((int64_t)1 << 31) - 1) return fail(PKV_ERR_INVALID_ARG, "more than 2^31 - 1 new tokens");
