@@ -29,7 +29,7 @@ blocking, fusion or reordering beyond what the definition states:
                       (running max, running sum, unnormalised accumulator)
                       and its merge; the merged result equals ``attend``.
 
-Readings of points the pages leave open (each also listed in the design doc):
+Readings of points the pages leave open (each also listed in the design notes):
 
 1. slot = physical_block * block_size + position % block_size; slot < 0 means
    "skip this token" (padding).

@@ -16,7 +16,7 @@ The stream follows the serving life cycle the pages describe:
 
 The op kinds are:
 
-* ``("prompt", seq, tokens)``: a new request.  The driver calls
+* ``("prompt", seq, tokens)``: a new request.  The caller calls
   try_get_prefix_blocks, then update for the tokens that were not cached.
 * ``("step", seqs, n_new, new_tokens)``: one batch step (prefill chunks,
   decode, several draft tokens).
