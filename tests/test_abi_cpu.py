@@ -88,3 +88,20 @@ def test_fp8_host_checks_need_no_gpu(lib):
     assert lib.paged_kv_write_fp8(None, None, None, None, None, 3, 4, 16, 1, 8, 0, 0, 1, f(1.0), f(1.0), None) == 2
     assert lib.paged_kv_write_fp8(None, None, None, None, None, 3, 4, 16, 4, 128, 0, 0, 2, f(1.0), f(1.0), None) == 2
     assert lib.paged_kv_write_fp8(None, None, None, None, None, 0, 4, 16, 4, 128, 0, 0, 1, f(1.0), f(1.0), None) == 0
+
+
+def test_headers_compile_as_plain_c(tmp_path):
+    """The public headers are C: each compiles alone with a C99 compiler."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        src = tmp_path / f"use_{h}.c"
+        src.write_text(f'#include "{h}"\nint main(void) {{ return 0; }}\n')
+        r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-pedantic", "-fsyntax-only",
+                            "-I" + os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+        assert r.returncode == 0, (h, r.stderr)
