@@ -401,6 +401,26 @@ def run_gpu(args, rank, world, local_rank):
         result["gpu_launches"] += launches_per_step(wm, tm["mql"], tm["sp"]) * len(ms_m)
         del tm
 
+    # ---------------- prefill chunks alone (tensor-bound multi-token q) ----------------
+    if args.mixed and args.workload != "prefill":
+        wp = wl.prefill_chunks(seed=1003 + rank)
+        tp = prepare(wp)
+        ms_p, kern_p, _ = timed(wp, tp, max(3, args.steps // 2), args.warmup)
+        kavg = sum(kern_p) / len(kern_p)
+        fl = mma_flops(wp)
+        tfl = fl / (kavg * 1e-3) / 1e12
+        result["prefill_chunks"] = {
+            "kernel": "mma_attn_kernel (tcgen05, TMEM accumulators)", "kernel_ms": round(kavg, 5),
+            "achieved": round(tfl, 1), "unit": "TFLOP/s", "peak": bf16_peak, "frac": round(tfl / bf16_peak, 4),
+            "peak_kind": peak_kind + " bf16 dense (burst)", "algorithmic_flops_per_launch": fl,
+            "flops": "4 * head_dim per unmasked (query row, key) pair: QK^T and PV",
+            "traffic": ncu_traffic("prefill"),
+            "step_ms": round(sum(ms_p) / len(ms_p), 5),
+            "query_tokens_per_s": round(wp.step.num_tokens / (sum(ms_p) / len(ms_p) * 1e-3), 1),
+            "workload": WORKLOAD_DESC["prefill"]}
+        result["gpu_launches"] += launches_per_step(wp, tp["mql"], tp["sp"]) * len(ms_p)
+        del tp
+
     # ---------------- copy-on-write block copy (HBM-bound) ----------------
     if rank == 0:
         result["copy_blocks"] = copy_blocks_timing(pkv, torch, dev, flush, hbm_peak, args.warmup)

@@ -44,11 +44,18 @@
  *
  * Errors: host-checkable problems return a status before any launch and set a
  * thread-local message (pkv_last_error).  Metadata that only the device sees
- * (a block id outside [0, num_blocks), a slot outside the pool, a sequence
- * with more queries than tokens or a non-monotone query_start_loc, a context
- * longer than its table) never faults: the offending access is skipped (or
- * read as zeros), the sequence's output rows are zero, and a bit is set in
- * the sticky device error word that pkv_device_errors reads.
+ * never faults; each case sets a bit in the sticky device error word that
+ * pkv_device_errors reads:
+ *   - a slot outside the pool: that token's write is skipped
+ *     (PKV_DEVERR_SLOT_OUT_OF_RANGE);
+ *   - a block id outside [0, num_blocks) among a sequence's first
+ *     ceil(context_len / block_size) table entries: that block is read as a
+ *     block of zeros, i.e. its keys score 0 and carry zero values, and the
+ *     rest of the sequence is attended as usual
+ *     (PKV_DEVERR_BLOCK_OUT_OF_RANGE);
+ *   - a sequence with more queries than tokens, a non-monotone
+ *     query_start_loc or a context longer than its table: the rows it
+ *     addresses are written as zeros (PKV_DEVERR_BAD_SEQUENCE).
  */
 #ifndef PAGED_KV_H_
 #define PAGED_KV_H_
@@ -163,8 +170,9 @@ size_t paged_attention_workspace_min(int32_t num_seqs, int64_t num_tokens, int32
  * Supported: dtype bf16 or f32; head_dim 64 or 128; block_size 8, 16, 32 or 64;
  * num_q_heads / num_kv_heads <= 128; num_seqs <= 32768 (PKV_ERR_UNSUPPORTED
  * beyond).
- * Rows of a sequence whose metadata is invalid (see the error notes above)
- * are written as zeros.
+ * Invalid metadata is handled as the error notes at the top of this file
+ * state (zero rows for an invalid sequence; an out-of-pool block id read as
+ * a block of zeros).
  */
 pkv_status paged_attention_forward(const void* q, const void* k_cache, const void* v_cache,
                                    const int32_t* block_tables, const int32_t* context_lens,
@@ -189,9 +197,10 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
  * nothing (no cudaMalloc / cudaFree, no allocating library routine).
  *   - A batch whose paged_attention_workspace_min exceeds the static size is
  *     rejected with PKV_ERR_WORKSPACE before any launch.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *   - Each call looks up the array's device address (cudaGetSymbolAddress,
+ *     with the current device); the first lookup on a device may load the
+ *     library's device code, so make the first call on each device before
+ *     any stream capture.
  *   - Every call on a device uses the same array, which keeps the last call's
  *     contents (each call rewrites what it reads).  Calls whose GPU work can
  *     overlap (other streams, unordered host threads) race on it: serialise
@@ -285,6 +294,22 @@ void pkv_set_profile_events(void* start, void* stop);
  * PKV_ERR_CUDA if either has not completed.
  */
 pkv_status pkv_event_elapsed_ms(void* start, void* stop, float* ms);
+
+/*
+ * pkv_debug_fault - testing hook for the bounded in-kernel waits (no
+ * counterpart on the source pages).  Arms the next paged_attention_forward /
+ * _fp8kv call made on this thread, and only that call:
+ *   wait_ns     > 0: every bounded wait of its attention kernels gives up
+ *               after wait_ns nanoseconds instead of 2 s;
+ *   fault_tile  > 0: in the first CTA of its decode-shaped attention kernel
+ *               the K/V producer skips the loads of its fault_tile-th key tile
+ *               (counting from 1), so the waits for that tile run out.
+ * The kernel then sets PKV_DEVERR_TIMEOUT, every role of the CTA leaves
+ * (tensor memory freed, copies in flight awaited) and the call's output is
+ * unspecified; the device and later calls are unaffected.  (0, 0) disarms.
+ * Returns PKV_ERR_INVALID_ARG for negative arguments.
+ */
+pkv_status pkv_debug_fault(int32_t fault_tile, int64_t wait_ns);
 
 /* Library version string, e.g. "paged_kv 0.1.0 sm_103a". */
 const char* pkv_version(void);

@@ -30,7 +30,7 @@ import torch
 
 __all__ = [
     "paged_kv_write", "paged_attention_forward", "workspace_size", "workspace_min",
-    "device_errors", "set_profile_events", "profile_elapsed_ms", "lib", "LibraryError", "DEVERR",
+    "device_errors", "debug_fault", "set_profile_events", "profile_elapsed_ms", "lib", "LibraryError", "DEVERR",
     "BlockManager", "OutOfBlocks", "copy_blocks", "paged_kv_write_fp8", "paged_attention_forward_fp8kv",
 ]
 
@@ -102,6 +102,8 @@ def lib() -> ctypes.CDLL:
             L.pkv_event_elapsed_ms.argtypes = [c_vp, c_vp, ctypes.POINTER(c_f)]
             L.pkv_version.restype = ctypes.c_char_p
             L.pkv_version.argtypes = []
+            L.pkv_debug_fault.restype = c_i32
+            L.pkv_debug_fault.argtypes = [c_i32, c_i64]
             c_p32 = ctypes.POINTER(c_i32)
             for name, args in (
                     ("pkv_bm_create", [c_i32, c_i32, c_i32, ctypes.POINTER(c_vp)]),
@@ -261,6 +263,14 @@ def profile_elapsed_ms(start, stop) -> float:
     ms = c_f(0.0)
     _check(lib().pkv_event_elapsed_ms(start.cuda_event, stop.cuda_event, ctypes.byref(ms)))
     return float(ms.value)
+
+
+def debug_fault(fault_tile: int, wait_ns: int) -> None:
+    """Testing hook (``pkv_debug_fault``): arm the next forward call of this
+    thread to give up its waits after ``wait_ns`` ns and, with
+    ``fault_tile`` >= 1, to skip the loads of one key tile in one CTA, so
+    that the bounded waits run out."""
+    _check(lib().pkv_debug_fault(int(fault_tile), int(wait_ns)))
 
 
 def device_errors(clear: bool = True) -> int:

@@ -22,6 +22,9 @@ namespace {
 
 thread_local char g_msg[512] = "";
 thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+// pkv_debug_fault: armed for the next forward call of this thread only
+thread_local int g_fault_tile = 0;
+thread_local uint64_t g_fault_wait_ns = 0;
 
 pkv_status fail(pkv_status st, const char* fmt, ...) {
   va_list ap;
@@ -198,6 +201,13 @@ pkv_status pkv_event_elapsed_ms(void* start, void* stop, float* ms) {
   if (!start || !stop || !ms) return fail(PKV_ERR_INVALID_ARG, "null argument");
   cudaError_t e = cudaEventElapsedTime(ms, static_cast<cudaEvent_t>(start), static_cast<cudaEvent_t>(stop));
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+  return PKV_OK;
+}
+
+pkv_status pkv_debug_fault(int32_t fault_tile, int64_t wait_ns) {
+  if (fault_tile < 0 || wait_ns < 0) return fail(PKV_ERR_INVALID_ARG, "fault_tile and wait_ns must be >= 0");
+  g_fault_tile = fault_tile;
+  g_fault_wait_ns = (uint64_t)wait_ns;
   return PKV_OK;
 }
 
@@ -460,6 +470,10 @@ static pkv_status forward_impl(const void* q, const void* k_cache, const void* v
   ap.causal = causal ? 1 : 0;
   ap.out_al32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   ap.err = dev->err;
+  ap.wait_ns = g_fault_wait_ns;
+  ap.fault_tile = g_fault_tile;
+  g_fault_tile = 0;
+  g_fault_wait_ns = 0;
 
   if (g_prof_start && (e = cudaEventRecord(g_prof_start, s)) != cudaSuccess) return cuda_fail(e, "profile event");
   if (mma_launch) {

@@ -200,6 +200,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* empty = full + C::kStages;
   int* flag_last = reinterpret_cast<int*>(empty + C::kStages);
+  volatile int* abort_flag = flag_last + 1;
+  const WaitCtl wc{p.err, abort_flag, p.wait_ns ? p.wait_ns : kWaitTimeoutNs};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -207,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
+    *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -221,13 +224,24 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
     }
     const int nb_per_tile = kDecTileKeys / p.bs;
     int tile = 0;
+    // On giving up: wait (bounded, whatever the abort flag says) until the
+    // copies of the last tiles issued have landed, so that none is still in
+    // flight into this CTA's shared memory when it exits.
+    auto drain = [&]() {
+      const WaitCtl dw{p.err, nullptr, wc.limit_ns};
+      for (int j = max(0, tile - C::kStages); j < tile; ++j)
+        __all_sync(0xffffffffu, mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1, dw));
+    };
     int idx = 0;
     if (lane == 0) idx = atomicAdd(p.counter, 1);
     idx = __shfl_sync(0xffffffffu, idx, 0);
     for (;;) {
       if (idx >= n_items) {
         const int stage = tile % C::kStages;
-        if (!mbar_wait(&empty[stage], ((tile / C::kStages) & 1) ^ 1, p.err)) return;
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], ((tile / C::kStages) & 1) ^ 1, wc))) {
+          drain();
+          return;
+        }
         if (lane == 0) {
           meta[stage].item = -1;
           meta[stage].flags = kMetaDone;
@@ -261,7 +275,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
         const int stage = tile % C::kStages;
         const bool first = kbase == it.kb;
         const int next_phys = (kbase + kDecTileKeys < it.ke) ? block_of(kbase + kDecTileKeys) : 0;
-        if (!mbar_wait(&empty[stage], ((tile / C::kStages) & 1) ^ 1, p.err)) return;
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], ((tile / C::kStages) & 1) ^ 1, wc))) {
+          drain();
+          return;
+        }
+        if (p.fault_tile == tile + 1 && blockIdx.x == 0) {
+          // testing only: this tile is never loaded, so its consumers' waits run out
+          phys = next_phys;
+          ++tile;
+          continue;
+        }
         uint8_t* sbase = smem + stage * C::kStageBytes;
         if (lane == 0) {
           Meta& m = meta[stage];
@@ -313,7 +336,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
   int tile = 0;
   for (;;) {
     const int stage = tile % C::kStages;
-    if (!mbar_wait(&full[stage], (tile / C::kStages) & 1, p.err)) break;
+    // The four consumer warps wait for the same tile; they agree before going
+    // on, so that if one gave up, all leave (none is left waiting alone at
+    // the item's end barrier).
+    const bool got = __all_sync(0xffffffffu, mbar_wait(&full[stage], (tile / C::kStages) & 1, wc));
+    if (barrier_any(3, kConsumerWarps * 32, !got)) break;
     const Meta mt = meta[stage];
     if (mt.flags & kMetaDone) break;
     const uint8_t* sbase = smem + stage * C::kStageBytes;

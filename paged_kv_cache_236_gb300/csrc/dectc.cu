@@ -853,6 +853,12 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  // Beside the tensor-core kernel this grid skipped its wait for it at
+  // launch; it waits here instead, before it completes.  The next call's
+  // kernels are launched with programmatic serialization and wait only for
+  // this grid, so its completion must imply the tensor-core kernel's (which
+  // still reads the plan, counters and tickets that the next call rewrites).
+  if (p.no_wait && threadIdx.x == 0) pdl_wait();
 }
 
 template <int NR, bool F8>

@@ -98,18 +98,56 @@ __device__ __forceinline__ bool mbar_test_wait3(uint64_t* a, uint32_t pa, uint64
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete.  Returns false (and
-// sets PKV_DEVERR_TIMEOUT) if it has not completed within kWaitTimeoutNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+// How a kernel's bounded waits give up: the device error word that records
+// a timeout, the CTA's abort flag in shared memory (set by the first wait
+// that times out; every other wait of the CTA then gives up at once, so all
+// roles leave together), and the time limit.
+struct WaitCtl {
+  int* err;
+  volatile int* abort;  // nullptr: no abort flag
+  uint64_t limit_ns;
+};
+
+// Wait for the phase with the given parity to complete.  Returns false if it
+// has not completed within w.limit_ns (then sets PKV_DEVERR_TIMEOUT and the
+// abort flag) or once the abort flag is set.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && globaltimer() - t0 > kWaitTimeoutNs) {
-      raise_error(err, PKV_DEVERR_TIMEOUT);
-      return false;
+    if ((i & 63u) == 0) {
+      if (w.abort && *w.abort) return false;
+      if (globaltimer() - t0 > w.limit_ns) {
+        raise_error(w.err, PKV_DEVERR_TIMEOUT);
+        if (w.abort) *w.abort = 1;
+        return false;
+      }
     }
   }
+}
+
+// The same with the default limit and no abort flag.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+  return mbar_wait(bar, parity, WaitCtl{err, nullptr, kWaitTimeoutNs});
+}
+
+// Named barrier over `nthreads` threads (whole warps) with id `id` (1..15)
+// that also ORs a predicate over them: every thread gets true if any thread
+// passed true.  Used where threads that may each have given up on a wait
+// must agree before going on, so that none waits at a later barrier for
+// threads that left.
+__device__ __forceinline__ bool barrier_any(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ---------------------------------------------------------------------------

@@ -145,6 +145,13 @@ struct AttnParams {
   // the tensor-core kernel, and reads the plan from L2.
   int no_wait;
   int* err;
+  // Bounded waits give up after wait_ns nanoseconds (0: the default, 2 s).
+  uint64_t wait_ns;
+  // Testing only (0 in every ordinary call): fault_tile >= 1 makes CTA 0's
+  // K/V producer skip the loads and the arrival of its fault_tile-th key tile
+  // (counting from 1), so that the waits for that tile run out and the
+  // kernel's timeout path is exercised without any other fault.
+  int fault_tile;
 };
 
 // Launch with programmatic stream serialization (the kernel may start before

@@ -18,7 +18,6 @@
 // (different streams, or different host threads without ordering) race on it.
 #include <cuda_runtime.h>
 
-#include <mutex>
 #include <stdio.h>
 
 #include "paged_kv.h"
@@ -30,29 +29,26 @@ constexpr size_t kStaticWorkspaceBytes = size_t(8) << 20;  // 8 MiB per device
 
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
-std::mutex g_static_mu;
-void* g_static_ptr[64] = {};  // device address of g_static_workspace, per device ordinal
-
-// Device address of the scratch on the current device.  The first call on a
-// device looks it up (cudaGetSymbolAddress must run with that device current).
+// Device address of the scratch on the current device.  In host code
+// g_static_workspace names a host-side stand-in, not device memory, so the
+// address is looked up with that device current: on every call, which costs
+// a runtime query and allocates nothing, so that an address never outlives
+// the module it came from (after cudaDeviceReset the library's device module
+// is loaded again, at another address).
 pkv_status static_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+  if (e != cudaSuccess) {
     pkv::set_last_error("static scratch: no usable current device");
     return PKV_ERR_CUDA;
   }
-  std::lock_guard<std::mutex> lk(g_static_mu);
-  if (!g_static_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_workspace);
-    if (e != cudaSuccess || !p) {
-      pkv::set_last_error("static scratch: cudaGetSymbolAddress failed");
-      return PKV_ERR_CUDA;
-    }
-    g_static_ptr[dev] = p;
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_static_workspace);
+  if (e != cudaSuccess || !p) {
+    pkv::set_last_error("static scratch: cudaGetSymbolAddress failed");
+    return PKV_ERR_CUDA;
   }
-  *out = g_static_ptr[dev];
+  *out = p;
   return PKV_OK;
 }
 

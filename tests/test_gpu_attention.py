@@ -115,8 +115,10 @@ def test_block_permutation_is_bit_identical():
 
 def test_invalid_metadata_is_flagged_and_zeroed():
     """A sequence with more queries than tokens and one whose table names a
-    block outside the pool: no fault, the first's rows are zero, both raise
-    device error bits, the valid sequence is still right."""
+    block outside the pool: no fault, both raise device error bits; the
+    first's rows are zero, the second reads that block as a block of zeros
+    (its rows equal the oracle's over a pool where the entry names an all-zero
+    block), and the valid sequence is still right."""
     w = wl.build("bad", context_lens=[40, 30, 50], q_lens=[2, 1, 1], num_blocks=12, block_size=16,
                  num_q_heads=4, num_kv_heads=2, head_dim=128, dtype="bf16", seed=2, poison=False)
     dw = DeviceWorkload(w)
@@ -140,6 +142,18 @@ def test_invalid_metadata_is_flagged_and_zeroed():
     a, b, ref = rows[2]
     from gpu_util import check_close
     check_close(o[a:b], ref, "bf16", "valid sequence next to bad ones")
+    # sequence 1: its second block reads as zeros; the oracle sees a pool with
+    # one extra all-zero block that the corrupted entry names
+    zk = np.concatenate([dw.kc_host, np.zeros_like(dw.kc_host[:1])])
+    zv = np.concatenate([dw.vc_host, np.zeros_like(dw.vc_host[:1])])
+    bt1 = st.block_tables[1].copy()
+    bt1[1] = w.num_blocks
+    L1 = int(st.context_lens[1])
+    a1, b1 = int(st.query_start_loc[1]), int(st.query_start_loc[2])
+    K = wl.to_f64(po.gather(zk, bt1, L1), "bf16")
+    V = wl.to_f64(po.gather(zv, bt1, L1), "bf16")
+    ref1 = po.attend(wl.to_f64(st.q[a1:b1], "bf16"), K, V, w.scale, True)
+    check_close(o[a1:b1], ref1, "bf16", "sequence with an out-of-pool block id")
 
 
 def test_host_side_errors():
@@ -175,3 +189,82 @@ def test_decode_with_length_hint(hq, hkv, max_q):
     out = dw.run_step(0, max_query_len=int(n.max()))
     check_step(dw, out, what=f"hint {hq}/{hkv} q<={max_q}")
     assert pkv.device_errors() == 0
+
+
+# GQA groups that are not powers of two (3, 5, 6, 7) and large groups (32,
+# 64): decode over a long split context, a speculative-verify window of 5
+# tokens, a 300-token prefill chunk and short ragged sequences in one batch.
+GQA_GROUPS = [(12, 4), (10, 2), (6, 1), (14, 2), (32, 1), (64, 1)]
+GQA_CASES = [(dt, D, hq, hkv) for (hq, hkv) in GQA_GROUPS for (dt, D) in (("bf16", 128), ("bf16", 64), ("f32", 128))]
+
+
+def _gqa_workload(dtype, D, hq, hkv, seed):
+    L = [6000, 3000, 700, 40, 17, 1]
+    n = [1, 5, 300, 1, 2, 1]
+    nb = sum(-(-x // 16) for x in L) + 5
+    return wl.build(f"gqa-{hq}-{hkv}", context_lens=L, q_lens=n, num_blocks=nb, block_size=16, num_q_heads=hq,
+                    num_kv_heads=hkv, head_dim=D, dtype=dtype, seed=seed, poison=True)
+
+
+@pytest.mark.parametrize("dtype,D,hq,hkv", GQA_CASES)
+def test_gqa_groups(dtype, D, hq, hkv):
+    w = _gqa_workload(dtype, D, hq, hkv, 900 + GQA_CASES.index((dtype, D, hq, hkv)))
+    dw = DeviceWorkload(w)
+    out = dw.run_step(0)
+    check_step(dw, out, what=f"{dtype} D{D} G{hq // hkv}")
+    # the same batch with the query-length hint (kernel choice by rows)
+    st = w.step
+    t = dw.step_tensors(st)
+    out2 = pkv.paged_attention_forward(t["q"], dw.kc, dw.vc, t["bt"], t["ctx"], t["qsl"], w.scale, True,
+                                       max_query_len=int(st.q_lens.max()))
+    torch.cuda.synchronize()
+    check_step(dw, out2, what=f"{dtype} D{D} G{hq // hkv}, length hint")
+    assert pkv.device_errors() == 0
+
+
+@pytest.mark.parametrize("hq,hkv", GQA_GROUPS)
+def test_gqa_groups_fp8(hq, hkv):
+    from test_gpu_fp8 import Fp8Run
+    w = _gqa_workload("bf16", 128, hq, hkv, 950 + GQA_GROUPS.index((hq, hkv)))
+    run = Fp8Run(w, 0.02, 0.015)
+    run.check(run.step(), what=f"fp8 G{hq // hkv}")
+    assert pkv.device_errors() == 0
+
+
+def test_back_to_back_calls_share_the_cached_workspace():
+    """Mixed batches forwarded back to back on one stream, with the default
+    cached workspace and no host synchronisation between the calls: the
+    tensor-core kernel of one call runs beside its decode kernel, and the next
+    call's planner must not rewrite the shared plan while it still reads it.
+    Every call's rows are checked against the oracle afterwards."""
+    mk = lambda name, seed, L, n: wl.build(name, context_lens=L, q_lens=n, num_blocks=sum(-(-x // 16) for x in L) + 4,
+                                           block_size=16, num_q_heads=16, num_kv_heads=4, head_dim=128,
+                                           dtype="bf16", seed=seed, poison=True)
+    # a: long prefill chunks (tensor-core work dominates) beside short decodes
+    wa = mk("b2b-a", 61, [3000, 2600] + [150 + 37 * i for i in range(24)], [1024, 900] + [1] * 24)
+    # b: long decodes beside a short chunk
+    wb = mk("b2b-b", 62, [7000, 5000, 900] + [4000 - 101 * i for i in range(20)], [1, 1, 200] + [1] * 20)
+    dws = [DeviceWorkload(wa), DeviceWorkload(wb)]
+    ts = []
+    for dw in dws:
+        st = dw.w.step
+        t = dw.step_tensors(st)
+        pkv.paged_kv_write(t["k"], t["v"], t["slots"], dw.kc, dw.vc)
+        po_write(dw, st)
+        ts.append(t)
+    torch.cuda.synchronize()
+    outs = []
+    for rep in range(3):
+        for i, dw in enumerate(dws):
+            t = ts[i]
+            outs.append((i, pkv.paged_attention_forward(t["q"], dw.kc, dw.vc, t["bt"], t["ctx"], t["qsl"],
+                                                        dw.w.scale, True)))
+    torch.cuda.synchronize()
+    for k, (i, out) in enumerate(outs):
+        check_step(dws[i], out, what=f"call {k} (batch {'ab'[i]})")
+    assert pkv.device_errors() == 0
+
+
+def po_write(dw, st):
+    from oracle import paged_oracle as po
+    po.kv_write(st.k_new, st.v_new, st.slot_mapping, dw.kc_host, dw.vc_host)

@@ -4,10 +4,12 @@ Some callers cannot give the library a workspace: they run under an
 allocator that refuses new device allocations once started, or can only
 pass through buffers that another component registered.  For them,
 paged_attention_forward_static_ws uses a scratch array built into the
-library.  This test calls it through the C ABI twice in a row and checks each
-result against the regular entry point (which gets a caller-allocated
-workspace), within the parity tolerances used everywhere else, and checks
-that a batch too large for the built-in scratch is refused before any launch.
+library.  This test calls it through the C ABI twice in a row, with no host
+synchronisation between the two calls, and checks each result against the
+regular entry point (which gets a caller-allocated workspace) and against
+the fp64 oracle, within the parity tolerances used everywhere else; it also
+checks that a batch too large for the built-in scratch is refused before any
+launch.
 
 Named so that pytest collects it last.
 """
@@ -19,7 +21,8 @@ import torch
 
 import paged_kv_cache_236_gb300 as pkv
 import workloads as wl
-from gpu_util import DeviceWorkload, check_close, to_f64
+from gpu_util import DeviceWorkload, check_close, check_step, to_f64
+from oracle import paged_oracle as po
 
 pytestmark = pytest.mark.gpu
 
@@ -51,16 +54,21 @@ def test_static_scratch_matches_workspace_entry_point():
     st = w.step
     t = dw.step_tensors(st)
     pkv.paged_kv_write(t["k"], t["v"], t["slots"], dw.kc, dw.vc)
+    po.kv_write(st.k_new, st.v_new, st.slot_mapping, dw.kc_host, dw.vc_host)
     ref = pkv.paged_attention_forward(t["q"], dw.kc, dw.vc, t["bt"], t["ctx"], t["qsl"], w.scale, w.causal)
     torch.cuda.synchronize()
     ref64 = to_f64(ref)
     f = _entry()
+    # two calls in a row on one stream, the second issued while the first may
+    # still run (both share the one static scratch)
+    outs = [torch.full_like(t["q"], float("nan")) for _ in range(2)]
     for call in range(2):
-        out = torch.full_like(t["q"], float("nan"))
-        status = _call(f, t, dw.kc, dw.vc, out, w, st.num_tokens, int(st.q_lens.max()))
+        status = _call(f, t, dw.kc, dw.vc, outs[call], w, st.num_tokens, 0)
         assert status == 0, pkv.lib().pkv_last_error()
-        torch.cuda.synchronize()
-        check_close(to_f64(out), ref64, "bf16", f"static scratch, call {call}")
+    torch.cuda.synchronize()
+    for call in range(2):
+        check_close(to_f64(outs[call]), ref64, "bf16", f"static scratch, call {call}")
+        check_step(dw, outs[call], what=f"static scratch against the oracle, call {call}")
     assert pkv.device_errors() == 0
 
 
