@@ -50,6 +50,15 @@
 // 4 Q tiles and 4 metadata slots (the producers are up to two tiles ahead).
 // The K scale is in the logit scale, the V scale multiplies the output.
 //
+// Bounded waits (failure detection): every wait gives up after a time limit
+// (2 s unless the call sets one) or as soon as another role of the CTA has
+// given up (an abort flag in shared memory).  Waits whose outcome decides
+// what a group of warps does next are settled across the group by a barrier
+// that ORs the failures, so that all of the group's warps go on or all
+// leave; nothing waits without a bound.  A producer that leaves first waits
+// (bounded) for its copies in flight, and the MMA thread for its last MMAs;
+// then every role meets at the end, where TMEM is freed.
+//
 // An unsplit item after a shared prefix (part < 0, merge group >= 0) folds
 // the prefix's partial rows, written by the tensor-core kernel before this
 // one ran, into its own rows in the epilogue; a split one leaves that to its
@@ -157,9 +166,9 @@ __device__ __forceinline__ MergeGroup load_group(const MergeGroup* g) {
   return m;
 }
 
-// All 128 softmax threads (warps 2-5) wait for the same phase; exit together.
-__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* err) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+// A warp waits for a phase; true for every lane only if it completed for all.
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
 }
 
 // Reduce NR values per lane over the 32 lanes of a warp with `op`,
@@ -265,6 +274,8 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
   Meta* meta = reinterpret_cast<Meta*>(smem + Y::kMetaOff);
   float* red = reinterpret_cast<float*>(smem + Y::kRedOff);  // [2][4 warps][NR rows]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  const WaitCtl wc{p.err, abort_flag, p.wait_ns ? p.wait_ns : kWaitTimeoutNs};
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Y::kStages; ++s) {
@@ -289,6 +300,7 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
       mbar_init(&bars->islot_free[b], 2);  // both producers read the slot
       mbar_init(&bars->stage_empty[b], 128);
     }
+    *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -321,9 +333,21 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
     const int nb_per_tile = kKeys / p.bs;
     const ItemSlot* islots = reinterpret_cast<const ItemSlot*>(smem + Y::kISlotOff);
     int g = 0;
+    // On giving up: wait (bounded, whatever the abort flag says) until the
+    // copies of the tiles issued last have landed, so that none is still in
+    // flight into this CTA's shared memory when it exits.
+    uint64_t* fullb = vprod ? bars->v_full : bars->k_full;
+    auto drain = [&]() {
+      const WaitCtl dw{p.err, nullptr, wc.limit_ns};
+      for (int j = max(0, g - Y::kStages); j < g; ++j)
+        __all_sync(0xffffffffu, mbar_wait(&fullb[j % Y::kStages], (j / Y::kStages) & 1, dw));
+    };
     for (int it_cnt = 0;; ++it_cnt) {
       const int qb = it_cnt & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->islot_full[qb], (it_cnt >> 1) & 1, p.err))) break;
+      if (!wait_all(&bars->islot_full[qb], (it_cnt >> 1) & 1, wc)) {
+        drain();
+        break;
+      }
       const ItemSlot& isl = islots[qb];
       const bool done = isl.done != 0;
       const WorkItem it = isl.it;
@@ -334,9 +358,10 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
       if (done) {
         if (vprod) break;
         const int st = g % Y::kStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(F8 ? &bars->stage_empty[st] : &bars->kv_empty[st],
-                                               ((g / Y::kStages) & 1) ^ 1, p.err)))
+        if (!wait_all(F8 ? &bars->stage_empty[st] : &bars->kv_empty[st], ((g / Y::kStages) & 1) ^ 1, wc)) {
+          drain();
           break;
+        }
         const int mi = F8 ? (g & 3) : st;
         if (lane == 0) {
           meta[mi].item = -1;
@@ -366,10 +391,14 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
         const int next_phys = (kbase + kKeys < it.ke) ? block_of(kbase + kKeys) : 0;
         // bf16: the stage's K/V tiles are free once its last P.V is done.
         // FP8: the staging slot is free once its codes are converted.
-        if (!__all_sync(0xffffffffu, mbar_wait(F8 ? &bars->stage_empty[st] : &bars->kv_empty[st],
-                                               ((g / Y::kStages) & 1) ^ 1, p.err))) {
+        if (!wait_all(F8 ? &bars->stage_empty[st] : &bars->kv_empty[st], ((g / Y::kStages) & 1) ^ 1, wc)) {
           ok = false;
           break;
+        }
+        if (!vprod && p.fault_tile == g + 1 && blockIdx.x == 0) {
+          // testing only: this tile is never loaded, so the waits for it run out
+          phys = next_phys;
+          continue;
         }
         uint8_t* kd = smem + st * kStageBytes;
         uint8_t* vd = kd + kTileBytes;
@@ -428,7 +457,10 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
         }
         phys = next_phys;
       }
-      if (!ok) break;
+      if (!ok) {
+        drain();
+        break;
+      }
     }
   } else if (warp == 10) {
     // ================================================================ item fetch
@@ -440,9 +472,7 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
       // c-1 (and so item c-2, freeing slot qb): one item waits while one is
       // loaded.  Taking items no earlier keeps the queue's largest-first
       // order close to the order in which the SMs fall idle.
-      if (c >= 1 &&
-          !__all_sync(0xffffffffu, mbar_wait(&bars->islot_free[(c - 1) & 1], ((c - 1) >> 1) & 1, p.err)))
-        break;
+      if (c >= 1 && !wait_all(&bars->islot_free[(c - 1) & 1], ((c - 1) >> 1) & 1, wc)) break;
       int idx = 0;
       if (lane == 0) idx = atomicAdd(p.counter, 1);
       idx = __shfl_sync(0xffffffffu, idx, 0);
@@ -488,6 +518,7 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
     if (lane == 0) {
       int g = 0, it_cnt = -1;
       int pend = -1, pend_item = 0;  // tile whose P.V is still to be issued, and its item count
+      int last_s = -1, last_pv = -1;  // the last S and P.V issued
       // descriptors of stage 0 / buffer 0; others are offsets of these
       const uint64_t dk0 = desc_k(smem_base);
       const uint64_t dv0 = desc_mn(smem_base + kTileBytes);
@@ -498,10 +529,10 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
         const int b = pend & 1, st = pend % Y::kStages, ob = pend_item & 1;
         if (pend_first) {
           // O^T[ob] is about to be overwritten: the epilogue of item pend_item-2 must have read it
-          if (!mbar_wait(&bars->o_empty[ob], ((pend_item >> 1) & 1) ^ 1, p.err)) return false;
+          if (!mbar_wait(&bars->o_empty[ob], ((pend_item >> 1) & 1) ^ 1, wc)) return false;
         }
-        if (!mbar_wait(&bars->p_full[b], (pend >> 1) & 1, p.err)) return false;
-        if (!mbar_wait(F8 ? &bars->vc_full[st] : &bars->v_full[st], (pend / Y::kStages) & 1, p.err)) return false;
+        if (!mbar_wait(&bars->p_full[b], (pend >> 1) & 1, wc)) return false;
+        if (!mbar_wait(F8 ? &bars->vc_full[st] : &bars->v_full[st], (pend / Y::kStages) & 1, wc)) return false;
         tc_fence_after();
         const uint64_t dv = desc_add(dv0, st * kStageBytes);
         const uint64_t dp = desc_add(dp0, b * 2 * kQHalf);
@@ -512,20 +543,28 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
         umma_commit(&bars->pv_done[b]);
         umma_commit(&bars->kv_empty[st]);
         if (pend_last) umma_commit(&bars->o_full[ob]);
+        last_pv = pend;
         pend = -1;
         return true;
       };
+      bool ok = true;
       for (;; ++g) {
         const int st = g % Y::kStages;
-        if (!mbar_wait(F8 ? &bars->kc_full[st] : &bars->k_full[st], (g / Y::kStages) & 1, p.err)) break;
+        if (!mbar_wait(F8 ? &bars->kc_full[st] : &bars->k_full[st], (g / Y::kStages) & 1, wc)) {
+          ok = false;
+          break;
+        }
         const int flags = meta[F8 ? (g & 3) : st].flags;
         if (flags & kMetaDone) {
-          if (pend >= 0) issue_pv();
+          if (pend >= 0) ok = issue_pv();
           break;
         }
         if (flags & kMetaFirst) ++it_cnt;
         const int b = g & 1;
-        if (!mbar_wait(&bars->s_free[b], ((g >> 1) & 1) ^ 1, p.err)) break;
+        if (!mbar_wait(&bars->s_free[b], ((g >> 1) & 1) ^ 1, wc)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint64_t dk = desc_add(dk0, st * kStageBytes);
         const uint64_t dq = desc_add(dq0, (it_cnt & (Y::kQBufs - 1)) * 2 * kQHalf);
@@ -534,11 +573,21 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
           umma_bf16(tmem + kSCol + b * kN, desc_add(dk, (kk >> 2) * kHalf + (kk & 3) * 32),
                     desc_add(dq, (kk >> 2) * kQHalf + (kk & 3) * 32), F8 ? kIdescS16 : kIdescS, kk > 0 ? 1u : 0u);
         umma_commit(&bars->s_full[b]);
-        if (pend >= 0 && !issue_pv()) break;
+        last_s = g;
+        if (pend >= 0 && !issue_pv()) {
+          ok = false;
+          break;
+        }
         pend = g;
         pend_item = it_cnt;
         pend_first = (flags & kMetaFirst) != 0;
         pend_last = (flags & kMetaLast) != 0;
+      }
+      if (!ok) {
+        // leaving early: let the MMAs already issued finish before TMEM is freed
+        const WaitCtl dw{p.err, nullptr, wc.limit_ns};
+        if (last_s >= 0) mbar_wait(&bars->s_full[last_s & 1], (last_s >> 1) & 1, dw);
+        if (last_pv >= 0) mbar_wait(&bars->pv_done[last_pv & 1], (last_pv >> 1) & 1, dw);
       }
     }
     __syncwarp();
@@ -554,14 +603,14 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
       for (int g = 0;; ++g) {
         const int st = g % Y::kStages;
         const uint32_t ph = (g / Y::kStages) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_full[st], ph, p.err))) break;
+        if (!wait_all(&bars->k_full[st], ph, wc)) break;
         const int flags = meta[g & 3].flags;
         if (flags & kMetaDone) {
           mbar_arrive(&bars->kc_full[st]);  // the MMA and softmax warps see the end
           break;
         }
         // the stage's fp16 tiles are free once the P.V of its previous tile is done
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->kv_empty[st], ph ^ 1, p.err))) break;
+        if (!wait_all(&bars->kv_empty[st], ph ^ 1, wc)) break;
         const uint8_t* codes = smem + Y::kStgOff + st * 2 * kCodeTile;
         uint8_t* kd = smem + st * kStageBytes;
         convert_tile(codes, kd, c);
@@ -572,7 +621,7 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
         }
         fence_proxy_async_smem();  // generic-proxy writes, read by the tensor core
         mbar_arrive(&bars->kc_full[st]);
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], ph, p.err))) break;
+        if (!wait_all(&bars->v_full[st], ph, wc)) break;
         convert_tile(codes + kCodeTile, kd + kTileBytes, c);
         fence_proxy_async_smem();
         mbar_arrive(&bars->vc_full[st]);
@@ -588,48 +637,58 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
     EpSlot* slots = reinterpret_cast<EpSlot*>(smem + Y::kSlotOff);
     if (warp < 6) {
       // ---------------------------------------------------------- softmax
+      // Failures of waits are carried in `pending` (warp-uniform) to the next
+      // agreement barrier (barrier 1 over the 4 softmax warps, which also
+      // exchanges the row maxima), where all four warps go on or leave.
       const int my_row = lane >> (5 - kLog);  // row this lane holds after a reduction
       const bool row_writer = (lane & ((1 << (5 - kLog)) - 1)) == 0;
       float m_ref[NR], lsum[NR];
       int vis[NR];
-      Meta mt;
-      int g = 0, it_cnt = -1;
-      for (;; ++g) {
-        const int st = g % Y::kStages;
-        if (!wait_all(F8 ? &bars->kc_full[st] : &bars->k_full[st], (g / Y::kStages) & 1, p.err)) break;
-        const int mi = F8 ? (g & 3) : st;
-        const int flags = meta[mi].flags;
-        if (flags & kMetaDone) {
-          // tell the epilogue warps there are no more items
-          const int ob = (it_cnt + 1) & 1;
-          if (wait_all(&bars->ml_empty[ob], (((it_cnt + 1) >> 1) & 1) ^ 1, p.err)) {
-            if (t == 0) slots[ob].done = 1;
-            mbar_arrive(&bars->ml_full[ob]);
-          }
-          break;
-        }
-        if (flags & kMetaFirst) {
-          mt = meta[mi];
-          ++it_cnt;
 #pragma unroll
-          for (int r = 0; r < NR; ++r) {
-            m_ref[r] = -CUDART_INF_F;
-            lsum[r] = 0.f;
-            const int tok = (mt.row0 + r) / p.G;
-            vis[r] = r < mt.nrows ? min(mt.ke, p.causal ? mt.L - mt.n + tok + 1 : mt.L) : 0;
-          }
-        }
-        const int kbase = meta[mi].kbase;
+      for (int r = 0; r < NR; ++r) {
+        m_ref[r] = -CUDART_INF_F;
+        lsum[r] = 0.f;
+        vis[r] = 0;
+      }
+      Meta mt{};
+      int it_cnt = -1;
+      bool pending = false;
+      for (int g = 0;; ++g) {
+        const int st = g % Y::kStages;
+        const int mi = F8 ? (g & 3) : st;
         const int b = g & 1;
         float* redb = red + b * 4 * NR;  // [4 warps][NR], double-buffered by tile
-        if (!wait_all(&bars->s_full[b], (g >> 1) & 1, p.err)) break;
-        tc_fence_after();
+        // the stage's K (and metadata) arrived; the stage is not refilled
+        // before this tile's P.V, which needs this tile's P from these warps
+        bool fail = pending || !wait_all(F8 ? &bars->kc_full[st] : &bars->k_full[st], (g / Y::kStages) & 1, wc);
+        const int flags = fail ? 0 : meta[mi].flags;
+        const bool done = (flags & kMetaDone) != 0;
         uint32_t sraw[NR];
-        tmem_ld_rows<NR>(lane_base + kSCol + b * kN, sraw);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bars->s_free[b]);
-
+#pragma unroll
+        for (int r = 0; r < NR; ++r) sraw[r] = 0;
+        int kbase = 0;
+        if (!fail && !done) {
+          if (flags & kMetaFirst) {
+            mt = meta[mi];
+            ++it_cnt;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+              m_ref[r] = -CUDART_INF_F;
+              lsum[r] = 0.f;
+              const int tok = (mt.row0 + r) / p.G;
+              vis[r] = r < mt.nrows ? min(mt.ke, p.causal ? mt.L - mt.n + tok + 1 : mt.L) : 0;
+            }
+          }
+          kbase = meta[mi].kbase;
+          fail = !wait_all(&bars->s_full[b], (g >> 1) & 1, wc);
+          if (!fail) {
+            tc_fence_after();
+            tmem_ld_rows<NR>(lane_base + kSCol + b * kN, sraw);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bars->s_free[b]);
+          }
+        }
         // ---- masked logits of this thread's key; row maxima over the tile
         const int key = kbase + t;
         float v[NR], a[NR];
@@ -640,7 +699,17 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
         }
         const float wmax = xreduce<NR>(a, lane, MaxOp());
         if (row_writer) redb[q4 * NR + my_row] = wmax;
-        named_barrier(1, 128);
+        if (barrier_any(1, 128, fail || done)) {
+          // leaving: at the end of the work (nobody failed), tell the epilogue
+          if (!barrier_any(1, 128, fail)) {
+            const int ob = (it_cnt + 1) & 1;
+            if (wait_all(&bars->ml_empty[ob], (((it_cnt + 1) >> 1) & 1) ^ 1, wc)) {
+              if (t == 0) slots[ob].done = 1;
+              mbar_arrive(&bars->ml_full[ob]);
+            }
+          }
+          break;
+        }
         float alpha[NR], m_use[NR];
         bool any_rescale = false;
 #pragma unroll
@@ -658,38 +727,42 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
         any_rescale = any_rescale && !(flags & kMetaFirst);
 
         // ---- P (bf16) into this tile's P buffer: row r, column t, 128-byte swizzle
-        if (!wait_all(&bars->pv_done[b], ((g >> 1) & 1) ^ 1, p.err)) break;  // P.V of tile g-2 is done
+        pending = !wait_all(&bars->pv_done[b], ((g >> 1) & 1) ^ 1, wc);  // P.V of tile g-2 is done
         uint8_t* pbuf = smem + Y::kPOff + b * 2 * kQHalf + (t >> 6) * kQHalf;
         const int pchunk = (t & 63) >> 3, pbyte = (t & 7) * 2;
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
           const float e = fast_exp2(fmaf(v[r], p.scale_log2, -m_use[r]));
           lsum[r] = fmaf(lsum[r], alpha[r], e);
-          if constexpr (F8)
-            *reinterpret_cast<__half*>(pbuf + r * 128 + ((pchunk ^ (r & 7)) << 4) + pbyte) = __float2half_rn(e);
-          else
-            *reinterpret_cast<__nv_bfloat16*>(pbuf + r * 128 + ((pchunk ^ (r & 7)) << 4) + pbyte) =
-                __float2bfloat16_rn(e);
+          if (!pending) {
+            if constexpr (F8)
+              *reinterpret_cast<__half*>(pbuf + r * 128 + ((pchunk ^ (r & 7)) << 4) + pbyte) = __float2half_rn(e);
+            else
+              *reinterpret_cast<__nv_bfloat16*>(pbuf + r * 128 + ((pchunk ^ (r & 7)) << 4) + pbyte) =
+                  __float2bfloat16_rn(e);
+          }
         }
-        if (any_rescale) {
+        if (any_rescale && !pending) {
           // O^T must hold every earlier tile's P.V before it is scaled; thread t
           // owns O^T row t (output column t), whose column r belongs to row r
-          if (!wait_all(&bars->pv_done[b ^ 1], ((g - 1) >> 1) & 1, p.err)) break;
-          tc_fence_after();
-          const uint32_t ocol = lane_base + kOCol + (it_cnt & 1) * kN;
-          uint32_t o[NR];
-          tmem_ld_rows<NR>(ocol, o);
-          tmem_wait_ld();
+          pending = !wait_all(&bars->pv_done[b ^ 1], ((g - 1) >> 1) & 1, wc);
+          if (!pending) {
+            tc_fence_after();
+            const uint32_t ocol = lane_base + kOCol + (it_cnt & 1) * kN;
+            uint32_t o[NR];
+            tmem_ld_rows<NR>(ocol, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int r = 0; r < NR; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
-          tmem_st_rows<NR>(ocol, o);
-          tmem_wait_st();
+            for (int r = 0; r < NR; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+            tmem_st_rows<NR>(ocol, o);
+            tmem_wait_st();
+          }
         }
-        if (kbase + kKeys > mt.L) {
+        if (kbase + kKeys > mt.L && !pending) {
           // keys at or past the sequence's end hold arbitrary bits: zero their V
           // rows (after the tile has landed) so that 0 * V stays 0
-          if (!wait_all(F8 ? &bars->vc_full[st] : &bars->v_full[st], (g / Y::kStages) & 1, p.err)) break;
-          if (key >= mt.L) {
+          pending = !wait_all(F8 ? &bars->vc_full[st] : &bars->v_full[st], (g / Y::kStages) & 1, wc);
+          if (!pending && key >= mt.L) {
             uint4* v0 = reinterpret_cast<uint4*>(smem + st * kStageBytes + kTileBytes + t * 128);
             uint4* v1 = reinterpret_cast<uint4*>(smem + st * kStageBytes + kTileBytes + kHalf + t * 128);
 #pragma unroll
@@ -710,31 +783,38 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
           const float wsum = xreduce<NR>(c, lane, AddOp());
           if (row_writer) reds[q4 * NR + my_row] = wsum;
         }
-        named_barrier(1, 128);
+        if (barrier_any(1, 128, pending)) break;
         const int ob = it_cnt & 1;
-        if (!wait_all(&bars->ml_empty[ob], ((it_cnt >> 1) & 1) ^ 1, p.err)) break;
-        EpSlot& es = slots[ob];
+        pending = !wait_all(&bars->ml_empty[ob], ((it_cnt >> 1) & 1) ^ 1, wc);
+        if (!pending) {
+          EpSlot& es = slots[ob];
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          if (t == r) {
-            es.m[r] = m_ref[r];
-            es.l[r] = (reds[r] + reds[NR + r]) + (reds[2 * NR + r] + reds[3 * NR + r]);
+          for (int r = 0; r < NR; ++r) {
+            if (t == r) {
+              es.m[r] = m_ref[r];
+              es.l[r] = (reds[r] + reds[NR + r]) + (reds[2 * NR + r] + reds[3 * NR + r]);
+            }
+          }
+          if (t == 0) {
+            es.mt = mt;
+            es.done = 0;
           }
         }
-        if (t == 0) {
-          es.mt = mt;
-          es.done = 0;
-        }
-        named_barrier(1, 128);  // reds[] is rewritten two tiles from now; the slot is complete
+        // reds[] is rewritten two tiles from now; the slot is complete
+        if (barrier_any(1, 128, pending)) break;
         mbar_arrive(&bars->ml_full[ob]);
       }
     } else {
       // ---------------------------------------------------------- epilogue
+      // Over the 4 epilogue warps, barrier 3: agreement after each wait that
+      // decides what they do next; barrier 2: the split tickets' ordering.
       const int d = t;
       int* flag_last = reinterpret_cast<int*>(tmem_slot + 1);
+      bool pending = false;
       for (int it_cnt = 0;; ++it_cnt) {
         const int ob = it_cnt & 1;
-        if (!wait_all(&bars->ml_full[ob], (it_cnt >> 1) & 1, p.err)) break;
+        const bool fail = pending || !wait_all(&bars->ml_full[ob], (it_cnt >> 1) & 1, wc);
+        if (barrier_any(3, 128, fail)) break;
         const EpSlot& es = slots[ob];
         if (es.done) break;
         const Meta mt = es.mt;
@@ -745,15 +825,18 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
           lrow[r] = r < mt.nrows ? es.l[r] : 1.f;
         }
         mbar_arrive(&bars->ml_empty[ob]);
-        if (!wait_all(&bars->o_full[ob], (it_cnt >> 1) & 1, p.err)) break;
-        tc_fence_after();
+        pending = !wait_all(&bars->o_full[ob], (it_cnt >> 1) & 1, wc);
         uint32_t o[NR];
-        tmem_ld_rows<NR>(lane_base + kOCol + ob * kN, o);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bars->o_empty[ob]);
+        if (!pending) {
+          tc_fence_after();
+          tmem_ld_rows<NR>(lane_base + kOCol + ob * kN, o);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&bars->o_empty[ob]);
+        }
         const int nr = mt.nrows;
         if (mt.part < 0) {
+          if (pending) continue;  // leaves at the next agreement
           // The item finishes its rows.  With a merge group it follows a
           // shared prefix, whose partial rows (complete before this kernel
           // started) are folded in: m = max, weights 2^(m_p - m).
@@ -792,11 +875,13 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
           }
           continue;
         }
+        if (!pending) {
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          if (r < nr) {
-            p.part_acc[(int64_t)(mt.part + r) * 128 + d] = __uint_as_float(o[r]);
-            if (d == r) p.part_ml[mt.part + r] = make_float2(mrow[r], lrow[r]);
+          for (int r = 0; r < NR; ++r) {
+            if (r < nr) {
+              p.part_acc[(int64_t)(mt.part + r) * 128 + d] = __uint_as_float(o[r]);
+              if (d == r) p.part_ml[mt.part + r] = make_float2(mrow[r], lrow[r]);
+            }
           }
         }
         // The split that completes its merge group combines the group's
@@ -804,7 +889,7 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
         // Release: the barrier orders every thread's partial writes before
         // thread 0's fence and ticket; acquire: thread 0's fence after the
         // ticket, then the barrier, before anyone reads other splits' rows.
-        named_barrier(2, 128);
+        if (barrier_any(3, 128, pending)) break;
         if (d == 0) {
           __threadfence();
           *flag_last = atomicAdd(p.tickets + mt.grp, 1);

@@ -17,12 +17,14 @@
 // chunk), so that the attention kernels, which take items in list order,
 // end with small ones and finish together.
 //
-// One CTA.  The unit instances (kv head, sequence, row unit) are numbered
-// kv head major, each sequence's units contiguous (per-sequence unit offsets
-// in shared memory); each thread walks a contiguous range of that numbering,
-// so that a long prefill sequence's many units spread over many threads.
-// Block-wide exclusive scans give every item a fixed slot (items ordered by
-// size class, then unit instance, then split).
+// One CTA.  The unit instances (sequence, row unit), each standing for all
+// kv heads, are numbered with each sequence's units contiguous (per-sequence
+// unit offsets in shared memory); each thread walks a contiguous range of
+// that numbering, so that a long prefill sequence's many units spread over
+// many threads.  Block-wide exclusive scans give every item a fixed slot
+// (items ordered by size class, then unit instance, then split, then kv
+// head: the kv heads of one key range are adjacent in the queue, so the CTAs
+// that take them read the same pool rows at about the same time).
 //
 // Shared prefixes (when the call asks for them): consecutive decode-shaped
 // sequences whose block tables start with the same physical blocks read
@@ -142,16 +144,16 @@ __device__ void block_scan(int (&v)[K], int (&totals)[K]) {
   __syncthreads();
 }
 
-// Walks a contiguous range of unit instances i = kvh * U + seq_off[s] + u.
+// Walks a contiguous range of unit instances i = seq_off[s] + u (a unit of
+// rows of one sequence; each stands for its Hkv kv heads).
 struct UnitIter {
-  int i, end, U, B, kvh, s, u;
+  int i, end, B, s, u;
   SeqDesc d;
 };
 
 __device__ __forceinline__ void iter_seek(UnitIter& t, const PlanParams& p, const int* seq_off) {
   if (t.i >= t.end) return;
-  t.kvh = t.i / t.U;
-  const int j = t.i - t.kvh * t.U;
+  const int j = t.i;
   int lo = 0, hi = t.B - 1;  // the last sequence whose first unit is <= j
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -166,14 +168,8 @@ __device__ __forceinline__ void iter_next(UnitIter& t, const PlanParams& p, cons
   ++t.i;
   if (t.i >= t.end) return;
   if (++t.u < t.d.units) return;
-  // next sequence with units (or the next kv head's first one)
-  int s = t.s + 1;
+  int s = t.s + 1;  // the next sequence with units
   while (s < t.B && seq_off[s + 1] == seq_off[s]) ++s;
-  if (s >= t.B) {
-    ++t.kvh;
-    s = 0;
-    while (seq_off[s + 1] == seq_off[s]) ++s;
-  }
   t.s = s;
   t.u = 0;
   t.d = describe(p, s);
@@ -396,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
     __syncthreads();
   }
   const int U = seq_off[B];
-  const int N = U * p.Hkv;  // unit instances
+  const int N = U;  // unit instances, each for all kv heads
   const int per_thread = (N + kThreads - 1) / kThreads;
   const int i0 = min(N, tid * per_thread), i1 = min(N, i0 + per_thread);
 
@@ -407,9 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   __shared__ int sh_state;
   unsigned long long w_dec = 0, w_mma = 0;
   {
-    UnitIter t{i0, i1, U, B, 0, 0, 0, {}};
+    UnitIter t{i0, i1, B, 0, 0, {}};
     for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off))
-      (t.d.mma ? w_mma : w_dec) += (unsigned long long)(unit_keys(t.d, t.u, p.G, p.causal) - t.d.pre);
+      (t.d.mma ? w_mma : w_dec) += (unsigned long long)(unit_keys(t.d, t.u, p.G, p.causal) - t.d.pre) * p.Hkv;
   }
   // warp sums, then one thread adds the warps' (no contended 64-bit atomics)
 #pragma unroll
@@ -478,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
     const int cd = sh_chunk[0], cm = sh_chunk[1];
 #pragma unroll
     for (int k = 0; k < kNumCounts; ++k) s_cnt[k][tid] = 0;
-    UnitIter t{i0, i1, U, B, 0, 0, 0, {}};
+    UnitIter t{i0, i1, B, 0, 0, {}};
     for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off)) {
       const SeqDesc& d = t.d;
       const int chunk = d.mma ? cm : cd;
@@ -486,12 +482,13 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       const int keys = unit_keys(d, t.u, p.G, p.causal) - d.pre;
       int ns, per;
       split_of(keys, chunk, d.mma ? kMmaTileKeys : p.dec_tile_keys, ns, per);
-      s_cnt[cb + size_class(per, chunk)][tid] += ns - 1;  // all splits but the last are full
-      s_cnt[cb + size_class(keys - (ns - 1) * per, chunk)][tid] += 1;
+      s_cnt[cb + size_class(per, chunk)][tid] += (ns - 1) * p.Hkv;  // all splits but the last are full
+      s_cnt[cb + size_class(keys - (ns - 1) * per, chunk)][tid] += p.Hkv;
       if (ns > 1 || d.pre > 0) {
-        s_cnt[kCntMerge][tid] += 1;
+        s_cnt[kCntMerge][tid] += p.Hkv;
         if (ns > 1)
-          s_cnt[d.mma ? kCntPartMma : kCntPartDec][tid] += ns * min(d.rows - t.u * d.unit_rows, d.unit_rows);
+          s_cnt[d.mma ? kCntPartMma : kCntPartDec][tid] +=
+              p.Hkv * ns * min(d.rows - t.u * d.unit_rows, d.unit_rows);
       }
     }
 #pragma unroll
@@ -574,10 +571,10 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   int off_grp = cnt[kCntMerge];
   int off_part = cnt[kCntPartDec] + cnt[kCntPartMma];
   {
-    UnitIter t{i0, i1, U, B, 0, 0, 0, {}};
+    UnitIter t{i0, i1, B, 0, 0, {}};
     for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off)) {
       const SeqDesc& d = t.d;
-      const int s = t.s, kvh = t.kvh, u = t.u;
+      const int s = t.s, u = t.u;
       WorkItem* items = d.mma ? p.mma_items : p.dec_items;
       const int chunk = d.mma ? cm : cd;
       const int cbase = d.mma ? kClasses : 0;
@@ -587,49 +584,57 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       const int nr = min(d.rows - r0, d.unit_rows);
       int ns, per;
       split_of(keys, chunk, d.mma ? kMmaTileKeys : p.dec_tile_keys, ns, per);
-      int grp = -1, part_base = 0;
-      if (ns > 1 || d.pre > 0) {
-        // A unit after a shared prefix always names a merge group (where its
-        // prefix partials are); unsplit, its one item folds them in itself.
-        grp = off_grp++;
-        if (ns > 1) {
-          part_base = off_part;
-          off_part += ns * nr;
+      // one merge group per kv head when split (or after a shared prefix)
+      const bool grouped = ns > 1 || d.pre > 0;
+      const int grp0 = grouped ? off_grp : -1;
+      const int part0 = off_part;
+      if (grouped) {
+        off_grp += p.Hkv;
+        if (ns > 1) off_part += p.Hkv * ns * nr;
+        for (int kvh = 0; kvh < p.Hkv; ++kvh) {
+          // A unit after a shared prefix always names a merge group (where its
+          // prefix partials are); unsplit, its one item folds them in itself.
+          MergeGroup g;
+          g.seq = s;
+          g.kvh = kvh;
+          g.row0 = r0;
+          g.nrows = nr;
+          g.nsplit = ns;
+          g.part_base = ns > 1 ? part0 + kvh * ns * nr : 0;
+          g.pre_base = 0;
+          g.pre_n = 0;
+          g.pre_stride = 0;
+          g.pad0 = g.pad1 = g.pad2 = 0;
+          if (d.pre > 0) {
+            // this unit's rows in its group's prefix partials ([kvh][chunk][row])
+            const int npre = d.pre_shape >> 24, grows = d.pre_shape & 0xffffff;
+            g.pre_base = pre_part_base + d.pre_rel + kvh * npre * grows + r0;
+            g.pre_n = npre;
+            g.pre_stride = grows;
+          }
+          p.merges[grp0 + kvh] = g;
+          p.tickets[grp0 + kvh] = 0;
         }
-        MergeGroup g;
-        g.seq = s;
-        g.kvh = kvh;
-        g.row0 = r0;
-        g.nrows = nr;
-        g.nsplit = ns;
-        g.part_base = part_base;
-        g.pre_base = 0;
-        g.pre_n = 0;
-        g.pre_stride = 0;
-        g.pad0 = g.pad1 = g.pad2 = 0;
-        if (d.pre > 0) {
-          // this unit's rows in its group's prefix partials ([kvh][chunk][row])
-          const int npre = d.pre_shape >> 24, grows = d.pre_shape & 0xffffff;
-          g.pre_base = pre_part_base + d.pre_rel + kvh * npre * grows + r0;
-          g.pre_n = npre;
-          g.pre_stride = grows;
-        }
-        p.merges[grp] = g;
-        p.tickets[grp] = 0;
       }
       const int full_cls = cbase + size_class(per, chunk);
       const int last_cls = cbase + size_class(keys - (ns - 1) * per, chunk);
+      // split-major, kv head minor: the kv heads of one key range sit next to
+      // each other in the queue, so the CTAs that take them read the same
+      // pool rows (one token's row holds every kv head) at about the same
+      // time, which keeps the DRAM accesses of a block together
       for (int sp = 0; sp < ns; ++sp) {
-        WorkItem it;
-        it.seq = s;
-        it.kvh = kvh;
-        it.row0 = r0;
-        it.nrows = nr;
-        it.kb = d.pre + sp * per;
-        it.ke = min(kend, d.pre + (sp + 1) * per);
-        it.part = ns > 1 ? part_base + sp * nr : -1;
-        it.grp = grp;
-        items[s_cnt[sp == ns - 1 ? last_cls : full_cls][tid]++] = it;
+        for (int kvh = 0; kvh < p.Hkv; ++kvh) {
+          WorkItem it;
+          it.seq = s;
+          it.kvh = kvh;
+          it.row0 = r0;
+          it.nrows = nr;
+          it.kb = d.pre + sp * per;
+          it.ke = min(kend, d.pre + (sp + 1) * per);
+          it.part = ns > 1 ? part0 + kvh * ns * nr + sp * nr : -1;
+          it.grp = grouped ? grp0 + kvh : -1;
+          items[s_cnt[sp == ns - 1 ? last_cls : full_cls][tid]++] = it;
+        }
       }
     }
   }

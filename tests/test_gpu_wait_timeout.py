@@ -7,6 +7,7 @@ default 2 s, and the next ordinary call on the same device must match the
 fp64 oracle."""
 import time
 
+import numpy as np
 import pytest
 import torch
 
@@ -49,4 +50,55 @@ def test_cuda_core_decode_wait_runs_out(fault_tile):
     out = pkv.paged_attention_forward(t["q"], dw.kc, dw.vc, t["bt"], t["ctx"], t["qsl"], w.scale, True)
     torch.cuda.synchronize()
     check_step(dw, out, what="after the fault")
+    assert pkv.device_errors() == 0
+
+
+def _decode_batch(seed):
+    return wl.build("timeout-tc", context_lens=[2600 - 13 * i for i in range(64)], q_lens=[1] * 64,
+                    num_blocks=64 * 163 + 8, block_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                    dtype="bf16", seed=seed, poison=True)
+
+
+@pytest.mark.parametrize("fault_tile", [1, 2, 4])
+def test_tensor_core_decode_wait_runs_out(fault_tile):
+    """bf16, head_dim 128 with the query-length hint: the tensor-core decode
+    kernel (K and V producers, item fetch, the MMA thread, four softmax and
+    four epilogue warps that settle every wait across the group)."""
+    dw = DeviceWorkload(_decode_batch(72))
+    out = dw.run_step(0, max_query_len=1)
+    check_step(dw, out, what="before the fault")
+    flags, secs = _run_with_fault(dw, fault_tile, max_query_len=1)
+    assert flags & pkv.DEVERR["timeout"], f"no timeout recorded (flags {flags:#x})"
+    assert secs < 1.5, f"the call took {secs:.2f} s: the short limit was not used"
+    st = dw.w.step
+    t = dw.step_tensors(st)
+    out = pkv.paged_attention_forward(t["q"], dw.kc, dw.vc, t["bt"], t["ctx"], t["qsl"], dw.w.scale, True,
+                                      max_query_len=1)
+    torch.cuda.synchronize()
+    check_step(dw, out, what="after the fault")
+    assert pkv.device_errors() == 0
+
+
+@pytest.mark.parametrize("fault_tile", [1, 3])
+def test_tensor_core_decode_fp8_wait_runs_out(fault_tile):
+    """FP8 pools with the query-length hint: the same kernel with its K and V
+    converter warps between the staged codes and the MMAs."""
+    from test_gpu_fp8 import Fp8Run
+    run = Fp8Run(_decode_batch(73), 0.02, 0.015)
+    run.check(run.step(max_query_len=1), what="before the fault")
+    st = run.w.step
+    q = torch.from_numpy(st.q.view(np.int16)).cuda().view(torch.bfloat16)
+    args = (q, run.kc, run.vc, torch.from_numpy(st.block_tables).cuda(), torch.from_numpy(st.context_lens).cuda(),
+            torch.from_numpy(st.query_start_loc).cuda(), run.w.scale, run.ks, run.vs, True)
+    pkv.device_errors(clear=True)
+    pkv.debug_fault(fault_tile, LIMIT_NS)
+    t0 = time.perf_counter()
+    pkv.paged_attention_forward_fp8kv(*args, max_query_len=1)
+    flags = pkv.device_errors(clear=True)
+    secs = time.perf_counter() - t0
+    assert flags & pkv.DEVERR["timeout"], f"no timeout recorded (flags {flags:#x})"
+    assert secs < 1.5, f"the call took {secs:.2f} s"
+    out = pkv.paged_attention_forward_fp8kv(*args, max_query_len=1)
+    torch.cuda.synchronize()
+    run.check(out, what="after the fault")
     assert pkv.device_errors() == 0
