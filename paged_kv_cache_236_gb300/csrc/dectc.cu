@@ -32,11 +32,12 @@
 //             P.V of tile g is issued after the S of tile g+1;
 //   warps 2-5 softmax (thread = key = TMEM lane);
 //   warps 6-9 epilogue (thread = output column = TMEM lane of O^T);
-//   warp 10   item fetch: one item ahead, it reads each item's record,
-//             its sequence's length and query offset and the block ids of
-//             its first tile into a slot in shared memory, so that the
-//             producers start an item's loads without a chain of dependent
-//             global reads.
+//   warp 10   item fetch: shortly before the K producer needs the next item
+//             (two tiles before the end of the current one), it takes it
+//             from the queue and reads its record, its sequence's length and
+//             query offset and the block ids of its first tile into a slot
+//             in shared memory, so that the producers start an item's loads
+//             without a chain of dependent global reads.
 // Shared memory: 3 stages of K+V (192 KB), 2 Q tiles and 2 P tiles (4 KB
 // each).  TMEM: S^T double-buffered in columns [0,32), O^T in [32,48).
 //
@@ -81,7 +82,12 @@ constexpr int kTileBytes = kKeys * 128 * 2;    // one of K or V: 32 KB
 constexpr int kStageBytes = 2 * kTileBytes;
 constexpr int kCodeTile = kKeys * 128;         // one of K or V as E4M3 codes: 16 KB
 constexpr int kQHalf = kN * 128;               // one 64-column half of the Q / P tiles (2 KB)
-constexpr int kNumBars = 5 * kMaxStages + 2 * 8 + 4 + 2;
+constexpr int kNumBars = 5 * kMaxStages + 2 * 8 + 4 + 2 + 1;
+// The K producer asks for the next item when this many tiles of the current
+// one are left to load: early enough to hide the fetch (a few dependent
+// global reads), late enough that an SM does not hold an item for long
+// while others fall idle at the end of the queue.
+constexpr int kFetchLeadTiles = 2;
 
 // Shared-memory layout.  bf16 pools: 3 stages of K+V.  FP8 pools: 2 stages
 // of fp16 K+V (what the MMAs read) and 2 stages of staged codes (what TMA
@@ -133,6 +139,7 @@ struct Bars {
   uint64_t o_full[2], o_empty[2], ml_full[2], ml_empty[2];
   uint64_t islot_full[2], islot_free[2];
   uint64_t stage_empty[2];  // FP8: a staging slot's codes converted (the producers may refill it)
+  uint64_t fetch_go;        // phase c: the K producer is near the end of item c (fetch item c + 1)
 };
 
 // An item as the item-fetch warp hands it to the producer.
@@ -298,6 +305,7 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
       mbar_init(&bars->ml_empty[b], 128);
       mbar_init(&bars->islot_full[b], 32);
       mbar_init(&bars->islot_free[b], 2);  // both producers read the slot
+      if (b == 0) mbar_init(&bars->fetch_go, 1);
       mbar_init(&bars->stage_empty[b], 128);
     }
     *abort_flag = 0;
@@ -395,6 +403,9 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
           ok = false;
           break;
         }
+        if (!vprod && lane == 0 && it.ke - kbase <= kFetchLeadTiles * kKeys &&
+            (first || it.ke - (kbase - kKeys) > kFetchLeadTiles * kKeys))
+          mbar_arrive(&bars->fetch_go);  // once per item: the next one may be taken now
         if (!vprod && p.fault_tile == g + 1 && blockIdx.x == 0) {
           // testing only: this tile is never loaded, so the waits for it run out
           phys = next_phys;
@@ -468,11 +479,13 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
     ItemSlot* islots = reinterpret_cast<ItemSlot*>(smem + Y::kISlotOff);
     for (int c = 0;; ++c) {
       const int qb = c & 1;
-      // Item c is taken from the queue once the producers have taken item
-      // c-1 (and so item c-2, freeing slot qb): one item waits while one is
-      // loaded.  Taking items no earlier keeps the queue's largest-first
-      // order close to the order in which the SMs fall idle.
-      if (c >= 1 && !wait_all(&bars->islot_free[(c - 1) & 1], ((c - 1) >> 1) & 1, wc)) break;
+      // Item c is taken from the queue when the K producer is within
+      // kFetchLeadTiles tiles of the end of item c-1, and once both
+      // producers have taken item c-2 (freeing slot qb).  Taking items no
+      // earlier keeps the queue's largest-first order close to the order in
+      // which the SMs fall idle, so the SMs finish together.
+      if (c >= 1 && !wait_all(&bars->fetch_go, (c - 1) & 1, wc)) break;
+      if (c >= 2 && !wait_all(&bars->islot_free[(c - 2) & 1], ((c - 2) >> 1) & 1, wc)) break;
       int idx = 0;
       if (lane == 0) idx = atomicAdd(p.counter, 1);
       idx = __shfl_sync(0xffffffffu, idx, 0);
