@@ -1,8 +1,10 @@
 #!/usr/bin/env python
 """Benchmark of the paged-KV hot path on GB300.
 
-One step = one pass of the whole hot path over one batch: paged_kv_write of
-the batch's new K/V rows, then paged_attention_forward over the block pool.
+One step = one pass of the whole hot path over one batch: the write of the
+batch's new K/V rows into the block pool, then attention over it, through
+paged_kv_write_attention_forward (one call; the write runs in the planner's
+launch).
 Default workload: the decode batch (64 sequences, contexts U[512, 4096], one
 query token each, 32 q / 8 kv heads, head_dim 128, block_size 16, bf16, a
 20000-block pool, seeded random block permutation).  Also measured (extra
@@ -117,19 +119,20 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
 
 
 def launches_per_step(w, max_q_len: int, shared_prefix: bool, fp8: bool = False) -> int:
-    """Our kernels per step, as paged_attention_forward chooses them: the K/V
-    write, [the shared-prefix search], the planner, [the tensor-core kernel],
-    the decode-shaped kernel (split merges run inside the attention kernels).
-    FP8 pools: the write, the planner and one decode kernel."""
+    """Our kernels per step, as paged_kv_write_attention_forward chooses them:
+    [the shared-prefix search], the planner (whose extra CTAs write the new
+    K/V rows), [the tensor-core kernel], the decode-shaped kernel (split
+    merges run inside the attention kernels).  FP8 pools: the planner with
+    the write, and one decode kernel."""
     if fp8:
-        return 3
+        return 2
     g = w.num_q_heads // w.num_kv_heads
     tc = w.dtype == "bf16" and w.head_dim == 128 and g & (g - 1) == 0
     dectc = tc and g <= 16
     dec_rows = 16 if dectc else 4
     cascade = shared_prefix and dectc
     mma = tc and (cascade or not (max_q_len > 0 and max_q_len * g <= dec_rows))
-    return 3 + int(cascade) + int(mma)
+    return 2 + int(cascade) + int(mma)
 
 
 class ClockSampler:
@@ -235,15 +238,15 @@ def run_gpu(args, rank, world, local_rank):
                                             w.head_dim), dtype=torch.uint8, device=dev)
 
         def one():
+            # the step's write and attention in one call (the write in the planner's launch)
             if t["fp8"]:
-                pkv.paged_kv_write_fp8(t["k"], t["v"], t["slots"], t["kc"], t["vc"], FP8_SCALE, FP8_SCALE)
-                pkv.paged_attention_forward_fp8kv(t["q"], t["kc"], t["vc"], t["bt"], t["ctx"], t["qsl"], w.scale,
-                                                  FP8_SCALE, FP8_SCALE, w.causal, out=out, workspace=ws,
-                                                  max_query_len=t["mql"])
+                pkv.paged_kv_write_attention_forward_fp8kv(t["k"], t["v"], t["slots"], t["q"], t["kc"], t["vc"],
+                                                           t["bt"], t["ctx"], t["qsl"], w.scale, FP8_SCALE, FP8_SCALE,
+                                                           w.causal, out=out, workspace=ws, max_query_len=t["mql"])
                 return
-            pkv.paged_kv_write(t["k"], t["v"], t["slots"], t["kc"], t["vc"])
-            pkv.paged_attention_forward(t["q"], t["kc"], t["vc"], t["bt"], t["ctx"], t["qsl"], w.scale, w.causal,
-                                        out=out, workspace=ws, max_query_len=t["mql"], shared_prefix=t["sp"])
+            pkv.paged_kv_write_attention_forward(t["k"], t["v"], t["slots"], t["q"], t["kc"], t["vc"], t["bt"],
+                                                 t["ctx"], t["qsl"], w.scale, w.causal, out=out, workspace=ws,
+                                                 max_query_len=t["mql"], shared_prefix=t["sp"])
 
         for _ in range(warmup):
             flush.fill_(1)
@@ -350,15 +353,14 @@ def run_gpu(args, rank, world, local_rank):
         a.record()
         dev_buf.copy_(host_buf, non_blocking=True)
         if fp8:
-            pkv.paged_kv_write_fp8(d["k"], d["v"], d["slots"], t["kc"], t["vc"], FP8_SCALE, FP8_SCALE)
-            o = pkv.paged_attention_forward_fp8kv(d["q"], t["kc"], t["vc"], d["bt"], d["ctx"], d["qsl"], w.scale,
-                                                  FP8_SCALE, FP8_SCALE, w.causal, out=out_dev, workspace=ws,
-                                                  max_query_len=t["mql"])
+            o = pkv.paged_kv_write_attention_forward_fp8kv(d["k"], d["v"], d["slots"], d["q"], t["kc"], t["vc"],
+                                                           d["bt"], d["ctx"], d["qsl"], w.scale, FP8_SCALE,
+                                                           FP8_SCALE, w.causal, out=out_dev, workspace=ws,
+                                                           max_query_len=t["mql"])
         else:
-            pkv.paged_kv_write(d["k"], d["v"], d["slots"], t["kc"], t["vc"])
-            o = pkv.paged_attention_forward(d["q"], t["kc"], t["vc"], d["bt"], d["ctx"], d["qsl"], w.scale,
-                                            w.causal, out=out_dev, workspace=ws, max_query_len=t["mql"],
-                                            shared_prefix=t["sp"])
+            o = pkv.paged_kv_write_attention_forward(d["k"], d["v"], d["slots"], d["q"], t["kc"], t["vc"], d["bt"],
+                                                     d["ctx"], d["qsl"], w.scale, w.causal, out=out_dev,
+                                                     workspace=ws, max_query_len=t["mql"], shared_prefix=t["sp"])
         host_out.copy_(o, non_blocking=True)
         b.record()
         b.synchronize()
@@ -372,7 +374,8 @@ def run_gpu(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(tot_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC[args.workload],
-                   "step": "paged_kv_write of the batch's new K/V rows + paged_attention_forward",
+                   "step": "paged_kv_write_attention_forward: the write of the batch's new K/V rows and the "
+                           "attention in one call (the write runs in the planner's launch)",
                    "l2": "flushed between steps (512 MB write outside the timed events)",
                    "bytes_per_step": ab["step"], "kv_bytes": ab["kv"], "query_tokens": w.step.num_tokens,
                    "parallelism": f"replicas x{world}"},

@@ -185,6 +185,35 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
                                    pkv_dtype dtype, void* stream);
 
 /*
+ * paged_kv_write_attention_forward - paged_kv_write of a step's new K/V rows
+ * followed by paged_attention_forward over the pools, in one call and one
+ * launch fewer ("ADR 004", Consequences: the model writes a layer's new K/V
+ * and then attends, prefill and decode alike).  The results are those of the
+ * two calls made in that order on `stream`.
+ *
+ *   k, v, slot_mapping, num_new_tokens, k_token_stride, v_token_stride
+ *                   the new rows, as paged_kv_write takes them ([num_new_tokens,
+ *                   num_kv_heads, head_dim] of `dtype`, strides in elements, 0
+ *                   means dense; slots < 0 skipped)
+ *   the rest        as paged_attention_forward
+ * When every row start is 16-byte aligned, the rows are copied by extra CTAs
+ * of the planner's launch (the attention kernels wait for that launch, so
+ * they read the new rows); otherwise the write kernel runs first.  Errors as
+ * for the two calls (the write's arguments are checked before any launch).
+ */
+pkv_status paged_kv_write_attention_forward(const void* k, const void* v, const int64_t* slot_mapping,
+                                            int64_t num_new_tokens, int64_t k_token_stride,
+                                            int64_t v_token_stride, const void* q, const void* k_cache,
+                                            const void* v_cache, const int32_t* block_tables,
+                                            const int32_t* context_lens, const int32_t* query_start_loc,
+                                            void* out, int32_t num_seqs, int64_t num_tokens,
+                                            int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                            int64_t num_blocks, int32_t block_size, int32_t max_blocks_per_seq,
+                                            int32_t max_query_len, float scale, int32_t causal, int32_t hints,
+                                            void* workspace, size_t workspace_bytes, pkv_dtype dtype,
+                                            void* stream);
+
+/*
  * paged_attention_forward_static_ws - paged_attention_forward for callers
  * that cannot allocate device memory (no counterpart on the source pages).
  *
@@ -263,6 +292,22 @@ pkv_status paged_attention_forward_fp8kv(const void* q, const void* k_cache, con
                                          int32_t max_query_len, float scale, int32_t causal,
                                          float k_scale, float v_scale, int32_t hints, void* workspace,
                                          size_t workspace_bytes, void* stream);
+
+/*
+ * paged_kv_write_attention_forward_fp8kv - paged_kv_write_fp8 of a step's new
+ * rows (of row_dtype, bf16 or f32, 16-byte aligned with strides of multiples
+ * of 16 bytes) followed by paged_attention_forward_fp8kv, in one call; the
+ * rows are encoded by extra CTAs of the planner's launch.  Arguments and
+ * errors as for the two calls.
+ */
+pkv_status paged_kv_write_attention_forward_fp8kv(
+    const void* k, const void* v, const int64_t* slot_mapping, int64_t num_new_tokens, int64_t k_token_stride,
+    int64_t v_token_stride, pkv_dtype row_dtype, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, const int32_t* query_start_loc, void* out,
+    int32_t num_seqs, int64_t num_tokens, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int64_t num_blocks, int32_t block_size, int32_t max_blocks_per_seq, int32_t max_query_len, float scale,
+    int32_t causal, float k_scale, float v_scale, int32_t hints, void* workspace, size_t workspace_bytes,
+    void* stream);
 
 /* Bytes of the static scratch used by paged_attention_forward_static_ws. */
 size_t paged_attention_static_workspace_bytes(void);

@@ -32,6 +32,7 @@ __all__ = [
     "paged_kv_write", "paged_attention_forward", "workspace_size", "workspace_min",
     "device_errors", "debug_fault", "set_profile_events", "profile_elapsed_ms", "lib", "LibraryError", "DEVERR",
     "BlockManager", "OutOfBlocks", "copy_blocks", "paged_kv_write_fp8", "paged_attention_forward_fp8kv",
+    "paged_kv_write_attention_forward", "paged_kv_write_attention_forward_fp8kv",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -104,6 +105,13 @@ def lib() -> ctypes.CDLL:
             L.pkv_version.argtypes = []
             L.pkv_debug_fault.restype = c_i32
             L.pkv_debug_fault.argtypes = [c_i32, c_i64]
+            L.paged_kv_write_attention_forward.restype = c_i32
+            L.paged_kv_write_attention_forward.argtypes = [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64] + \
+                L.paged_attention_forward.argtypes
+            L.paged_kv_write_attention_forward_fp8kv.restype = c_i32
+            L.paged_kv_write_attention_forward_fp8kv.argtypes = [
+                c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i64,
+                c_i32, c_i32, c_i32, c_i64, c_i32, c_i32, c_i32, c_f, c_i32, c_f, c_f, c_i32, c_vp, c_sz, c_vp]
             c_p32 = ctypes.POINTER(c_i32)
             for name, args in (
                     ("pkv_bm_create", [c_i32, c_i32, c_i32, ctypes.POINTER(c_vp)]),
@@ -211,6 +219,16 @@ def paged_attention_forward(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     their common prefix once (``PKV_HINT_SHARED_PREFIX``).
     """
     dev = _need_cuda(q, k_cache, v_cache, block_tables, context_lens, query_start_loc)
+    args, out = _forward_args(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale, causal, out,
+                              workspace, max_query_len, shared_prefix, dev)
+    with torch.cuda.device(dev):
+        _check(lib().paged_attention_forward(*args))
+    return out
+
+
+def _forward_args(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale, causal, out, workspace,
+                  max_query_len, shared_prefix, dev) -> tuple:
+    """Checks paged_attention_forward's tensors; returns (its C arguments, out)."""
     if q.dtype not in DTYPE or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
         raise ValueError("q, k_cache, v_cache must share dtype bfloat16 or float32")
     if q.dim() != 3 or not q.is_contiguous():
@@ -241,11 +259,45 @@ def paged_attention_forward(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
             workspace = _workspace(dev, workspace_size(B, T, Hq, Hkv, D))
         if workspace.dtype != torch.uint8 or workspace.device != dev or workspace.numel() < need:
             raise ValueError(f"workspace must be a uint8 CUDA tensor of at least {need} bytes")
-        _check(lib().paged_attention_forward(
-            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
-            context_lens.data_ptr(), query_start_loc.data_ptr(), out.data_ptr(), B, T, Hq, Hkv, D, NB, bs,
-            max(1, block_tables.shape[1]), int(max_query_len), float(scale), 1 if causal else 0,
-            HINT_SHARED_PREFIX if shared_prefix else 0, workspace.data_ptr(), workspace.numel(), DTYPE[q.dtype], _stream(dev)))
+    args = (q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
+            query_start_loc.data_ptr(), out.data_ptr(), B, T, Hq, Hkv, D, NB, bs, max(1, block_tables.shape[1]),
+            int(max_query_len), float(scale), 1 if causal else 0, HINT_SHARED_PREFIX if shared_prefix else 0,
+            workspace.data_ptr(), workspace.numel(), DTYPE[q.dtype], _stream(dev))
+    return args, out
+
+
+def _new_rows(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, Hkv: int, D: int, dtypes) -> tuple:
+    """Checks a step's new K/V rows [T, Hkv, D] (contiguous heads) and returns
+    (T, k token stride, v token stride)."""
+    if k.dtype not in dtypes or v.dtype != k.dtype:
+        raise ValueError("k and v must share a dtype the pools accept")
+    T = k.shape[0]
+    for name, t in (("k", k), ("v", v)):
+        if t.dim() != 3 or tuple(t.shape[1:]) != (Hkv, D) or t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError(f"{name} must be [T, {Hkv}, {D}] with contiguous heads")
+    if v.shape[0] != T or slot_mapping.shape != (T,) or slot_mapping.dtype != torch.int64 or \
+            not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous int64 [T]")
+    return T, (k.stride(0) if T else 0), (v.stride(0) if T else 0)
+
+
+def paged_kv_write_attention_forward(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                                     q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                     block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                     query_start_loc: torch.Tensor, scale: float, causal: bool = True, *,
+                                     out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                                     max_query_len: int = 0, shared_prefix: bool = False) -> torch.Tensor:
+    """``paged_kv_write(k, v, slot_mapping, k_cache, v_cache)`` then
+    ``paged_attention_forward(q, k_cache, v_cache, ...)`` in one call: the
+    new rows are written by extra CTAs of the planner's launch (one launch
+    fewer per step).  Same arguments and result as the two calls."""
+    dev = _need_cuda(k, v, slot_mapping, q, k_cache, v_cache, block_tables, context_lens, query_start_loc)
+    Tn, ks, vs = _new_rows(k, v, slot_mapping, k_cache.shape[2], k_cache.shape[3], {k_cache.dtype})
+    args, out = _forward_args(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale, causal, out,
+                              workspace, max_query_len, shared_prefix, dev)
+    with torch.cuda.device(dev):
+        _check(lib().paged_kv_write_attention_forward(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), Tn, ks, vs,
+                                                      *args))
     return out
 
 
@@ -489,6 +541,37 @@ def paged_attention_forward_fp8kv(q: torch.Tensor, k_cache: torch.Tensor, v_cach
     """``paged_attention_forward`` over FP8 pools read as code * k_scale and
     code * v_scale; q and the result are bf16, head_dim 128."""
     dev = _need_cuda(q, k_cache, v_cache, block_tables, context_lens, query_start_loc)
+    args, out = _fp8_forward_args(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale, k_scale,
+                                  v_scale, causal, out, workspace, max_query_len, dev)
+    with torch.cuda.device(dev):
+        _check(lib().paged_attention_forward_fp8kv(*args))
+    return out
+
+
+def paged_kv_write_attention_forward_fp8kv(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                                           q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                           block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                           query_start_loc: torch.Tensor, scale: float, k_scale: float,
+                                           v_scale: float, causal: bool = True, *, out: torch.Tensor | None = None,
+                                           workspace: torch.Tensor | None = None,
+                                           max_query_len: int = 0) -> torch.Tensor:
+    """``paged_kv_write_fp8`` of a step's new rows (bf16 or f32) then
+    ``paged_attention_forward_fp8kv``, in one call (the rows are encoded by
+    extra CTAs of the planner's launch)."""
+    dev = _need_cuda(k, v, slot_mapping, q, k_cache, v_cache, block_tables, context_lens, query_start_loc)
+    _check_fp8_pools(k_cache, v_cache)
+    Tn, ks, vs = _new_rows(k, v, slot_mapping, k_cache.shape[2], k_cache.shape[3], set(DTYPE))
+    args, out = _fp8_forward_args(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale, k_scale,
+                                  v_scale, causal, out, workspace, max_query_len, dev)
+    with torch.cuda.device(dev):
+        _check(lib().paged_kv_write_attention_forward_fp8kv(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), Tn,
+                                                            ks, vs, DTYPE[k.dtype], *args))
+    return out
+
+
+def _fp8_forward_args(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale, k_scale, v_scale,
+                      causal, out, workspace, max_query_len, dev) -> tuple:
+    """Checks paged_attention_forward_fp8kv's tensors; returns (its C arguments, out)."""
     _check_fp8_pools(k_cache, v_cache)
     if q.dtype != torch.bfloat16 or q.dim() != 3 or not q.is_contiguous():
         raise ValueError("q must be contiguous bfloat16 [T, Hq, D]")
@@ -515,9 +598,8 @@ def paged_attention_forward_fp8kv(q: torch.Tensor, k_cache: torch.Tensor, v_cach
             workspace = _workspace(dev, workspace_size(B, T, Hq, Hkv, D))
         if workspace.dtype != torch.uint8 or workspace.device != dev or workspace.numel() < need:
             raise ValueError(f"workspace must be a uint8 CUDA tensor of at least {need} bytes")
-        _check(lib().paged_attention_forward_fp8kv(
-            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
+    args = (q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
             query_start_loc.data_ptr(), out.data_ptr(), B, T, Hq, Hkv, D, NB, bs, max(1, block_tables.shape[1]),
             int(max_query_len), float(scale), 1 if causal else 0, float(k_scale), float(v_scale), 0,
-            workspace.data_ptr(), workspace.numel(), _stream(dev)))
-    return out
+            workspace.data_ptr(), workspace.numel(), _stream(dev))
+    return args, out

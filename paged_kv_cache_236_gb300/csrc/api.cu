@@ -303,15 +303,47 @@ size_t paged_attention_workspace_min(int32_t num_seqs, int64_t num_tokens, int32
   return workspace_layout(num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, 0, 0, false).total;
 }
 
+// The step's new K/V rows for a fused write (paged_kv_write_attention_forward):
+// rows of row_dtype with token strides in elements (0: dense), copied (bf16 /
+// f32 pools) or encoded as E4M3 codes (FP8 pools).
+struct FusedWrite {
+  const void* k;
+  const void* v;
+  const int64_t* slots;
+  int64_t n, k_stride, v_stride;
+  pkv_dtype row_dtype;
+};
+
+// Checks the fused write's arguments (as paged_kv_write / _fp8 do) and fills
+// its stride defaults.
+static pkv_status check_fused_write(FusedWrite* fw, int Hkv, int D, bool kv_fp8, pkv_dtype pool_dtype) {
+  if (fw->n < 0) return fail(PKV_ERR_INVALID_ARG, "num_new_tokens must be >= 0");
+  if (kv_fp8 ? (fw->row_dtype != PKV_DTYPE_BF16 && fw->row_dtype != PKV_DTYPE_F32) : fw->row_dtype != pool_dtype)
+    return fail(PKV_ERR_UNSUPPORTED, "new rows of dtype %d for these pools", (int)fw->row_dtype);
+  const int64_t row = (int64_t)Hkv * D;
+  if (fw->k_stride == 0) fw->k_stride = row;
+  if (fw->v_stride == 0) fw->v_stride = row;
+  if (fw->k_stride < row || fw->v_stride < row)
+    return fail(PKV_ERR_INVALID_ARG, "token stride smaller than num_kv_heads * head_dim");
+  if (fw->n > 0 && (!fw->k || !fw->v || !fw->slots)) return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (kv_fp8) {
+    const int es = elem_bytes(fw->row_dtype);
+    if ((fw->k_stride * es) % 16 != 0 || (fw->v_stride * es) % 16 != 0 || !aligned16(fw->k) || !aligned16(fw->v))
+      return fail(PKV_ERR_UNSUPPORTED, "new rows must be 16-byte aligned with strides of multiples of 16 bytes");
+  }
+  return PKV_OK;
+}
+
 // The forward call; kv_fp8: the pools hold E4M3 codes (q and out bf16), read
-// as code * k_scale and code * v_scale.
+// as code * k_scale and code * v_scale.  fw: the step's new K/V rows, written
+// first (by extra CTAs of the planner's launch where the rows allow it).
 static pkv_status forward_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                                const int32_t* context_lens, const int32_t* query_start_loc, void* out,
                                int32_t num_seqs, int64_t num_tokens, int32_t num_q_heads, int32_t num_kv_heads,
                                int32_t head_dim, int64_t num_blocks, int32_t block_size, int32_t max_blocks_per_seq,
                                int32_t max_query_len, float scale, int32_t causal, int32_t hints, void* workspace,
                                size_t workspace_bytes, pkv_dtype dtype, bool kv_fp8, float k_scale, float v_scale,
-                               void* stream) {
+                               void* stream, const FusedWrite* fw = nullptr) {
   g_msg[0] = 0;
   const int B = num_seqs, Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim, bs = block_size;
   const int64_t T = num_tokens;
@@ -327,7 +359,15 @@ static pkv_status forward_impl(const void* q, const void* k_cache, const void* v
   if (!(scale > 0.f) || !isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale must be positive and finite");
   if ((int64_t)max_blocks_per_seq * bs > (int64_t)1 << 30) return fail(PKV_ERR_UNSUPPORTED, "context too long");
   if (T > ((int64_t)1 << 31) / ((int64_t)Hq * D)) return fail(PKV_ERR_UNSUPPORTED, "num_tokens too large");
-  if (B == 0 || T == 0) return PKV_OK;
+  if (B == 0 || T == 0) {
+    if (!fw || fw->n == 0) return PKV_OK;
+    // nothing to attend: the write alone
+    return kv_fp8 ? paged_kv_write_fp8(fw->k, fw->v, fw->slots, const_cast<void*>(k_cache),
+                                       const_cast<void*>(v_cache), fw->n, num_blocks, bs, Hkv, D, fw->k_stride,
+                                       fw->v_stride, fw->row_dtype, k_scale, v_scale, stream)
+                  : paged_kv_write(fw->k, fw->v, fw->slots, const_cast<void*>(k_cache), const_cast<void*>(v_cache),
+                                   fw->n, num_blocks, bs, Hkv, D, fw->k_stride, fw->v_stride, dtype, stream);
+  }
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start_loc || !out)
     return fail(PKV_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
@@ -436,6 +476,35 @@ static pkv_status forward_impl(const void* q, const void* k_cache, const void* v
   pp.out = out;
   pp.out_row_bytes = Hq * D * elem_bytes(dtype);
   pp.err = dev->err;
+  if (fw && fw->n > 0) {
+    // The new rows go in with the planner's launch when every row start is
+    // 16-byte aligned (the vector copy, or the FP8 encoder); otherwise the
+    // write kernel runs first, as paged_kv_write would.
+    const int es = elem_bytes(fw->row_dtype);
+    const int64_t row_bytes = (int64_t)Hkv * D * es;
+    const bool vec = row_bytes % 16 == 0 && (fw->k_stride * es) % 16 == 0 && (fw->v_stride * es) % 16 == 0 &&
+                     aligned16(fw->k) && aligned16(fw->v);
+    if (vec) {
+      pp.write_ctas = (int)std::min<int64_t>((fw->n + 15) / 16, 4 * (int64_t)dev->sms);
+      pp.write_mode = kv_fp8 ? (fw->row_dtype == PKV_DTYPE_BF16 ? 2 : 3) : 1;
+      pp.w_row = kv_fp8 ? Hkv * D : (int)(row_bytes / 16);
+      pp.wk = fw->k;
+      pp.wv = fw->v;
+      pp.wslots = fw->slots;
+      pp.wkc = const_cast<void*>(k_cache);
+      pp.wvc = const_cast<void*>(v_cache);
+      pp.wT = fw->n;
+      pp.w_num_slots = num_blocks * bs;
+      pp.wk_stride = kv_fp8 ? fw->k_stride : fw->k_stride * es;
+      pp.wv_stride = kv_fp8 ? fw->v_stride : fw->v_stride * es;
+      pp.wk_scale = k_scale;
+      pp.wv_scale = v_scale;
+    } else {
+      e = launch_kv_write(fw->k, fw->v, fw->slots, const_cast<void*>(k_cache), const_cast<void*>(v_cache), fw->n,
+                          num_blocks * bs, Hkv * D, es, fw->k_stride, fw->v_stride, dev->err, s);
+      if (e != cudaSuccess) return cuda_fail(e, "paged_kv_write launch");
+    }
+  }
   if (cascade && (e = launch_prefix_search(pp, s)) != cudaSuccess) return cuda_fail(e, "prefix search launch");
   if ((e = launch_planner(pp, s)) != cudaSuccess) return cuda_fail(e, "planner launch");
 
@@ -533,6 +602,48 @@ pkv_status paged_attention_forward(const void* q, const void* k_cache, const voi
   return forward_impl(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, out, num_seqs, num_tokens,
                       num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq, max_query_len,
                       scale, causal, hints, workspace, workspace_bytes, dtype, false, 1.f, 1.f, stream);
+}
+
+pkv_status paged_kv_write_attention_forward(const void* k, const void* v, const int64_t* slot_mapping,
+                                            int64_t num_new_tokens, int64_t k_token_stride, int64_t v_token_stride,
+                                            const void* q, const void* k_cache, const void* v_cache,
+                                            const int32_t* block_tables, const int32_t* context_lens,
+                                            const int32_t* query_start_loc, void* out, int32_t num_seqs,
+                                            int64_t num_tokens, int32_t num_q_heads, int32_t num_kv_heads,
+                                            int32_t head_dim, int64_t num_blocks, int32_t block_size,
+                                            int32_t max_blocks_per_seq, int32_t max_query_len, float scale,
+                                            int32_t causal, int32_t hints, void* workspace, size_t workspace_bytes,
+                                            pkv_dtype dtype, void* stream) {
+  g_msg[0] = 0;
+  FusedWrite fw{k, v, slot_mapping, num_new_tokens, k_token_stride, v_token_stride, dtype};
+  if (num_kv_heads <= 0 || head_dim <= 0) return fail(PKV_ERR_INVALID_ARG, "sizes must be positive");
+  pkv_status st = check_fused_write(&fw, num_kv_heads, head_dim, false, dtype);
+  if (st != PKV_OK) return st;
+  return forward_impl(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, out, num_seqs, num_tokens,
+                      num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq, max_query_len,
+                      scale, causal, hints, workspace, workspace_bytes, dtype, false, 1.f, 1.f, stream, &fw);
+}
+
+pkv_status paged_kv_write_attention_forward_fp8kv(
+    const void* k, const void* v, const int64_t* slot_mapping, int64_t num_new_tokens, int64_t k_token_stride,
+    int64_t v_token_stride, pkv_dtype row_dtype, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, const int32_t* query_start_loc, void* out,
+    int32_t num_seqs, int64_t num_tokens, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int64_t num_blocks, int32_t block_size, int32_t max_blocks_per_seq, int32_t max_query_len, float scale,
+    int32_t causal, float k_scale, float v_scale, int32_t hints, void* workspace, size_t workspace_bytes,
+    void* stream) {
+  g_msg[0] = 0;
+  if (!(k_scale > 0.f) || !isfinite(k_scale) || !(v_scale > 0.f) || !isfinite(v_scale))
+    return fail(PKV_ERR_INVALID_ARG, "k_scale and v_scale must be positive and finite");
+  if (head_dim != 128) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d with an FP8 cache (supported: 128)", head_dim);
+  if (num_kv_heads <= 0) return fail(PKV_ERR_INVALID_ARG, "sizes must be positive");
+  FusedWrite fw{k, v, slot_mapping, num_new_tokens, k_token_stride, v_token_stride, row_dtype};
+  pkv_status st = check_fused_write(&fw, num_kv_heads, head_dim, true, PKV_DTYPE_FP8_E4M3);
+  if (st != PKV_OK) return st;
+  return forward_impl(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, out, num_seqs, num_tokens,
+                      num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq, max_query_len,
+                      scale, causal, hints, workspace, workspace_bytes, PKV_DTYPE_BF16, true, k_scale, v_scale,
+                      stream, &fw);
 }
 
 pkv_status paged_attention_forward_fp8kv(const void* q, const void* k_cache, const void* v_cache,

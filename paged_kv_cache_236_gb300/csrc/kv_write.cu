@@ -11,21 +11,12 @@
 // HBM-bound: one warp per token, 16-byte vector loads (read-only, no L1
 // allocation) and stores, all of a token's K and V chunks in flight before
 // the first store.
-#include <cuda_fp8.h>
-
+#include "kv_rows.cuh"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 namespace {
-
-__device__ __forceinline__ int4 ld_stream(const int4* p) {
-  int4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
 
 // Vector path: every row start is 16-byte aligned and a row is a multiple of
 // 16 bytes.  kChunks = chunks per lane held in registers per pass.
@@ -37,37 +28,8 @@ __global__ void __launch_bounds__(256) kv_write_vec(const uint8_t* __restrict__ 
   pdl_launch_dependents();  // a following planner reads nothing this kernel writes
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
-    const int64_t s = slots[t];
-    if (s < 0) continue;
-    if (s >= num_slots) {
-      if (lane == 0) raise_error(err, PKV_DEVERR_SLOT_OUT_OF_RANGE);
-      continue;
-    }
-    const int4* ks = reinterpret_cast<const int4*>(k + t * k_stride_b);
-    const int4* vs = reinterpret_cast<const int4*>(v + t * v_stride_b);
-    int4* kd = reinterpret_cast<int4*>(kc + s * (int64_t)row_chunks * 16);
-    int4* vd = reinterpret_cast<int4*>(vc + s * (int64_t)row_chunks * 16);
-    for (int base = 0; base < row_chunks; base += 32 * kChunks) {
-      int4 kr[kChunks], vr[kChunks];
-#pragma unroll
-      for (int i = 0; i < kChunks; ++i) {
-        const int c = base + i * 32 + lane;
-        if (c < row_chunks) {
-          kr[i] = ld_stream(ks + c);
-          vr[i] = ld_stream(vs + c);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kChunks; ++i) {
-        const int c = base + i * 32 + lane;
-        if (c < row_chunks) {
-          kd[c] = kr[i];
-          vd[c] = vr[i];
-        }
-      }
-    }
-  }
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps)
+    copy_token_rows<kChunks>(k, v, slots, kc, vc, t, num_slots, row_chunks, k_stride_b, v_stride_b, err, lane);
 }
 
 // Element path for rows that are not 16-byte aligned (odd strides): one warp
@@ -93,9 +55,7 @@ __global__ void __launch_bounds__(256) kv_write_elem(const U* __restrict__ k, co
   }
 }
 
-// FP8 (E4M3) cache write: code = e4m3(RNE(x / scale)), saturating at +-448
-// (the division is IEEE fp32).  One warp per token, 16 elements a lane per
-// pass: one 16-byte store of codes from 32 (bf16) or 64 (fp32) bytes of row.
+// FP8 (E4M3) cache write: one warp per token (quantize_token_rows).
 template <typename U>
 __global__ void __launch_bounds__(256) kv_write_fp8_kernel(const U* __restrict__ k, const U* __restrict__ v,
                                                            const int64_t* __restrict__ slots, uint8_t* kc,
@@ -105,49 +65,9 @@ __global__ void __launch_bounds__(256) kv_write_fp8_kernel(const U* __restrict__
   pdl_launch_dependents();  // a following planner reads nothing this kernel writes
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  constexpr int kVec = 16 / sizeof(U);  // elements per 16-byte load
-  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
-    const int64_t s = slots[t];
-    if (s < 0) continue;
-    if (s >= num_slots) {
-      if (lane == 0) raise_error(err, PKV_DEVERR_SLOT_OUT_OF_RANGE);
-      continue;
-    }
-    for (int e0 = lane * 16; e0 < row_elems; e0 += 32 * 16) {
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const U* src = (which ? v + t * v_stride : k + t * k_stride) + e0;
-        const float sc = which ? v_scale : k_scale;
-        float x[16];
-#pragma unroll
-        for (int c = 0; c < 16 / kVec; ++c) {
-          const int4 r = ld_stream(reinterpret_cast<const int4*>(src) + c);
-          const uint32_t w[4] = {(uint32_t)r.x, (uint32_t)r.y, (uint32_t)r.z, (uint32_t)r.w};
-          if constexpr (sizeof(U) == 2) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              x[c * 8 + 2 * i] = __uint_as_float(w[i] << 16);
-              x[c * 8 + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) x[c * 4 + i] = __uint_as_float(w[i]);
-          }
-        }
-        uint32_t out[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t lo = __nv_cvt_float2_to_fp8x2(
-              make_float2(__fdiv_rn(x[4 * i], sc), __fdiv_rn(x[4 * i + 1], sc)), __NV_SATFINITE, __NV_E4M3);
-          const uint32_t hi = __nv_cvt_float2_to_fp8x2(
-              make_float2(__fdiv_rn(x[4 * i + 2], sc), __fdiv_rn(x[4 * i + 3], sc)), __NV_SATFINITE, __NV_E4M3);
-          out[i] = (lo & 0xFFFFu) | (hi << 16);
-        }
-        uint8_t* dst = (which ? vc : kc) + s * row_elems + e0;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
-      }
-    }
-  }
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps)
+    quantize_token_rows<U>(k, v, slots, kc, vc, t, num_slots, row_elems, k_stride, v_stride, k_scale, v_scale, err,
+                           lane);
 }
 
 }  // namespace

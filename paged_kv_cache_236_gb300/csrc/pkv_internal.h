@@ -118,6 +118,18 @@ struct PlanParams {
   void* out;        // rows of invalid sequences are zeroed
   int out_row_bytes;  // bytes of one token's output row (Hq * D * elem)
   int* err;
+  // The step's new K/V rows, written by CTAs 1 .. write_ctas of the
+  // planner's grid (write_ctas 0: none).  write_mode 1: row copy of w_row
+  // 16-byte chunks, strides in bytes; 2 / 3: FP8 quantizing write of bf16 /
+  // fp32 rows of w_row elements, strides in elements.
+  int write_ctas, write_mode, w_row;
+  const void* wk;
+  const void* wv;
+  const int64_t* wslots;
+  void* wkc;
+  void* wvc;
+  int64_t wT, w_num_slots, wk_stride, wv_stride;
+  float wk_scale, wv_scale;
 };
 
 struct AttnParams {

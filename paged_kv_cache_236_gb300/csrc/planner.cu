@@ -17,14 +17,13 @@
 // chunk), so that the attention kernels, which take items in list order,
 // end with small ones and finish together.
 //
-// One CTA.  The unit instances (sequence, row unit), each standing for all
-// kv heads, are numbered with each sequence's units contiguous (per-sequence
-// unit offsets in shared memory); each thread walks a contiguous range of
-// that numbering, so that a long prefill sequence's many units spread over
-// many threads.  Block-wide exclusive scans give every item a fixed slot
-// (items ordered by size class, then unit instance, then split, then kv
-// head: the kv heads of one key range are adjacent in the queue, so the CTAs
-// that take them read the same pool rows at about the same time).
+// One CTA.  The unit instances (sequence, row unit, kv head) are numbered
+// sequence major, each sequence's units contiguous (per-sequence unit offsets
+// in shared memory); each thread walks a contiguous range of that numbering,
+// so that a long prefill sequence's many units spread over many threads.
+// Per-class totals are summed with shared-memory atomics, and each item takes
+// its slot in its class's range from a cursor (items ordered by size class;
+// within a class in no particular order, which changes no result).
 //
 // Shared prefixes (when the call asks for them): consecutive decode-shaped
 // sequences whose block tables start with the same physical blocks read
@@ -36,6 +35,7 @@
 // prefix, always as merge groups, whose merge folds in the prefix partials.
 // Those are complete before the decode kernel runs (the tensor-core kernel
 // precedes it in the stream).
+#include "kv_rows.cuh"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -144,16 +144,18 @@ __device__ void block_scan(int (&v)[K], int (&totals)[K]) {
   __syncthreads();
 }
 
-// Walks a contiguous range of unit instances i = seq_off[s] + u (a unit of
-// rows of one sequence; each stands for its Hkv kv heads).
+// Walks a contiguous range of unit instances i = (seq_off[s] + u) * Hkv +
+// kvh: a unit of rows of one sequence and one kv head, numbered sequence
+// major, so that the kv heads of one unit are adjacent.
 struct UnitIter {
-  int i, end, B, s, u;
+  int i, end, B, Hkv, s, u, kvh;
   SeqDesc d;
 };
 
 __device__ __forceinline__ void iter_seek(UnitIter& t, const PlanParams& p, const int* seq_off) {
   if (t.i >= t.end) return;
-  const int j = t.i;
+  const int j = t.i / t.Hkv;
+  t.kvh = t.i - j * t.Hkv;
   int lo = 0, hi = t.B - 1;  // the last sequence whose first unit is <= j
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -167,6 +169,8 @@ __device__ __forceinline__ void iter_seek(UnitIter& t, const PlanParams& p, cons
 __device__ __forceinline__ void iter_next(UnitIter& t, const PlanParams& p, const int* seq_off) {
   ++t.i;
   if (t.i >= t.end) return;
+  if (++t.kvh < t.Hkv) return;
+  t.kvh = 0;
   if (++t.u < t.d.units) return;
   int s = t.s + 1;  // the next sequence with units
   while (s < t.B && seq_off[s + 1] == seq_off[s]) ++s;
@@ -344,15 +348,51 @@ __device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre)
   __syncthreads();
 }
 
+// CTAs 1 .. write_ctas of the planner's grid: the step's new K/V rows, one
+// warp per token, after the predecessor grid has completed (stream order:
+// the previous call's kernels may still read the pool).  The attention
+// kernels wait for this whole grid, so they see these rows and the plan.
+__device__ __noinline__ void write_new_rows(const PlanParams& p) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)(gridDim.x - 1) * (kThreads / 32);
+  for (int64_t t = (int64_t)(blockIdx.x - 1) * (kThreads / 32) + (threadIdx.x >> 5); t < p.wT; t += warps) {
+    if (p.write_mode == 1) {
+      if (p.w_row <= 64)
+        copy_token_rows<2>(static_cast<const uint8_t*>(p.wk), static_cast<const uint8_t*>(p.wv), p.wslots,
+                           static_cast<uint8_t*>(p.wkc), static_cast<uint8_t*>(p.wvc), t, p.w_num_slots, p.w_row,
+                           p.wk_stride, p.wv_stride, p.err, lane);
+      else
+        copy_token_rows<4>(static_cast<const uint8_t*>(p.wk), static_cast<const uint8_t*>(p.wv), p.wslots,
+                           static_cast<uint8_t*>(p.wkc), static_cast<uint8_t*>(p.wvc), t, p.w_num_slots, p.w_row,
+                           p.wk_stride, p.wv_stride, p.err, lane);
+    } else if (p.write_mode == 2) {
+      quantize_token_rows<uint16_t>(static_cast<const uint16_t*>(p.wk), static_cast<const uint16_t*>(p.wv), p.wslots,
+                                    static_cast<uint8_t*>(p.wkc), static_cast<uint8_t*>(p.wvc), t, p.w_num_slots,
+                                    p.w_row, p.wk_stride, p.wv_stride, p.wk_scale, p.wv_scale, p.err, lane);
+    } else {
+      quantize_token_rows<float>(static_cast<const float*>(p.wk), static_cast<const float*>(p.wv), p.wslots,
+                                 static_cast<uint8_t*>(p.wkc), static_cast<uint8_t*>(p.wvc), t, p.w_num_slots,
+                                 p.w_row, p.wk_stride, p.wv_stride, p.wk_scale, p.wv_scale, p.err, lane);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   // The attention kernel may start its prologue while this plans (it waits
   // for this grid).  This grid may start while its predecessor runs: the
-  // only predecessor that lets it (paged_kv_write) writes neither the
-  // metadata read here nor anything written here, so the plan is computed
-  // at once and the wait for the predecessor comes before the first write
-  // that later kernels read (which also makes this grid's completion imply
-  // the predecessor's, as the attention kernels need).
+  // predecessors that let it (paged_kv_write, the shared-prefix search)
+  // write neither the metadata read here nor anything written here, so the
+  // plan is computed at once and the wait for the predecessor comes before
+  // the first write that later kernels read (which also makes this grid's
+  // completion imply the predecessor's, as the attention kernels need).
+  // With a fused write, CTAs 1 .. write_ctas write the step's new K/V rows
+  // (after the same wait) while CTA 0 plans.
   pdl_launch_dependents();
+  if (blockIdx.x > 0) {  // the step's new K/V rows (a fused write)
+    write_new_rows(p);
+    return;
+  }
   extern __shared__ int seq_off[];  // [B + 1]: first unit of each sequence (per kv head)
   const int tid = threadIdx.x;
   const int B = p.B;
@@ -392,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
     __syncthreads();
   }
   const int U = seq_off[B];
-  const int N = U;  // unit instances, each for all kv heads
+  const int N = U * p.Hkv;  // unit instances
   const int per_thread = (N + kThreads - 1) / kThreads;
   const int i0 = min(N, tid * per_thread), i1 = min(N, i0 + per_thread);
 
@@ -403,9 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   __shared__ int sh_state;
   unsigned long long w_dec = 0, w_mma = 0;
   {
-    UnitIter t{i0, i1, B, 0, 0, {}};
+    UnitIter t{i0, i1, B, p.Hkv, 0, 0, 0, {}};
     for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off))
-      (t.d.mma ? w_mma : w_dec) += (unsigned long long)(unit_keys(t.d, t.u, p.G, p.causal) - t.d.pre) * p.Hkv;
+      (t.d.mma ? w_mma : w_dec) += (unsigned long long)(unit_keys(t.d, t.u, p.G, p.causal) - t.d.pre);
   }
   // warp sums, then one thread adds the warps' (no contended 64-bit atomics)
 #pragma unroll
@@ -467,42 +507,45 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   __syncthreads();
 
   // ---- count items per size class, merge groups and partial rows; grow the
-  // chunks until the plan fits the workspace
-  __shared__ int s_cnt[kNumCounts][kThreads];  // per-thread counters, then running offsets
-  int cnt[kNumCounts], tot[kNumCounts];
+  // chunks until the plan fits the workspace.  Totals go through shared
+  // atomics; an item's slot is taken from its class's cursor when it is
+  // written (the order within a class does not change any result: every
+  // item computes the same rows whichever CTA takes it, and split merges
+  // follow split order).
+  __shared__ int s_tot[kNumCounts];
+  __shared__ int s_cur[kNumCounts];  // emit cursors: class offsets, then the merge / partial-row cursors
   for (int iter = 0;; ++iter) {
     const int cd = sh_chunk[0], cm = sh_chunk[1];
-#pragma unroll
-    for (int k = 0; k < kNumCounts; ++k) s_cnt[k][tid] = 0;
-    UnitIter t{i0, i1, B, 0, 0, {}};
-    for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off)) {
-      const SeqDesc& d = t.d;
-      const int chunk = d.mma ? cm : cd;
-      const int cb = d.mma ? kClasses : 0;
-      const int keys = unit_keys(d, t.u, p.G, p.causal) - d.pre;
-      int ns, per;
-      split_of(keys, chunk, d.mma ? kMmaTileKeys : p.dec_tile_keys, ns, per);
-      s_cnt[cb + size_class(per, chunk)][tid] += (ns - 1) * p.Hkv;  // all splits but the last are full
-      s_cnt[cb + size_class(keys - (ns - 1) * per, chunk)][tid] += p.Hkv;
-      if (ns > 1 || d.pre > 0) {
-        s_cnt[kCntMerge][tid] += p.Hkv;
-        if (ns > 1)
-          s_cnt[d.mma ? kCntPartMma : kCntPartDec][tid] +=
-              p.Hkv * ns * min(d.rows - t.u * d.unit_rows, d.unit_rows);
+    if (tid < kNumCounts) s_tot[tid] = 0;
+    __syncthreads();
+    {
+      UnitIter t{i0, i1, B, p.Hkv, 0, 0, 0, {}};
+      for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off)) {
+        const SeqDesc& d = t.d;
+        const int chunk = d.mma ? cm : cd;
+        const int cb = d.mma ? kClasses : 0;
+        const int keys = unit_keys(d, t.u, p.G, p.causal) - d.pre;
+        int ns, per;
+        split_of(keys, chunk, d.mma ? kMmaTileKeys : p.dec_tile_keys, ns, per);
+        if (ns > 1) atomicAdd(&s_tot[cb + size_class(per, chunk)], ns - 1);  // all splits but the last are full
+        atomicAdd(&s_tot[cb + size_class(keys - (ns - 1) * per, chunk)], 1);
+        if (ns > 1 || d.pre > 0) {
+          atomicAdd(&s_tot[kCntMerge], 1);
+          if (ns > 1)
+            atomicAdd(&s_tot[d.mma ? kCntPartMma : kCntPartDec], ns * min(d.rows - t.u * d.unit_rows, d.unit_rows));
+        }
       }
     }
-#pragma unroll
-    for (int k = 0; k < kNumCounts; ++k) cnt[k] = s_cnt[k][tid];
-    block_scan<kNumCounts>(cnt, tot);
+    __syncthreads();
     if (tid == 0) {
       int nd = 0, nm = 0;
 #pragma unroll
       for (int k = 0; k < kClasses; ++k) {
-        nd += tot[k];
-        nm += tot[kClasses + k];
+        nd += s_tot[k];
+        nm += s_tot[kClasses + k];
       }
-      const int pd = tot[kCntPartDec], pm = tot[kCntPartMma];
-      const bool fits = nd <= p.dec_cap && nm + sh_pre[0] <= p.mma_cap && tot[kCntMerge] <= p.merge_cap &&
+      const int pd = s_tot[kCntPartDec], pm = s_tot[kCntPartMma];
+      const bool fits = nd <= p.dec_cap && nm + sh_pre[0] <= p.mma_cap && s_tot[kCntMerge] <= p.merge_cap &&
                         (int64_t)pd + pm + sh_pre[1] <= p.part_cap;
       sh_state = fits ? 1 : 0;
       // Once: if the decode items are mostly full chunks (long sequences
@@ -511,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       // to the largest-first order.
       const int P = max(1, sh_mma_ctas < p.sms ? p.dec_ctas * (p.sms - sh_mma_ctas) / p.sms : p.dec_ctas);
       const int extra = nd % P;
-      if (fits && iter == 0 && nd > P && extra > 0 && 2 * extra <= P && 4 * tot[0] >= 3 * nd) {
+      if (fits && iter == 0 && nd > P && extra > 0 && 2 * extra <= P && 4 * s_tot[0] >= 3 * nd) {
         const long long grown = ((long long)cd * nd + (nd - extra) - 1) / (nd - extra);
         sh_chunk[0] = (int)min((grown + p.dec_tile_keys - 1) / p.dec_tile_keys * p.dec_tile_keys, (long long)(1 << 30));
         sh_state = 0;
@@ -525,6 +568,19 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
         const bool mma_over = nm > p.mma_cap || pm > pd;
         if (dec_over) sh_chunk[0] = (int)min(2LL * cd, (long long)(1 << 30));
         if (mma_over) sh_chunk[1] = (int)min(2LL * cm, (long long)(1 << 30));
+      }
+      if (sh_state == 1) {
+        // cursors: class k's items start after all larger classes' (largest first)
+        int od = 0, om = 0;
+#pragma unroll
+        for (int k = 0; k < kClasses; ++k) {
+          s_cur[k] = od;
+          od += s_tot[k];
+          s_cur[kClasses + k] = om;
+          om += s_tot[kClasses + k];
+        }
+        s_cur[kCntMerge] = 0;
+        s_cur[kCntPartDec] = 0;  // partial rows of both kinds from one cursor
       }
     }
     __syncthreads();
@@ -555,26 +611,14 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
     }
   }
 
-  // ---- emit: class k's items start after all larger classes' (largest first)
+  // ---- emit
   const int cd = sh_chunk[0], cm = sh_chunk[1];
+  const int pre_part_base = s_tot[kCntPartDec] + s_tot[kCntPartMma];  // prefix partial rows follow the units'
   {
-    int base_dec = 0, base_mma = 0;
-#pragma unroll
-    for (int k = 0; k < kClasses; ++k) {
-      s_cnt[k][tid] = base_dec + cnt[k];
-      base_dec += tot[k];
-      s_cnt[kClasses + k][tid] = base_mma + cnt[kClasses + k];
-      base_mma += tot[kClasses + k];
-    }
-  }
-  const int pre_part_base = tot[kCntPartDec] + tot[kCntPartMma];  // prefix partial rows follow the units'
-  int off_grp = cnt[kCntMerge];
-  int off_part = cnt[kCntPartDec] + cnt[kCntPartMma];
-  {
-    UnitIter t{i0, i1, B, 0, 0, {}};
+    UnitIter t{i0, i1, B, p.Hkv, 0, 0, 0, {}};
     for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off)) {
       const SeqDesc& d = t.d;
-      const int s = t.s, u = t.u;
+      const int s = t.s, u = t.u, kvh = t.kvh;
       WorkItem* items = d.mma ? p.mma_items : p.dec_items;
       const int chunk = d.mma ? cm : cd;
       const int cbase = d.mma ? kClasses : 0;
@@ -584,57 +628,48 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       const int nr = min(d.rows - r0, d.unit_rows);
       int ns, per;
       split_of(keys, chunk, d.mma ? kMmaTileKeys : p.dec_tile_keys, ns, per);
-      // one merge group per kv head when split (or after a shared prefix)
-      const bool grouped = ns > 1 || d.pre > 0;
-      const int grp0 = grouped ? off_grp : -1;
-      const int part0 = off_part;
-      if (grouped) {
-        off_grp += p.Hkv;
-        if (ns > 1) off_part += p.Hkv * ns * nr;
-        for (int kvh = 0; kvh < p.Hkv; ++kvh) {
-          // A unit after a shared prefix always names a merge group (where its
-          // prefix partials are); unsplit, its one item folds them in itself.
-          MergeGroup g;
-          g.seq = s;
-          g.kvh = kvh;
-          g.row0 = r0;
-          g.nrows = nr;
-          g.nsplit = ns;
-          g.part_base = ns > 1 ? part0 + kvh * ns * nr : 0;
-          g.pre_base = 0;
-          g.pre_n = 0;
-          g.pre_stride = 0;
-          g.pad0 = g.pad1 = g.pad2 = 0;
-          if (d.pre > 0) {
-            // this unit's rows in its group's prefix partials ([kvh][chunk][row])
-            const int npre = d.pre_shape >> 24, grows = d.pre_shape & 0xffffff;
-            g.pre_base = pre_part_base + d.pre_rel + kvh * npre * grows + r0;
-            g.pre_n = npre;
-            g.pre_stride = grows;
-          }
-          p.merges[grp0 + kvh] = g;
-          p.tickets[grp0 + kvh] = 0;
+      int grp = -1, part_base = 0;
+      if (ns > 1 || d.pre > 0) {
+        // A unit after a shared prefix always names a merge group (where its
+        // prefix partials are); unsplit, its one item folds them in itself.
+        grp = atomicAdd(&s_cur[kCntMerge], 1);
+        if (ns > 1) part_base = atomicAdd(&s_cur[kCntPartDec], ns * nr);
+        MergeGroup g;
+        g.seq = s;
+        g.kvh = kvh;
+        g.row0 = r0;
+        g.nrows = nr;
+        g.nsplit = ns;
+        g.part_base = part_base;
+        g.pre_base = 0;
+        g.pre_n = 0;
+        g.pre_stride = 0;
+        g.pad0 = g.pad1 = g.pad2 = 0;
+        if (d.pre > 0) {
+          // this unit's rows in its group's prefix partials ([kvh][chunk][row])
+          const int npre = d.pre_shape >> 24, grows = d.pre_shape & 0xffffff;
+          g.pre_base = pre_part_base + d.pre_rel + kvh * npre * grows + r0;
+          g.pre_n = npre;
+          g.pre_stride = grows;
         }
+        p.merges[grp] = g;
+        p.tickets[grp] = 0;
       }
       const int full_cls = cbase + size_class(per, chunk);
       const int last_cls = cbase + size_class(keys - (ns - 1) * per, chunk);
-      // split-major, kv head minor: the kv heads of one key range sit next to
-      // each other in the queue, so the CTAs that take them read the same
-      // pool rows (one token's row holds every kv head) at about the same
-      // time, which keeps the DRAM accesses of a block together
+      const int full0 = ns > 1 ? atomicAdd(&s_cur[full_cls], ns - 1) : 0;
+      const int last0 = atomicAdd(&s_cur[last_cls], 1);
       for (int sp = 0; sp < ns; ++sp) {
-        for (int kvh = 0; kvh < p.Hkv; ++kvh) {
-          WorkItem it;
-          it.seq = s;
-          it.kvh = kvh;
-          it.row0 = r0;
-          it.nrows = nr;
-          it.kb = d.pre + sp * per;
-          it.ke = min(kend, d.pre + (sp + 1) * per);
-          it.part = ns > 1 ? part0 + kvh * ns * nr + sp * nr : -1;
-          it.grp = grouped ? grp0 + kvh : -1;
-          items[s_cnt[sp == ns - 1 ? last_cls : full_cls][tid]++] = it;
-        }
+        WorkItem it;
+        it.seq = s;
+        it.kvh = kvh;
+        it.row0 = r0;
+        it.nrows = nr;
+        it.kb = d.pre + sp * per;
+        it.ke = min(kend, d.pre + (sp + 1) * per);
+        it.part = ns > 1 ? part_base + sp * nr : -1;
+        it.grp = grp;
+        items[sp == ns - 1 ? last0 : full0 + sp] = it;
       }
     }
   }
@@ -642,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   if (sh_pre[0] > 0) {
     int nm = 0;
 #pragma unroll
-    for (int k = 0; k < kClasses; ++k) nm += tot[kClasses + k];
+    for (int k = 0; k < kClasses; ++k) nm += s_tot[kClasses + k];
     const int ng = sh_pre[3];
     // item k of a group: kv head, row tile, key chunk (chunk fastest)
     auto emit = [&](const PreGroup& pg, int k) {
@@ -680,17 +715,17 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
     int nd = 0, nm = 0;
 #pragma unroll
     for (int k = 0; k < kClasses; ++k) {
-      nd += tot[k];
-      nm += tot[kClasses + k];
+      nd += s_tot[k];
+      nm += s_tot[kClasses + k];
     }
     p.header->n_dec = nd;
     p.header->n_mma = nm + sh_pre[0];
     p.header->n_pre = sh_pre[0];
     p.header->n_groups = sh_pre[2];
-    p.header->n_merge = tot[kCntMerge];
+    p.header->n_merge = s_tot[kCntMerge];
     p.header->chunk_dec = cd;
     p.header->chunk_mma = cm;
-    p.header->part_rows = tot[kCntPartDec] + tot[kCntPartMma] + sh_pre[1];
+    p.header->part_rows = s_tot[kCntPartDec] + s_tot[kCntPartMma] + sh_pre[1];
     p.header->dec_counter = 0;
     p.header->mma_counter = 0;
     p.header->merge_counter = 0;
@@ -721,7 +756,7 @@ cudaError_t launch_planner(const PlanParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, 1ull << dev, __ATOMIC_RELEASE);
   }
-  e = launch_pdl(plan_kernel, dim3(1), dim3(kThreads), smem, s, p);
+  e = launch_pdl(plan_kernel, dim3(1 + p.write_ctas), dim3(kThreads), smem, s, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -1,6 +1,6 @@
 """Host-side pieces of bench.py: the algorithmic byte counts (the FP8 pools
 hold one byte per element, so the decode batch's K/V bytes halve), the kernel
-launch count per step, and the block manager's host timing on a small batch."""
+launch count per step (the write inside the planner's launch), and the block manager's host timing on a small batch."""
 import numpy as np
 
 import bench
@@ -18,10 +18,11 @@ def test_fp8_halves_the_cached_bytes():
 
 def test_launches_per_step():
     w = wl.random_small(4, batch=4, max_ctx=200, max_q=1, num_q_heads=8, num_kv_heads=2)
-    assert bench.launches_per_step(w, 1, False, fp8=True) == 3
-    assert bench.launches_per_step(w, 1, False) == 3          # write, planner, tensor-core decode
-    assert bench.launches_per_step(w, 0, False) == 4          # + the multi-token kernel (no hint)
-    assert bench.launches_per_step(w, 1, True) == 5           # + the prefix search and prefix items
+    # the step's write runs in the planner's launch (paged_kv_write_attention_forward)
+    assert bench.launches_per_step(w, 1, False, fp8=True) == 2
+    assert bench.launches_per_step(w, 1, False) == 2          # planner with the write, tensor-core decode
+    assert bench.launches_per_step(w, 0, False) == 3          # + the multi-token kernel (no hint)
+    assert bench.launches_per_step(w, 1, True) == 4           # + the prefix search and prefix items
 
 
 def test_block_manager_timing_runs_on_the_host():
