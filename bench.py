@@ -39,7 +39,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged-attn decode KV GB/s (% HBM peak); mixed-batch query tokens/s"
 BASE_SEED = {"decode": 1002, "mixed": 1003, "prefill": 1003, "specverify": 1004, "prefix": 1005, "prefix-long": 1006,
-             "decode-fp8": 1002}
+             "decode-fp8": 1002, "prefill-g7": 1003, "prefill-d64": 1003}
 # The FP8 (E4M3) cache workload: the decode batch with both pools encoded with
 # one scale each, chosen so that N(0, 1) values span the E4M3 range.
 FP8_SCALE = 4.5 / 448
@@ -50,6 +50,10 @@ WORKLOAD_DESC = {
              "context U[256,8192], 32q/8kv heads, head_dim 128, block_size 16, 80000-block pool, bf16",
     "prefill": "the mixed batch's 8 prefill chunks alone (512 tokens on U[0,2048] cached), 32q/8kv, head_dim 128, "
                "block_size 16, bf16",
+    "prefill-g7": "the prefill chunks (8 x 512 tokens on U[0,2048] cached) with 56q/8kv heads (GQA group 7), "
+                  "head_dim 128, block_size 16, bf16",
+    "prefill-d64": "the prefill chunks (8 x 512 tokens on U[0,2048] cached) with 32q/8kv heads and head_dim 64, "
+                   "block_size 16, bf16",
     "specverify": "speculative verify: 32 seqs x 5 query tokens on 8192-token contexts, 64q/8kv heads, head_dim "
                   "128, block_size 32, 10240-block pool, bf16",
     "prefix": "prefix-shared decode: 256 seqs sharing a 2048-token prefix (128 blocks) + private U[128,1024] "
@@ -127,8 +131,8 @@ def launches_per_step(w, max_q_len: int, shared_prefix: bool, fp8: bool = False)
     if fp8:
         return 2
     g = w.num_q_heads // w.num_kv_heads
-    tc = w.dtype == "bf16" and w.head_dim == 128 and g & (g - 1) == 0
-    dectc = tc and g <= 16
+    tc = w.dtype == "bf16" and g <= 128                      # the multi-token tensor-core kernel
+    dectc = tc and w.head_dim == 128 and g & (g - 1) == 0 and g <= 16
     dec_rows = 16 if dectc else 4
     cascade = shared_prefix and dectc
     mma = tc and (cascade or not (max_q_len > 0 and max_q_len * g <= dec_rows))
@@ -299,7 +303,7 @@ def run_gpu(args, rank, world, local_rank):
     tot_ms = max_over_ranks(sum(step_ms), world, dev)
     value = ab["step"] * args.steps * world / (tot_ms * 1e-3) / 1e9
     kern_avg_ms = sum(kern_ms) / len(kern_ms)
-    if args.workload == "prefill":
+    if args.workload in ("prefill", "prefill-g7", "prefill-d64"):
         fl = mma_flops(w)
         achieved = fl / (kern_avg_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": "mma_attn_kernel (tcgen05, per launch)", "achieved": round(achieved, 1),

@@ -141,7 +141,9 @@ WorkspaceLayout workspace_layout(int B, int64_t T, int Hq, int Hkv, int D, size_
   const int G = Hq / Hkv;
   const int64_t rows = T * (int64_t)G;
   const int64_t dec_units = (int64_t)Hkv * ((rows + kDecRows - 1) / kDecRows + B);
-  const int64_t mma_units = (int64_t)Hkv * ((rows + kMmaRows - 1) / kMmaRows + B);
+  // tensor-core items hold whole tokens: floor(kMmaRows / G) of them
+  const int64_t mma_tok = G <= kMmaRows ? kMmaRows / G : 1;
+  const int64_t mma_units = (int64_t)Hkv * ((T + mma_tok - 1) / mma_tok + B);
   const int64_t dec_cap = kCapTargetDec + dec_units;
   const int64_t mma_cap = kCapTargetMma + mma_units;
   const int64_t merge_cap = dec_cap + mma_cap;
@@ -398,16 +400,16 @@ static pkv_status forward_impl(const void* q, const void* k_cache, const void* v
   float2* part_ml = reinterpret_cast<float2*>(ws + lay.ml_off);
   float* part_acc = reinterpret_cast<float*>(ws + lay.acc_off);
 
-  // tensor-core path: bf16, head_dim 128, G a power of two (a 128-row tile is
-  // 128/G whole tokens)
-  const bool mma_ok = !kv_fp8 && bf16 && D == 128 && (G & (G - 1)) == 0 && G <= 128;
+  // tensor-core path for multi-token rows: bf16, head_dim 64 or 128, any G
+  // up to 128 (an item is the floor(128 / G) whole tokens that fit 128 rows)
+  const bool mma_ok = !kv_fp8 && bf16 && G <= kMmaRows;
   // decode-shaped rows: tensor-core kernel (keys on M, rows on N) for bf16,
   // head_dim 128 and G dividing 16; the CUDA-core kernel otherwise
   // FP8 pools: the same kernel on fp16 MMAs over converted tiles when the
   // host hint bounds every sequence's rows by 8, the CUDA-core kernel otherwise
   const bool f8tc = kv_fp8 && D == 128 && (G & (G - 1)) == 0 && max_query_len > 0 &&
                     (int64_t)max_query_len * G <= 8;
-  const bool dectc = (mma_ok && G <= kTcDecRows) || f8tc;
+  const bool dectc = (mma_ok && D == 128 && (G & (G - 1)) == 0 && G <= kTcDecRows) || f8tc;
   const int dec_rows_max = dectc ? kTcDecRows : kDecRows;
   // rows of softmax per key in that kernel: a power of two >= G (so items hold
   // whole tokens) covering the hinted query length; 16 when there is no hint
@@ -446,6 +448,7 @@ static pkv_status forward_impl(const void* q, const void* k_cache, const void* v
   pp.block_tables = block_tables;
   pp.dec_rows_max = dec_rows_max;
   pp.dec_unit_rows = dectc ? tc_rows : kDecRows;
+  pp.mma_unit_rows = (kMmaRows / G) * G;
   pp.dec_tile_keys = dectc ? kMmaTileKeys : kDecTileKeys;
   // Four items per CTA of the decode kernels: fewer, longer items cost less
   // per item (pipeline restarts, partial writes, merges) than a finer tail
@@ -538,6 +541,7 @@ static pkv_status forward_impl(const void* q, const void* k_cache, const void* v
   ap.v_scale = kv_fp8 ? v_scale : 1.f;
   ap.causal = causal ? 1 : 0;
   ap.out_al32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
+  ap.mma_unit_rows = (kMmaRows / G) * G;
   ap.err = dev->err;
   ap.wait_ns = g_fault_wait_ns;
   ap.fault_tile = g_fault_tile;

@@ -111,7 +111,9 @@ constexpr int kRegsLight = 64, kRegsSoftmax = 184;
 static_assert(2 * 128 * (kRegsLight + kRegsSoftmax) <= kThreads * 128, "register split above 128 per thread");
 
 constexpr uint32_t kIdescS = idesc_bf16(128, kKeys, false, false);
-constexpr uint32_t kIdescO = idesc_bf16(128, 128, false, true);
+// P.V with N = head_dim (64 or 128)
+template <int D>
+constexpr uint32_t kIdescO = idesc_bf16(128, D, false, true);
 
 // V as the B of P.V (MN-major): the two 64-column halves are kHalfKV apart,
 // 8-key groups 1024 bytes apart.
@@ -149,24 +151,32 @@ static_assert(kKOff % 1024 == 0 && kVOff % 1024 == 0 && kTileBytes % 1024 == 0 &
               "swizzled tiles");
 static_assert(kBarOff % 8 == 0 && kSlotOff % alignof(ItemSlot) == 0 && kRedOff % 16 == 0, "alignment");
 
-// 64 bf16 (128 bytes) of an output row: four 32-byte stores when the output
-// is 32-byte aligned, else eight 16-byte ones.
-__device__ __forceinline__ void store_row128(__nv_bfloat16* dst, const uint32_t* w, int al32) {
+// N bf16 (2N bytes) of an output row, packed in pairs in w: 32-byte stores
+// when the output is 32-byte aligned, else 16-byte ones.
+template <int N>
+__device__ __forceinline__ void store_row(__nv_bfloat16* dst, const uint32_t* w, int al32) {
   if (al32) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) st_global_v8(dst + 16 * u, w + 8 * u);
+    for (int u = 0; u < N / 16; ++u) st_global_v8(dst + 16 * u, w + 8 * u);
   } else {
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
+    for (int u = 0; u < N / 8; ++u)
       *reinterpret_cast<uint4*>(dst + 8 * u) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
   }
 }
 
+// D: head_dim, 64 or 128 (one or two 64-column halves of Q, K, V and the
+// output; the shared-memory and TMEM layouts are those of 128, with the
+// second halves unused at 64).  Each softmax thread owns D / 2 output
+// columns of its row.
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams p,
                                                                const __grid_constant__ CUtensorMap qmap,
                                                                const __grid_constant__ CUtensorMap kmap,
                                                                const __grid_constant__ CUtensorMap vmap,
                                                                const __grid_constant__ CUtensorMap omap) {
+  constexpr int kNH = D / 64;   // 64-column halves
+  constexpr int kOC = D / 2;    // output columns per softmax thread
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // uniform: every thread returns before any barrier
     if (threadIdx.x == 0) raise_error(p.err, PKV_DEVERR_INTERNAL);
@@ -258,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         const int tok = b ? otok1 : otok0, head = b ? ohead1 : ohead0;
         if (lane == 0 && tok >= 0) {
           tma_store_3d(&omap, smem + kQOff + b * kQBytes, 0, head, tok);
-          tma_store_3d(&omap, smem + kQOff + b * kQBytes + kHalf, 64, head, tok);
+          if constexpr (kNH == 2) tma_store_3d(&omap, smem + kQOff + b * kQBytes + kHalf, 64, head, tok);
           bulk_commit_group();
           bulk_wait_read_all();  // the buffer may take the next Q tile
         }
@@ -315,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           break;
         }
         // a full tile of whole tokens, not a split: its epilogue stages the output
-        const int tok = (it.nrows == kMmaRows && it.part < 0) ? qstart + it.row0 / p.G : -1;
+        const int tok = (it.nrows == p.mma_unit_rows && it.part < 0) ? qstart + it.row0 / p.G : -1;
         if (qb) {
           otok1 = tok;
           ohead1 = it.kvh * p.G;
@@ -324,10 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           ohead0 = it.kvh * p.G;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bars->q_full[qb], kQBytes);
+          // the Q box: {64, G, floor(128 / G)} (whole tokens, up to 128 rows)
+          mbar_arrive_expect_tx(&bars->q_full[qb], kNH * 128 * (kMmaRows / p.G) * p.G);
           const int tok0 = qstart + it.row0 / p.G;
           tma_load_3d(smem + kQOff + qb * kQBytes, &qmap, &bars->q_full[qb], 0, it.kvh * p.G, tok0);
-          tma_load_3d(smem + kQOff + qb * kQBytes + kHalf, &qmap, &bars->q_full[qb], 64, it.kvh * p.G, tok0);
+          if constexpr (kNH == 2)
+            tma_load_3d(smem + kQOff + qb * kQBytes + kHalf, &qmap, &bars->q_full[qb], 64, it.kvh * p.G, tok0);
         }
       }
       if (ok && c >= 1) store_staged(c - 1);  // the last item's output
@@ -352,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->slot_free[qb]);
         if (done) break;
+        if (hh >= kNH) continue;  // head_dim 64: the second half does not exist
         const int nblk = (L + p.bs - 1) / p.bs;
         const int32_t* bt = p.block_tables + (int64_t)it.seq * p.max_blocks;
         for (int kbase = it.kb; kbase < it.ke; kbase += kKeys, ++g) {
@@ -391,16 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           const int sb = gs & 1, st = gs % kKStages;
           // S buffer sb: the softmax warps have read S(gs-2) from it; both halves of K(gs) loaded
           const uint32_t kph = (gs / kKStages) & 1;
-          if (!mbar_test_wait3(&bars->s_free[sb], ((gs >> 1) & 1) ^ 1, &bars->k_full[st][0], kph, &bars->k_full[st][1],
-                               kph) &&
+          uint64_t* const kf1 = &bars->k_full[st][kNH - 1];  // the second half's barrier (the first at head_dim 64)
+          if (!mbar_test_wait3(&bars->s_free[sb], ((gs >> 1) & 1) ^ 1, &bars->k_full[st][0], kph, kf1, kph) &&
               (!mbar_wait(&bars->s_free[sb], ((gs >> 1) & 1) ^ 1, p.err) ||
-               !mbar_wait(&bars->k_full[st][0], kph, p.err) || !mbar_wait(&bars->k_full[st][1], kph, p.err)))
+               !mbar_wait(&bars->k_full[st][0], kph, p.err) || !mbar_wait(kf1, kph, p.err)))
             break;
           tc_fence_after();
           const uint64_t dqb = desc_add(dq, (s_item & 1) * kQBytes);
           const uint64_t dk = desc_add(dk0, st * kTileBytes);
   #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
+          for (int kk = 0; kk < D / 16; ++kk)
             umma_bf16(tmem + kSCol + 128 * sb, desc_add(dqb, (kk >> 2) * kHalf + (kk & 3) * 32),
                       desc_add(dk, (kk >> 2) * kHalfKV + (kk & 3) * 32), kIdescS, kk > 0 ? 1u : 0u);
           umma_commit(&bars->s_full[sb]);
@@ -430,10 +443,10 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
             const int pb = gp & 1, vst = gp % kVStages;
             // P(gp) written, both halves of V(gp) loaded
             const uint32_t vph = (gp / kVStages) & 1;
-            if (!mbar_test_wait3(&bars->p_full[pb], (gp >> 1) & 1, &bars->v_full[vst][0], vph, &bars->v_full[vst][1],
-                                 vph) &&
+            uint64_t* const vf1 = &bars->v_full[vst][kNH - 1];
+            if (!mbar_test_wait3(&bars->p_full[pb], (gp >> 1) & 1, &bars->v_full[vst][0], vph, vf1, vph) &&
                 (!mbar_wait(&bars->p_full[pb], (gp >> 1) & 1, p.err) || !mbar_wait(&bars->v_full[vst][0], vph, p.err) ||
-                 !mbar_wait(&bars->v_full[vst][1], vph, p.err))) {
+                 !mbar_wait(vf1, vph, p.err))) {
               ok = false;
               break;
             }
@@ -441,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
             const uint64_t dv = desc_add(dv0, vst * kTileBytes);
   #pragma unroll
             for (int kk = 0; kk < kKeys / 16; ++kk)
-              umma_bf16_ts(tmem + kOCol, tmem + kPCol + 64 * pb + kk * 8, desc_add(dv, kk * 2048), kIdescO,
+              umma_bf16_ts(tmem + kOCol, tmem + kPCol + 64 * pb + kk * 8, desc_add(dv, kk * 2048), kIdescO<D>,
                            (j == 0 && kk == 0) ? 0u : 1u);
             umma_commit(&bars->pv_done[pb]);  // P.V(gp) complete: frees P buffer and V stage gp % 2
           }
@@ -568,16 +581,16 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           tc_fence_after();
           const float f = rescale ? alpha : 1.f;
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
+          for (int cc = 0; cc < kOC / 32; ++cc) {
             uint32_t o[32];
-            tmem_ld32(lane_base + kOCol + 64 * h + cc * 32, o);
+            tmem_ld32(lane_base + kOCol + kOC * h + cc * 32, o);
             tmem_wait_ld();
 #pragma unroll
             for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * f);
-            tmem_st32(lane_base + kOCol + 64 * h + cc * 32, o);
+            tmem_st32(lane_base + kOCol + kOC * h + cc * 32, o);
           }
         }
-        if (kt + kKeys > L) {
+        if (kt + kKeys > L && h < kNH) {
           // keys at or past the sequence's end hold arbitrary bits: zero their V
           // rows (thread: key r of the tile, d-half h) so that 0 * V stays 0
           if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[vs][h], (g / kVStages) & 1, p.err))) {
@@ -596,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         mbar_arrive(&bars->p_full[sb]);
       }
       if (!ok) break;
-      // ---- epilogue: row sum of the pair, O (this thread's 64 output columns) / l.
+      // ---- epilogue: row sum of the pair, O (this thread's D / 2 output columns) / l.
       // The sums go through the max buffer the last tile did not use; the
       // second pair barrier keeps the next tile from overwriting them early.
       float* reds = red + (g & 1) * 256;
@@ -607,39 +620,43 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       // P.V of the item's last tile (g-1) complete
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, p.err))) break;
       tc_fence_after();
-      uint32_t o[64];
-      tmem_ld32(lane_base + kOCol + 64 * h, o);
-      tmem_ld32(lane_base + kOCol + 64 * h + 32, o + 32);
+      uint32_t o[kOC];
+#pragma unroll
+      for (int cc = 0; cc < kOC / 32; ++cc) tmem_ld32(lane_base + kOCol + kOC * h + 32 * cc, o + 32 * cc);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->o_empty);
       // a full tile of whole tokens leaves through TMA stores from Q buffer qb
       // (its Q K^T are complete), in the Q tile's layout: row r, 16-byte
-      // chunk j at chunk j ^ (r & 7) of the row (128-byte swizzle)
-      const bool staged = it.nrows == kMmaRows && it.part < 0;
+      // chunk j at chunk j ^ (r & 7) of the row (128-byte swizzle); this
+      // thread's columns kOC * h .. are chunks (kOC * h % 64) / 8 .. of half
+      // kOC * h / 64
+      const bool staged = it.nrows == p.mma_unit_rows && it.part < 0;
       if (valid) {
         if (it.part < 0) {
           const float inv = 1.f / ltot;
-          uint32_t w[32];
+          uint32_t w[kOC / 2];
 #pragma unroll
-          for (int u = 0; u < 32; ++u)
+          for (int u = 0; u < kOC / 2; ++u)
             w[u] = pack_bf16(__uint_as_float(o[2 * u]) * inv, __uint_as_float(o[2 * u + 1]) * inv);
           if (staged) {
-            uint8_t* srow = smem + kQOff + qb * kQBytes + h * kHalf + r * 128;
+            uint8_t* srow = smem + kQOff + qb * kQBytes + (kOC * h / 64) * kHalf + r * 128;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+            for (int jj = 0; jj < kOC / 8; ++jj) {
+              const int j = ((kOC * h) % 64) / 8 + jj;
               *reinterpret_cast<uint4*>(srow + ((j ^ (r & 7)) << 4)) =
-                  make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                  make_uint4(w[4 * jj], w[4 * jj + 1], w[4 * jj + 2], w[4 * jj + 3]);
+            }
           } else {
             __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                  ((int64_t)(qstart + tok) * p.Hq + (int64_t)it.kvh * p.G + gh) * 128 + 64 * h;
-            store_row128(orow, w, p.out_al32);
+                                  ((int64_t)(qstart + tok) * p.Hq + (int64_t)it.kvh * p.G + gh) * D + kOC * h;
+            store_row<kOC>(orow, w, p.out_al32);
           }
         } else {
-          // this split's partial row: 256 bytes of fp32 (the workspace is 256-byte aligned)
-          float* dst = p.part_acc + (int64_t)(it.part + r) * 128 + 64 * h;
+          // this split's partial row: D fp32 (the workspace is 256-byte aligned)
+          float* dst = p.part_acc + (int64_t)(it.part + r) * D + kOC * h;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) st_global_v8(dst + 8 * u, o + 8 * u);
+          for (int u = 0; u < kOC / 8; ++u) st_global_v8(dst + 8 * u, o + 8 * u);
           if (h == 0) p.part_ml[it.part + r] = make_float2(m_ref, ltot);
         }
       }
@@ -668,17 +685,17 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
               M = fmaxf(M, __ldcg(&p.part_ml[gr.part_base + sp * gr.nrows + r]).x);
             const float Mu = M == -CUDART_INF_F ? 0.f : M;
             float lsum = 0.f;
-            float acc[64];
+            float acc[kOC];
 #pragma unroll
-            for (int cc = 0; cc < 64; ++cc) acc[cc] = 0.f;
+            for (int cc = 0; cc < kOC; ++cc) acc[cc] = 0.f;
             for (int sp = 0; sp < gr.nsplit; ++sp) {
               const int slot = gr.part_base + sp * gr.nrows + r;
               const float2 ml = __ldcg(&p.part_ml[slot]);
               const float wt = fast_exp2(ml.x - Mu);
               lsum = fmaf(wt, ml.y, lsum);
-              const float4* src = reinterpret_cast<const float4*>(p.part_acc + (int64_t)slot * 128 + 64 * h);
+              const float4* src = reinterpret_cast<const float4*>(p.part_acc + (int64_t)slot * D + kOC * h);
 #pragma unroll
-              for (int u = 0; u < 16; ++u) {
+              for (int u = 0; u < kOC / 4; ++u) {
                 const float4 a = __ldcg(src + u);
                 acc[4 * u] = fmaf(wt, a.x, acc[4 * u]);
                 acc[4 * u + 1] = fmaf(wt, a.y, acc[4 * u + 1]);
@@ -690,11 +707,11 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
             const int grow = gr.row0 + r;
             const int gtok = grow / p.G, ggh = grow - gtok * p.G;
             __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                  ((int64_t)(qstart + gtok) * p.Hq + (int64_t)gr.kvh * p.G + ggh) * 128 + 64 * h;
-            uint32_t w[32];
+                                  ((int64_t)(qstart + gtok) * p.Hq + (int64_t)gr.kvh * p.G + ggh) * D + kOC * h;
+            uint32_t w[kOC / 2];
 #pragma unroll
-            for (int u = 0; u < 32; ++u) w[u] = pack_bf16(acc[2 * u] * inv, acc[2 * u + 1] * inv);
-            store_row128(orow, w, p.out_al32);
+            for (int u = 0; u < kOC / 2; ++u) w[u] = pack_bf16(acc[2 * u] * inv, acc[2 * u + 1] * inv);
+            store_row<kOC>(orow, w, p.out_al32);
           }
         }
         named_barrier(5, 256);
@@ -708,10 +725,9 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-}  // namespace
-
-cudaError_t launch_mma(const AttnParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                       const CUtensorMap& omap, int grid, cudaStream_t s) {
+template <int D>
+cudaError_t launch_mma_t(const AttnParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                         const CUtensorMap& vmap, const CUtensorMap& omap, int grid, cudaStream_t s) {
   static unsigned long long done_mask = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -720,15 +736,23 @@ cudaError_t launch_mma(const AttnParams& p, const CUtensorMap& qmap, const CUten
   if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & (1ull << dev))) {
     // the register split needs the block launched with 128 registers per thread
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, mma_attn_kernel);
+    e = cudaFuncGetAttributes(&fa, mma_attn_kernel<D>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(mma_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    e = cudaFuncSetAttribute(mma_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, 1ull << dev, __ATOMIC_RELEASE);
   }
-  e = launch_pdl(mma_attn_kernel, dim3(grid), dim3(kThreads), kSmem, s, p, qmap, kmap, vmap, omap);
+  e = launch_pdl(mma_attn_kernel<D>, dim3(grid), dim3(kThreads), kSmem, s, p, qmap, kmap, vmap, omap);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mma(const AttnParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                       const CUtensorMap& omap, int grid, cudaStream_t s) {
+  return p.D == 64 ? launch_mma_t<64>(p, qmap, kmap, vmap, omap, grid, s)
+                   : launch_mma_t<128>(p, qmap, kmap, vmap, omap, grid, s);
 }
 
 }  // namespace pkv

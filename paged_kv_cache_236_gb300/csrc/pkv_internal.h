@@ -97,6 +97,7 @@ struct PlanParams {
   const int32_t* block_tables;
   int dec_rows_max;  // rows <= this go to the decode-shaped path when mma_ok
   int dec_unit_rows;  // rows per decode-shaped item (4 CUDA-core, 16 tensor-core)
+  int mma_unit_rows;  // rows per tensor-core item: the whole tokens that fit 128 rows, floor(128 / G) * G
   int dec_tile_keys;  // key tile of the decode-shaped kernel (splits are multiples)
   int target_dec, target_mma;  // desired item counts
   int dec_ctas;     // CTAs of the decode-shaped kernel (one wave of items)
@@ -151,6 +152,7 @@ struct AttnParams {
   float v_scale;     // output factor: the V scale for an FP8 cache, else 1
   int causal;
   int out_al32;      // out is 32-byte aligned (256-bit stores)
+  int mma_unit_rows;  // rows of a full tensor-core item: floor(128 / G) * G (whole tokens)
   // The decode kernel launches beside the tensor-core kernel, after every
   // CTA of that kernel has seen the plan complete (they signal dependents
   // only then): it skips the grid-dependency wait, which would also wait for

@@ -4,7 +4,8 @@
 // Each sequence s has n_s query tokens at positions L_s - n_s .. L_s - 1; for
 // one kv head its rows are the (token, head-in-group) pairs.  Rows are cut
 // into units - groups of kDecRows rows for the CUDA-core kernel, or tiles of
-// kMmaRows rows for the tensor-core kernel - and a unit's visible keys
+// the whole tokens that fit kMmaRows rows for the tensor-core kernel
+// (mma_unit_rows = floor(kMmaRows / G) * G) - and a unit's visible keys
 // (0 .. L - n + last_token for causal, all L otherwise) are split into
 // chunks so that the item count roughly matches the number of resident CTAs
 // times a few waves ("split-KV": long contexts and small batches still fill
@@ -68,7 +69,7 @@ __device__ __forceinline__ SeqDesc describe_base(const PlanParams& p, int s) {
             (int64_t)d.L <= (int64_t)p.max_blocks * p.bs;
   d.rows = d.valid ? d.n * p.G : 0;
   d.mma = p.mma_ok && d.rows > p.dec_rows_max;
-  d.unit_rows = d.mma ? kMmaRows : p.dec_unit_rows;
+  d.unit_rows = d.mma ? p.mma_unit_rows : p.dec_unit_rows;
   d.units = (d.rows + d.unit_rows - 1) / d.unit_rows;
   d.pre = 0;
   return d;
@@ -286,7 +287,7 @@ __device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre)
     PreGroup& pg = p.pre_groups[g];
     pg.rows = (p.query_start_loc[pg.s1 + 1] - p.query_start_loc[pg.s0]) * p.G;
     if (pg.s1 - pg.s0 + 1 < kMinGroupSeqs) continue;
-    rtiles += p.Hkv * ((pg.rows + kMmaRows - 1) / kMmaRows);
+    rtiles += p.Hkv * ((pg.rows + p.mma_unit_rows - 1) / p.mma_unit_rows);
     rows += p.Hkv * pg.rows;
   }
   {
@@ -309,7 +310,7 @@ __device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre)
     if (pg.valid) {
       const int chunk_tiles = (pg.pre_tiles + min(npre, pg.pre_tiles) - 1) / min(npre, pg.pre_tiles);
       pg.npre = (pg.pre_tiles + chunk_tiles - 1) / chunk_tiles;
-      nitems += p.Hkv * ((pg.rows + kMmaRows - 1) / kMmaRows) * pg.npre;
+      nitems += p.Hkv * ((pg.rows + p.mma_unit_rows - 1) / p.mma_unit_rows) * pg.npre;
       nrows += p.Hkv * pg.rows * pg.npre;
       ++nvalid;
     } else {
@@ -325,7 +326,7 @@ __device__ __noinline__ void plan_prefix_groups(const PlanParams p, int* sh_pre)
       pg.item_off = io;
       pg.part_off = ro;
       if (pg.valid) {
-        io += p.Hkv * ((pg.rows + kMmaRows - 1) / kMmaRows) * pg.npre;
+        io += p.Hkv * ((pg.rows + p.mma_unit_rows - 1) / p.mma_unit_rows) * pg.npre;
         ro += p.Hkv * pg.rows * pg.npre;
       }
     }
@@ -681,14 +682,14 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
     const int ng = sh_pre[3];
     // item k of a group: kv head, row tile, key chunk (chunk fastest)
     auto emit = [&](const PreGroup& pg, int k) {
-      const int rt = (pg.rows + kMmaRows - 1) / kMmaRows;
+      const int rt = (pg.rows + p.mma_unit_rows - 1) / p.mma_unit_rows;
       const int per_keys = (pg.pre_tiles + pg.npre - 1) / pg.npre * kMmaTileKeys;
       const int c = k % pg.npre, t = (k / pg.npre) % rt, kvh = k / (pg.npre * rt);
       WorkItem it;
       it.seq = pg.s0;  // the group's rows are its tokens onwards
       it.kvh = kvh;
-      it.row0 = t * kMmaRows;
-      it.nrows = min(kMmaRows, pg.rows - it.row0);
+      it.row0 = t * p.mma_unit_rows;
+      it.nrows = min(p.mma_unit_rows, pg.rows - it.row0);
       it.kb = c * per_keys;
       it.ke = min(pg.pre_tiles * kMmaTileKeys, (c + 1) * per_keys);
       it.part = pre_part_base + pg.part_off + (kvh * pg.npre + c) * pg.rows + it.row0;
@@ -699,14 +700,14 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       for (int g = 0; g < ng; ++g) {
         const PreGroup pg = p.pre_groups[g];
         if (!pg.valid) continue;
-        const int n = p.Hkv * ((pg.rows + kMmaRows - 1) / kMmaRows) * pg.npre;
+        const int n = p.Hkv * ((pg.rows + p.mma_unit_rows - 1) / p.mma_unit_rows) * pg.npre;
         for (int k = tid; k < n; k += kThreads) emit(pg, k);
       }
     } else {
       for (int g = tid; g < ng; g += kThreads) {
         const PreGroup pg = p.pre_groups[g];
         if (!pg.valid) continue;
-        const int n = p.Hkv * ((pg.rows + kMmaRows - 1) / kMmaRows) * pg.npre;
+        const int n = p.Hkv * ((pg.rows + p.mma_unit_rows - 1) / p.mma_unit_rows) * pg.npre;
         for (int k = 0; k < n; ++k) emit(pg, k);
       }
     }

@@ -409,6 +409,18 @@ def prefill_chunks(poison: bool = False, seed: int = 1003) -> Workload:
                  poison=poison, max_blocks_per_seq=512)
 
 
+def prefill_chunks_shape(num_q_heads: int, num_kv_heads: int, head_dim: int, poison: bool = False,
+                         seed: int = 1003, name: str = "prefill-shape") -> Workload:
+    """The prefill chunks' lengths (8 chunks of 512 new tokens on U[0, 2048]
+    cached, the mixed batch's draw) with other head shapes: a GQA group that
+    is not a power of two, or head_dim 64.  bf16, block_size 16."""
+    g = np.random.Generator(np.random.PCG64(seed + 7_000_000))
+    cached = g.integers(0, 2048, size=8, endpoint=True)
+    return build(name, context_lens=cached + 512, q_lens=np.full(8, 512), num_blocks=2048, block_size=16,
+                 num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim, dtype="bf16", seed=seed,
+                 poison=poison, max_blocks_per_seq=512)
+
+
 def spec_verify(poison: bool = False, seed: int = 1004) -> Workload:
     """Speculative verification, bf16: 32 sequences of 8192 tokens whose last
     5 are draft tokens (causal among themselves); 64 q / 8 kv heads, head_dim
@@ -466,6 +478,9 @@ CONFIGS = {
     "mixed": mixed_batch,
     "specverify": spec_verify,
     "prefill": prefill_chunks,
+    # the same chunks with 56 q / 8 kv heads (G = 7) and with head_dim 64
+    "prefill-g7": lambda poison=False, seed=1003: prefill_chunks_shape(56, 8, 128, poison, seed, "prefill-8x512-g7"),
+    "prefill-d64": lambda poison=False, seed=1003: prefill_chunks_shape(32, 8, 64, poison, seed, "prefill-8x512-d64"),
     "prefix": prefix_shared,
     "prefix-long": prefix_shared_long,
 }
