@@ -200,8 +200,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* empty = full + C::kStages;
   int* flag_last = reinterpret_cast<int*>(empty + C::kStages);
-  volatile int* abort_flag = flag_last + 1;
-  const WaitCtl wc{p.err, abort_flag, p.wait_ns ? p.wait_ns : kWaitTimeoutNs};
+  const WaitCtl wc{p.err, wait_limit(p.wait_ns)};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -209,7 +208,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
-    *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -224,13 +222,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p,
     }
     const int nb_per_tile = kDecTileKeys / p.bs;
     int tile = 0;
-    // On giving up: wait (bounded, whatever the abort flag says) until the
-    // copies of the last tiles issued have landed, so that none is still in
+    // On giving up: wait (bounded) until the copies of the last tiles
+    // issued have landed, so that none is still in
     // flight into this CTA's shared memory when it exits.
     auto drain = [&]() {
-      const WaitCtl dw{p.err, nullptr, wc.limit_ns};
       for (int j = max(0, tile - C::kStages); j < tile; ++j)
-        __all_sync(0xffffffffu, mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1, dw));
+        __all_sync(0xffffffffu, mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1, wc));
     };
     int idx = 0;
     if (lane == 0) idx = atomicAdd(p.counter, 1);

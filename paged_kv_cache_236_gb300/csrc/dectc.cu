@@ -52,8 +52,8 @@
 // The K scale is in the logit scale, the V scale multiplies the output.
 //
 // Bounded waits (failure detection): every wait gives up after a time limit
-// (2 s unless the call sets one) or as soon as another role of the CTA has
-// given up (an abort flag in shared memory).  Waits whose outcome decides
+// (2 s unless the call sets one); the roles that wait on one that gave up
+// run out in turn, in parallel.  Waits whose outcome decides
 // what a group of warps does next are settled across the group by a barrier
 // that ORs the failures, so that all of the group's warps go on or all
 // leave; nothing waits without a bound.  A producer that leaves first waits
@@ -281,8 +281,7 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
   Meta* meta = reinterpret_cast<Meta*>(smem + Y::kMetaOff);
   float* red = reinterpret_cast<float*>(smem + Y::kRedOff);  // [2][4 warps][NR rows]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
-  const WaitCtl wc{p.err, abort_flag, p.wait_ns ? p.wait_ns : kWaitTimeoutNs};
+  const WaitCtl wc{p.err, wait_limit(p.wait_ns)};
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Y::kStages; ++s) {
@@ -308,7 +307,6 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
       if (b == 0) mbar_init(&bars->fetch_go, 1);
       mbar_init(&bars->stage_empty[b], 128);
     }
-    *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -341,14 +339,13 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
     const int nb_per_tile = kKeys / p.bs;
     const ItemSlot* islots = reinterpret_cast<const ItemSlot*>(smem + Y::kISlotOff);
     int g = 0;
-    // On giving up: wait (bounded, whatever the abort flag says) until the
-    // copies of the tiles issued last have landed, so that none is still in
+    // On giving up: wait (bounded) until the copies of the tiles issued
+    // last have landed, so that none is still in
     // flight into this CTA's shared memory when it exits.
     uint64_t* fullb = vprod ? bars->v_full : bars->k_full;
     auto drain = [&]() {
-      const WaitCtl dw{p.err, nullptr, wc.limit_ns};
       for (int j = max(0, g - Y::kStages); j < g; ++j)
-        __all_sync(0xffffffffu, mbar_wait(&fullb[j % Y::kStages], (j / Y::kStages) & 1, dw));
+        __all_sync(0xffffffffu, mbar_wait(&fullb[j % Y::kStages], (j / Y::kStages) & 1, wc));
     };
     for (int it_cnt = 0;; ++it_cnt) {
       const int qb = it_cnt & 1;
@@ -598,9 +595,8 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
       }
       if (!ok) {
         // leaving early: let the MMAs already issued finish before TMEM is freed
-        const WaitCtl dw{p.err, nullptr, wc.limit_ns};
-        if (last_s >= 0) mbar_wait(&bars->s_full[last_s & 1], (last_s >> 1) & 1, dw);
-        if (last_pv >= 0) mbar_wait(&bars->pv_done[last_pv & 1], (last_pv >> 1) & 1, dw);
+        if (last_s >= 0) mbar_wait(&bars->s_full[last_s & 1], (last_s >> 1) & 1, wc);
+        if (last_pv >= 0) mbar_wait(&bars->pv_done[last_pv & 1], (last_pv >> 1) & 1, wc);
       }
     }
     __syncwarp();

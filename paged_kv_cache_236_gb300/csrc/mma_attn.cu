@@ -71,6 +71,17 @@
 // sharing leading blocks (their tokens are contiguous in q, from the run's
 // first sequence) over keys of that prefix.  It writes partial rows and no
 // merge; the decode kernel folds them into each member's rows.
+//
+// Bounded waits: every mbarrier wait gives up after the launch's limit
+// (default 2 s), sets PKV_DEVERR_TIMEOUT and makes its role leave; a role
+// that leaves first waits (bounded) for the copies or MMAs it has in flight,
+// so that TMEM and shared memory are not released under them.  The roles
+// that wait on one that left run out in turn, in parallel (no CTA-wide abort
+// flag: reading one inside the waits cost 8 % of the prefill rate on GB300).  The softmax warps
+// settle failures among themselves (see there); no warp is left at a named
+// barrier waiting for one that left.  The kernel instance with kFaultHook
+// (used only when a test sets the fault hook) skips one K copy so that the
+// waits for it run out.
 #include <math_constants.h>
 
 #include "pkv_device.cuh"
@@ -169,7 +180,7 @@ __device__ __forceinline__ void store_row(__nv_bfloat16* dst, const uint32_t* w,
 // output; the shared-memory and TMEM layouts are those of 128, with the
 // second halves unused at 64).  Each softmax thread owns D / 2 output
 // columns of its row.
-template <int D>
+template <int D, bool kFaultHook>
 __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams p,
                                                                const __grid_constant__ CUtensorMap qmap,
                                                                const __grid_constant__ CUtensorMap kmap,
@@ -186,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNumBars * 8);
   ItemSlot* slots = reinterpret_cast<ItemSlot*>(smem + kSlotOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WaitCtl wc{p.err, wait_limit(p.wait_ns)};
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -264,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       int otok0 = -1, otok1 = -1, ohead0 = 0, ohead1 = 0;
       auto store_staged = [&](int ci) -> bool {  // item ci's output, once its epilogue is done
         const int b = ci & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_staged[b], (ci >> 1) & 1, p.err))) return false;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_staged[b], (ci >> 1) & 1, wc))) return false;
         const int tok = b ? otok1 : otok0, head = b ? ohead1 : ohead0;
         if (lane == 0 && tok >= 0) {
           tma_store_3d(&omap, smem + kQOff + b * kQBytes, 0, head, tok);
@@ -275,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         __syncwarp();
         return true;
       };
-      int c = 0;
+      int c = 0, q_last = -1;  // the last item whose Q tile was loaded
       bool ok = true;
       for (;; ++c) {
         const int qb = c & 1;
@@ -285,8 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         // with its Q loaded.  Taking items no earlier keeps the queue's
         // largest-first order close to the order in which the SMs fall idle,
         // which is what keeps the tail short.
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_empty[qb], ((c >> 1) & 1) ^ 1, p.err) &&
-                                         mbar_wait(&bars->slot_free[qb], ((c >> 1) & 1) ^ 1, p.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_empty[qb], ((c >> 1) & 1) ^ 1, wc) &&
+                                         mbar_wait(&bars->slot_free[qb], ((c >> 1) & 1) ^ 1, wc))) {
           ok = false;
           break;
         }
@@ -341,8 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           if constexpr (kNH == 2)
             tma_load_3d(smem + kQOff + qb * kQBytes + kHalf, &qmap, &bars->q_full[qb], 64, it.kvh * p.G, tok0);
         }
+        q_last = c;
       }
       if (ok && c >= 1) store_staged(c - 1);  // the last item's output
+      // leaving early: the last Q tile's copy must have landed before the CTA exits
+      if (!ok && q_last >= 0) __all_sync(0xffffffffu, mbar_wait(&bars->q_full[q_last & 1], (q_last >> 1) & 1, wc));
       if (lane == 0) bulk_wait_all();
     } else if (warp == 2 || warp == 3 || warp == 12 || warp == 13) {
       // ================================================================ K / V producers
@@ -354,9 +369,19 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       uint8_t* const ring = smem + (is_v ? kVOff : kKOff) + hh * kHalfKV;
       int g = 0;
       bool ok = true;
+      // leaving early: wait (bounded) until the copies of the tiles issued
+      // last have landed
+      auto drain = [&]() {
+        for (int j = max(0, g - nst); j < g; ++j)
+          __all_sync(0xffffffffu, mbar_wait(is_v ? &bars->v_full[j % nst][hh] : &bars->k_full[j % nst][hh],
+                                            (j / nst) & 1, wc));
+      };
       for (int c = 0; ok; ++c) {
         const int qb = c & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->slot_full[qb], (c >> 1) & 1, p.err))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->slot_full[qb], (c >> 1) & 1, wc))) {
+          ok = false;
+          break;
+        }
         const bool done = slots[qb].done != 0;
         const WorkItem it = slots[qb].it;
         const int L = slots[qb].L;
@@ -372,28 +397,36 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           const int next_phys = (kbase + kKeys < it.ke) ? block_of(bt, nblk, kbase + kKeys) : 0;
           // K stage g % 3 is free once Q K^T(g-3) is complete; V stage g % 2
           // once P.V(g-2) is complete (phase of pv_done[g % 2])
-          if (!__all_sync(0xffffffffu, mbar_wait(is_v ? &bars->pv_done[st] : &bars->k_empty[st], ph ^ 1, p.err))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(is_v ? &bars->pv_done[st] : &bars->k_empty[st], ph ^ 1, wc))) {
             ok = false;
             break;
           }
           uint64_t* full = is_v ? &bars->v_full[st][hh] : &bars->k_full[st][hh];
           if (lane == 0) mbar_arrive_expect_tx(full, kHalfKV);
           __syncwarp();
-          if (lane < nb) tma_load_4d(ring + st * kTileBytes + lane * p.bs * 128, map, full, 64 * hh, it.kvh, 0, phys);
+          // testing only: one CTA's first K half of tile fault_tile - 1 is never
+          // loaded, so the waits for it run out
+          const bool skip = kFaultHook && p.fault_tile == g + 1 && !is_v && hh == 0 && blockIdx.x == 0;
+          if (lane < nb && !skip) tma_load_4d(ring + st * kTileBytes + lane * p.bs * 128, map, full, 64 * hh, it.kvh, 0, phys);
           phys = next_phys;
         }
       }
+      if (!ok) drain();
     } else if (warp == 1) {
       // ================================================================ Q K^T issuer
       if (lane == 0) {
         const uint64_t dq = desc_k(smem_base + kQOff);
         const uint64_t dk0 = desc_k(smem_base + kKOff);
         int gs = 0, s_item = -1, s_j = 0, s_nt = 0;
+        bool ok = true;
         for (;;) {
           if (s_j == s_nt) {  // next item: its Q tile loaded (its slot written before)
             ++s_item;
             const int qb = s_item & 1;
-            if (!mbar_wait(&bars->q_full[qb], (s_item >> 1) & 1, p.err)) break;
+            if (!mbar_wait(&bars->q_full[qb], (s_item >> 1) & 1, wc)) {
+              ok = false;
+              break;
+            }
             const bool done = slots[qb].done != 0;
             const int nt = (slots[qb].it.ke - slots[qb].it.kb + kKeys - 1) / kKeys;
             mbar_arrive(&bars->slot_free[qb]);
@@ -406,9 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           const uint32_t kph = (gs / kKStages) & 1;
           uint64_t* const kf1 = &bars->k_full[st][kNH - 1];  // the second half's barrier (the first at head_dim 64)
           if (!mbar_test_wait3(&bars->s_free[sb], ((gs >> 1) & 1) ^ 1, &bars->k_full[st][0], kph, kf1, kph) &&
-              (!mbar_wait(&bars->s_free[sb], ((gs >> 1) & 1) ^ 1, p.err) ||
-               !mbar_wait(&bars->k_full[st][0], kph, p.err) || !mbar_wait(kf1, kph, p.err)))
+              (!mbar_wait(&bars->s_free[sb], ((gs >> 1) & 1) ^ 1, wc) ||
+               !mbar_wait(&bars->k_full[st][0], kph, wc) || !mbar_wait(kf1, kph, wc))) {
+            ok = false;
             break;
+          }
           tc_fence_after();
           const uint64_t dqb = desc_add(dq, (s_item & 1) * kQBytes);
           const uint64_t dk = desc_add(dk0, st * kTileBytes);
@@ -422,6 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           ++s_j;
           ++gs;
         }
+        // leaving early: the S MMAs already issued finish before TMEM is freed
+        if (!ok && gs > 0) mbar_wait(&bars->s_full[(gs - 1) & 1], ((gs - 1) >> 1) & 1, wc);
       }
       __syncwarp();
     } else if (warp == 0) {
@@ -432,21 +469,27 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         bool ok = true;
         for (int c = 0; ok; ++c) {
           const int qb = c & 1;
-          if (!mbar_wait(&bars->slot_full[qb], (c >> 1) & 1, p.err)) break;
+          if (!mbar_wait(&bars->slot_full[qb], (c >> 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
           const bool done = slots[qb].done != 0;
           const int nt = (slots[qb].it.ke - slots[qb].it.kb + kKeys - 1) / kKeys;
           mbar_arrive(&bars->slot_free[qb]);
           if (done) break;
           // O is about to be overwritten: item c-1's epilogue must have read it
-          if (!mbar_wait(&bars->o_empty, (c & 1) ^ 1, p.err)) break;
+          if (!mbar_wait(&bars->o_empty, (c & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
           for (int j = 0; j < nt; ++j, ++gp) {
             const int pb = gp & 1, vst = gp % kVStages;
             // P(gp) written, both halves of V(gp) loaded
             const uint32_t vph = (gp / kVStages) & 1;
             uint64_t* const vf1 = &bars->v_full[vst][kNH - 1];
             if (!mbar_test_wait3(&bars->p_full[pb], (gp >> 1) & 1, &bars->v_full[vst][0], vph, vf1, vph) &&
-                (!mbar_wait(&bars->p_full[pb], (gp >> 1) & 1, p.err) || !mbar_wait(&bars->v_full[vst][0], vph, p.err) ||
-                 !mbar_wait(vf1, vph, p.err))) {
+                (!mbar_wait(&bars->p_full[pb], (gp >> 1) & 1, wc) || !mbar_wait(&bars->v_full[vst][0], vph, wc) ||
+                 !mbar_wait(vf1, vph, wc))) {
               ok = false;
               break;
             }
@@ -459,6 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
             umma_commit(&bars->pv_done[pb]);  // P.V(gp) complete: frees P buffer and V stage gp % 2
           }
         }
+        // leaving early: the P.V MMAs already issued finish before TMEM is freed
+        if (!ok && gp > 0) mbar_wait(&bars->pv_done[(gp - 1) & 1], ((gp - 1) >> 1) & 1, wc);
       }
       __syncwarp();
     }
@@ -471,11 +516,18 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
     const int pair_bar = 1 + q4;    // warps (w, w+4) of one row quarter
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
     float* red = reinterpret_cast<float*>(smem + kRedOff);
+    // A failed wait (warp-uniform) ends the warp's work on the item at once;
+    // it then takes the pair barriers the item still owes its partner
+    // (ntiles + 2 per item in all), so the partner never waits for a warp
+    // that left: the partner finishes the item, or gives up in turn when a
+    // wait of its own runs out.  All 8 warps then agree at an OR-reducing
+    // barrier (id 6)
+    // that each reaches once at the end of every item: there they all go on
+    // to the stores, or all leave.
     int g = 0;
-    bool ok = true;
-    for (int c = 0; ok; ++c) {
+    for (int c = 0;; ++c) {
       const int qb = c & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->slot_full[qb], (c >> 1) & 1, p.err))) break;
+      if (barrier_any(6, 256, !__all_sync(0xffffffffu, mbar_wait(&bars->slot_full[qb], (c >> 1) & 1, wc)))) break;
       const ItemSlot& sl = slots[qb];
       const bool done = sl.done != 0;
       const WorkItem it = sl.it;
@@ -487,12 +539,13 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
       const int tok = row / p.G, gh = row - tok * p.G;
       const int vis = valid ? min(it.ke, p.causal ? L - n + tok + 1 : L) : 0;
       float m_ref = -CUDART_INF_F, l = 0.f;
+      int owe = -1;  // after a failed wait: the pair barriers of the item not yet taken
       const int ntiles = (it.ke - it.kb + kKeys - 1) / kKeys;
       for (int j = 0; j < ntiles; ++j, ++g) {
         const int sb = g & 1, vs = g % kVStages;
         const int kt = it.kb + j * kKeys;  // first key of the tile
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (g >> 1) & 1, p.err))) {
-          ok = false;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (g >> 1) & 1, wc))) {
+          owe = ntiles - j + 2;
           break;
         }
         tc_fence_after();
@@ -561,8 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           }
         }
         // P buffer sb is free once the P.V of tile g-2, which read it, is done
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[sb], ((g >> 1) & 1) ^ 1, p.err))) {
-          ok = false;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[sb], ((g >> 1) & 1) ^ 1, wc))) {
+          owe = ntiles - j + 1;
           break;
         }
         tmem_st32(lane_base + kPCol + 64 * sb + 32 * h, pk);
@@ -574,8 +627,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
           // O must hold every earlier tile's P.V before it is scaled; the TMEM
           // accesses are warp-wide, rows that keep their max scale by 1
           // P.V(g-1) complete
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[sb ^ 1], ((g - 1) >> 1) & 1, p.err))) {
-            ok = false;
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[sb ^ 1], ((g - 1) >> 1) & 1, wc))) {
+            owe = ntiles - j + 1;
             break;
           }
           tc_fence_after();
@@ -593,8 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         if (kt + kKeys > L && h < kNH) {
           // keys at or past the sequence's end hold arbitrary bits: zero their V
           // rows (thread: key r of the tile, d-half h) so that 0 * V stays 0
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[vs][h], (g / kVStages) & 1, p.err))) {
-            ok = false;
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[vs][h], (g / kVStages) & 1, wc))) {
+            owe = ntiles - j + 1;
             break;
           }
           if (kt + r >= L) {
@@ -608,17 +661,21 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         tc_fence_before();
         mbar_arrive(&bars->p_full[sb]);
       }
-      if (!ok) break;
       // ---- epilogue: row sum of the pair, O (this thread's D / 2 output columns) / l.
       // The sums go through the max buffer the last tile did not use; the
       // second pair barrier keeps the next tile from overwriting them early.
-      float* reds = red + (g & 1) * 256;
-      reds[h * 128 + r] = l;
-      named_barrier(pair_bar, 64);
-      const float ltot = l + reds[(h ^ 1) * 128 + r];
-      named_barrier(pair_bar, 64);
-      // P.V of the item's last tile (g-1) complete
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, p.err))) break;
+      float ltot = 0.f;
+      if (owe < 0) {
+        float* reds = red + (g & 1) * 256;
+        reds[h * 128 + r] = l;
+        named_barrier(pair_bar, 64);
+        ltot = l + reds[(h ^ 1) * 128 + r];
+        named_barrier(pair_bar, 64);
+        // P.V of the item's last tile (g-1) complete
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, wc))) owe = 0;
+      }
+      for (int k = 0; k < owe; ++k) named_barrier(pair_bar, 64);
+      if (barrier_any(6, 256, owe >= 0)) break;
       tc_fence_after();
       uint32_t o[kOC];
 #pragma unroll
@@ -725,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D>
+template <int D, bool kFaultHook>
 cudaError_t launch_mma_t(const AttnParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap,
                          const CUtensorMap& vmap, const CUtensorMap& omap, int grid, cudaStream_t s) {
   static unsigned long long done_mask = 0;
@@ -736,14 +793,14 @@ cudaError_t launch_mma_t(const AttnParams& p, const CUtensorMap& qmap, const CUt
   if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & (1ull << dev))) {
     // the register split needs the block launched with 128 registers per thread
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, mma_attn_kernel<D>);
+    e = cudaFuncGetAttributes(&fa, mma_attn_kernel<D, kFaultHook>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(mma_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    e = cudaFuncSetAttribute(mma_attn_kernel<D, kFaultHook>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, 1ull << dev, __ATOMIC_RELEASE);
   }
-  e = launch_pdl(mma_attn_kernel<D>, dim3(grid), dim3(kThreads), kSmem, s, p, qmap, kmap, vmap, omap);
+  e = launch_pdl(mma_attn_kernel<D, kFaultHook>, dim3(grid), dim3(kThreads), kSmem, s, p, qmap, kmap, vmap, omap);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -751,8 +808,11 @@ cudaError_t launch_mma_t(const AttnParams& p, const CUtensorMap& qmap, const CUt
 
 cudaError_t launch_mma(const AttnParams& p, const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const CUtensorMap& omap, int grid, cudaStream_t s) {
-  return p.D == 64 ? launch_mma_t<64>(p, qmap, kmap, vmap, omap, grid, s)
-                   : launch_mma_t<128>(p, qmap, kmap, vmap, omap, grid, s);
+  if (p.fault_tile)  // testing only
+    return p.D == 64 ? launch_mma_t<64, true>(p, qmap, kmap, vmap, omap, grid, s)
+                     : launch_mma_t<128, true>(p, qmap, kmap, vmap, omap, grid, s);
+  return p.D == 64 ? launch_mma_t<64, false>(p, qmap, kmap, vmap, omap, grid, s)
+                   : launch_mma_t<128, false>(p, qmap, kmap, vmap, omap, grid, s);
 }
 
 }  // namespace pkv

@@ -99,37 +99,37 @@ __device__ __forceinline__ bool mbar_test_wait3(uint64_t* a, uint32_t pa, uint64
 }
 
 // How a kernel's bounded waits give up: the device error word that records
-// a timeout, the CTA's abort flag in shared memory (set by the first wait
-// that times out; every other wait of the CTA then gives up at once, so all
-// roles leave together), and the time limit.
+// a timeout and the time limit.  There is no CTA-wide abort flag: reading
+// one inside the waits cost several percent of the kernels' rates, and the
+// roles that wait on one that gave up run out in parallel, so a failure
+// still ends within a few limits.
 struct WaitCtl {
   int* err;
-  volatile int* abort;  // nullptr: no abort flag
-  uint64_t limit_ns;
+  uint32_t limit_ns;  // at most ~4.29 s
 };
 
+// The wait limit a kernel uses: the launch's (testing) limit, else the default.
+__device__ __forceinline__ uint32_t wait_limit(uint64_t launch_ns) {
+  return (uint32_t)(launch_ns ? launch_ns : kWaitTimeoutNs);
+}
+
 // Wait for the phase with the given parity to complete.  Returns false if it
-// has not completed within w.limit_ns (then sets PKV_DEVERR_TIMEOUT and the
-// abort flag) or once the abort flag is set.
+// has not completed within w.limit_ns (then sets PKV_DEVERR_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (w.abort && *w.abort) return false;
-      if (globaltimer() - t0 > w.limit_ns) {
-        raise_error(w.err, PKV_DEVERR_TIMEOUT);
-        if (w.abort) *w.abort = 1;
-        return false;
-      }
+    if ((i & 63u) == 0 && globaltimer() - t0 > w.limit_ns) {
+      raise_error(w.err, PKV_DEVERR_TIMEOUT);
+      return false;
     }
   }
 }
 
-// The same with the default limit and no abort flag.
+// The same with the default limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
-  return mbar_wait(bar, parity, WaitCtl{err, nullptr, kWaitTimeoutNs});
+  return mbar_wait(bar, parity, WaitCtl{err, (uint32_t)kWaitTimeoutNs});
 }
 
 // Named barrier over `nthreads` threads (whole warps) with id `id` (1..15)

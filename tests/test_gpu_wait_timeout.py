@@ -102,3 +102,33 @@ def test_tensor_core_decode_fp8_wait_runs_out(fault_tile):
     torch.cuda.synchronize()
     run.check(out, what="after the fault")
     assert pkv.device_errors() == 0
+
+
+def _prefill_batch(seed, head_dim):
+    # eight chunks of 384 new tokens after 1,500-1,800 cached ones: every CTA
+    # of the multi-token kernel works on items of 13 to 17 key tiles
+    ctx = [1900 + 40 * i for i in range(8)]
+    return wl.build("timeout-mma", context_lens=ctx, q_lens=[384] * 8, num_blocks=sum((c + 15) // 16 for c in ctx) + 8,
+                    block_size=16, num_q_heads=8, num_kv_heads=2, head_dim=head_dim, dtype="bf16", seed=seed,
+                    poison=True)
+
+
+@pytest.mark.parametrize("head_dim", [128, 64])
+@pytest.mark.parametrize("fault_tile", [1, 2, 5])
+def test_tensor_core_prefill_wait_runs_out(head_dim, fault_tile):
+    """bf16 prefill chunks: the multi-token tensor-core kernel (item fetch
+    and output stores, K and V producers, the Q K^T and P.V issuers, eight
+    softmax / epilogue warps that settle failed waits pairwise and then all
+    together before the stores)."""
+    dw = DeviceWorkload(_prefill_batch(74 + head_dim, head_dim))
+    out = dw.run_step(0)
+    check_step(dw, out, what="before the fault")
+    flags, secs = _run_with_fault(dw, fault_tile)
+    assert flags & pkv.DEVERR["timeout"], f"no timeout recorded (flags {flags:#x})"
+    assert secs < 1.5, f"the call took {secs:.2f} s: the short limit was not used"
+    st = dw.w.step
+    t = dw.step_tensors(st)
+    out = pkv.paged_attention_forward(t["q"], dw.kc, dw.vc, t["bt"], t["ctx"], t["qsl"], dw.w.scale, True)
+    torch.cuda.synchronize()
+    check_step(dw, out, what="after the fault")
+    assert pkv.device_errors() == 0
