@@ -29,7 +29,9 @@
 //             processed at about one 2 KB box per 100 cycles, under the
 //             HBM rate an SM needs, so K and V are issued by two warps;
 //   warp 1    TMEM allocation and the single thread issuing the MMAs; the
-//             P.V of tile g is issued after the S of tile g+1;
+//             P.V of tile g goes as soon as its P is written, or after the
+//             S of tile g+1 when K(g+1) lands first (a P.V held back behind
+//             a late K would hold its K/V stage, and the ring runs dry);
 //   warps 2-5 softmax (thread = key = TMEM lane);
 //   warps 6-9 epilogue (thread = output column = TMEM lane of O^T);
 //   warp 10   item fetch: shortly before the K producer needs the next item
@@ -560,7 +562,28 @@ __global__ void __launch_bounds__(Lay<F8>::kThreads, 1) dectc_kernel(const AttnP
       bool ok = true;
       for (;; ++g) {
         const int st = g % Y::kStages;
-        if (!mbar_wait(F8 ? &bars->kc_full[st] : &bars->k_full[st], (g / Y::kStages) & 1, wc)) {
+        uint64_t* const kf = F8 ? &bars->kc_full[st] : &bars->k_full[st];
+        const uint32_t kph = (g / Y::kStages) & 1;
+        if (pend >= 0) {
+          // Whichever comes first: K(g) landed (then S(g), and P.V(pend)
+          // after it, as below) or P(pend) written (then P.V(pend) now, which
+          // releases its K/V stage to the producers without waiting for K(g)).
+          const uint64_t t0 = globaltimer();
+          for (uint32_t i = 1;; ++i) {
+            if (mbar_test_wait(kf, kph)) break;
+            if (mbar_test_wait(&bars->p_full[pend & 1], (pend >> 1) & 1)) {
+              ok = issue_pv();
+              break;
+            }
+            if ((i & 63u) == 0 && globaltimer() - t0 > wc.limit_ns) {
+              raise_error(wc.err, PKV_DEVERR_TIMEOUT);
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+        }
+        if (!mbar_wait(kf, kph, wc)) {
           ok = false;
           break;
         }

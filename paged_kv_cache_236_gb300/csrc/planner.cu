@@ -22,9 +22,13 @@
 // sequence major, each sequence's units contiguous (per-sequence unit offsets
 // in shared memory); each thread walks a contiguous range of that numbering,
 // so that a long prefill sequence's many units spread over many threads.
-// Per-class totals are summed with shared-memory atomics, and each item takes
-// its slot in its class's range from a cursor (items ordered by size class;
-// within a class in no particular order, which changes no result).
+// Each sequence's (L, n) is read from global memory once and kept in shared
+// memory.  Per-class totals are summed per thread, per warp (warp
+// reductions) and then across warps; each item takes its slot from its
+// warp's cursor within its class's range (items ordered by size class;
+// within a class in no particular order, which changes no result).  Every
+// pass is thus a few shared-memory round trips, not a chain of dependent
+// global reads or contended atomics.
 //
 // Shared prefixes (when the call asks for them): consecutive decode-shaped
 // sequences whose block tables start with the same physical blocks read
@@ -75,8 +79,27 @@ __device__ __forceinline__ SeqDesc describe_base(const PlanParams& p, int s) {
   return d;
 }
 
-__device__ __forceinline__ SeqDesc describe(const PlanParams& p, int s) {
-  SeqDesc d = describe_base(p, s);
+// (L, n) of sequence s as read once from global memory; n = -1: invalid.
+// Kept in shared memory for up to kPlanSmemSeqs sequences, so that the
+// planner's later passes do not repeat the dependent global reads.
+constexpr int kPlanSmemSeqs = 4096;
+
+__device__ __forceinline__ SeqDesc describe_from(const PlanParams& p, int2 ln) {
+  SeqDesc d;
+  d.L = ln.x;
+  d.valid = ln.y >= 0;
+  d.n = d.valid ? ln.y : 0;
+  d.rows = d.valid ? d.n * p.G : 0;
+  d.mma = p.mma_ok && d.rows > p.dec_rows_max;
+  d.unit_rows = d.mma ? p.mma_unit_rows : p.dec_unit_rows;
+  d.units = (d.rows + d.unit_rows - 1) / d.unit_rows;
+  d.pre = 0;
+  return d;
+}
+
+// seq_ln: the shared-memory copy of every sequence's (L, n), or nullptr
+__device__ __forceinline__ SeqDesc describe(const PlanParams& p, int s, const int2* seq_ln = nullptr) {
+  SeqDesc d = seq_ln ? describe_from(p, seq_ln[s]) : describe_base(p, s);
   d.pre_rel = d.pre_shape = 0;
   if (p.cascade) {
     d.pre = p.seq_pre[s];
@@ -151,6 +174,7 @@ __device__ void block_scan(int (&v)[K], int (&totals)[K]) {
 struct UnitIter {
   int i, end, B, Hkv, s, u, kvh;
   SeqDesc d;
+  const int2* seq_ln;  // cached (L, n) per sequence, or nullptr
 };
 
 __device__ __forceinline__ void iter_seek(UnitIter& t, const PlanParams& p, const int* seq_off) {
@@ -164,7 +188,7 @@ __device__ __forceinline__ void iter_seek(UnitIter& t, const PlanParams& p, cons
   }
   t.s = lo;
   t.u = j - seq_off[lo];
-  t.d = describe(p, lo);
+  t.d = describe(p, lo, t.seq_ln);
 }
 
 __device__ __forceinline__ void iter_next(UnitIter& t, const PlanParams& p, const int* seq_off) {
@@ -177,7 +201,7 @@ __device__ __forceinline__ void iter_next(UnitIter& t, const PlanParams& p, cons
   while (s < t.B && seq_off[s + 1] == seq_off[s]) ++s;
   t.s = s;
   t.u = 0;
-  t.d = describe(p, s);
+  t.d = describe(p, s, t.seq_ln);
 }
 
 constexpr int kSearchWarps = 8;  // sequences per CTA of the prefix search
@@ -395,8 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
     return;
   }
   extern __shared__ int seq_off[];  // [B + 1]: first unit of each sequence (per kv head)
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.B;
+  // after seq_off (8-byte aligned): every sequence's (L, n) when B <= kPlanSmemSeqs
+  int2* const seq_ln = B <= kPlanSmemSeqs ? reinterpret_cast<int2*>(seq_off + ((B + 2) & ~1)) : nullptr;
 
   // ---- shared-prefix groups
   __shared__ int sh_pre[4];  // prefix items, prefix partial rows, groups read once, groups
@@ -413,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
     const SeqDesc d = describe(p, s);
     any_invalid |= !d.valid;
     seq_off[s] = d.units;  // 0 for an invalid sequence
+    if (seq_ln) seq_ln[s] = make_int2(d.L, d.valid ? d.n : -1);
   }
   __syncthreads();
   {
@@ -444,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   __shared__ int sh_state;
   unsigned long long w_dec = 0, w_mma = 0;
   {
-    UnitIter t{i0, i1, B, p.Hkv, 0, 0, 0, {}};
+    UnitIter t{i0, i1, B, p.Hkv, 0, 0, 0, {}, seq_ln};
     for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off))
       (t.d.mma ? w_mma : w_dec) += (unsigned long long)(unit_keys(t.d, t.u, p.G, p.causal) - t.d.pre);
   }
@@ -513,14 +540,25 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   // written (the order within a class does not change any result: every
   // item computes the same rows whichever CTA takes it, and split merges
   // follow split order).
+  // Counts are kept per thread in registers, summed per warp with warp
+  // reductions (no contended shared atomics), then across warps; each warp's
+  // exclusive base per counter is what its threads' items start from when
+  // emitted (the same threads walk the same instances in both passes).
   __shared__ int s_tot[kNumCounts];
-  __shared__ int s_cur[kNumCounts];  // emit cursors: class offsets, then the merge / partial-row cursors
+  __shared__ int s_cur[kNumCounts];           // class offsets (largest class first)
+  __shared__ int s_wcnt[kWarps][kNumCounts];  // per-warp counts, then per-warp bases
+  __shared__ int s_wcur[kWarps][kNumCounts];  // per-warp emit cursors
   for (int iter = 0;; ++iter) {
     const int cd = sh_chunk[0], cm = sh_chunk[1];
-    if (tid < kNumCounts) s_tot[tid] = 0;
-    __syncthreads();
+    int cnt[kNumCounts];
+#pragma unroll
+    for (int k = 0; k < kNumCounts; ++k) cnt[k] = 0;
+    auto add = [&](int idx, int v) {
+#pragma unroll
+      for (int k = 0; k < kNumCounts; ++k) cnt[k] += idx == k ? v : 0;
+    };
     {
-      UnitIter t{i0, i1, B, p.Hkv, 0, 0, 0, {}};
+      UnitIter t{i0, i1, B, p.Hkv, 0, 0, 0, {}, seq_ln};
       for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off)) {
         const SeqDesc& d = t.d;
         const int chunk = d.mma ? cm : cd;
@@ -528,14 +566,25 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
         const int keys = unit_keys(d, t.u, p.G, p.causal) - d.pre;
         int ns, per;
         split_of(keys, chunk, d.mma ? kMmaTileKeys : p.dec_tile_keys, ns, per);
-        if (ns > 1) atomicAdd(&s_tot[cb + size_class(per, chunk)], ns - 1);  // all splits but the last are full
-        atomicAdd(&s_tot[cb + size_class(keys - (ns - 1) * per, chunk)], 1);
+        if (ns > 1) add(cb + size_class(per, chunk), ns - 1);  // all splits but the last are full
+        add(cb + size_class(keys - (ns - 1) * per, chunk), 1);
         if (ns > 1 || d.pre > 0) {
-          atomicAdd(&s_tot[kCntMerge], 1);
-          if (ns > 1)
-            atomicAdd(&s_tot[d.mma ? kCntPartMma : kCntPartDec], ns * min(d.rows - t.u * d.unit_rows, d.unit_rows));
+          add(kCntMerge, 1);
+          if (ns > 1) add(d.mma ? kCntPartMma : kCntPartDec, ns * min(d.rows - t.u * d.unit_rows, d.unit_rows));
         }
       }
+    }
+#pragma unroll
+    for (int k = 0; k < kNumCounts; ++k) {
+      const int v = __reduce_add_sync(0xffffffffu, cnt[k]);
+      if (lane == 0) s_wcnt[warp][k] = v;
+    }
+    __syncthreads();
+    if (tid < kNumCounts) {
+      int tot = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) tot += s_wcnt[w][tid];
+      s_tot[tid] = tot;
     }
     __syncthreads();
     if (tid == 0) {
@@ -581,12 +630,25 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
           om += s_tot[kClasses + k];
         }
         s_cur[kCntMerge] = 0;
-        s_cur[kCntPartDec] = 0;  // partial rows of both kinds from one cursor
+        s_cur[kCntPartDec] = 0;  // partial rows of both kinds from one range
+        s_cur[kCntPartMma] = 0;
       }
     }
     __syncthreads();
     if (sh_state) break;
   }
+  // per-warp bases: warp w's items of counter k start after those of warps
+  // 0 .. w-1 (partial rows of both kinds share one range)
+  if (tid < kNumCounts && tid != kCntPartMma) {
+    int run = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = s_wcnt[w][tid] + (tid == kCntPartDec ? s_wcnt[w][kCntPartMma] : 0);
+      s_wcnt[w][tid] = run;
+      s_wcur[w][tid] = 0;
+      run += c;
+    }
+  }
+  __syncthreads();
   if (sh_state == 2) {  // cannot happen with capacities from workspace_layout; emit nothing
     pdl_wait();
     if (tid == 0) {
@@ -616,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
   const int cd = sh_chunk[0], cm = sh_chunk[1];
   const int pre_part_base = s_tot[kCntPartDec] + s_tot[kCntPartMma];  // prefix partial rows follow the units'
   {
-    UnitIter t{i0, i1, B, p.Hkv, 0, 0, 0, {}};
+    UnitIter t{i0, i1, B, p.Hkv, 0, 0, 0, {}, seq_ln};
     for (iter_seek(t, p, seq_off); t.i < t.end; iter_next(t, p, seq_off)) {
       const SeqDesc& d = t.d;
       const int s = t.s, u = t.u, kvh = t.kvh;
@@ -633,8 +695,8 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       if (ns > 1 || d.pre > 0) {
         // A unit after a shared prefix always names a merge group (where its
         // prefix partials are); unsplit, its one item folds them in itself.
-        grp = atomicAdd(&s_cur[kCntMerge], 1);
-        if (ns > 1) part_base = atomicAdd(&s_cur[kCntPartDec], ns * nr);
+        grp = s_wcnt[warp][kCntMerge] + atomicAdd(&s_wcur[warp][kCntMerge], 1);
+        if (ns > 1) part_base = s_wcnt[warp][kCntPartDec] + atomicAdd(&s_wcur[warp][kCntPartDec], ns * nr);
         MergeGroup g;
         g.seq = s;
         g.kvh = kvh;
@@ -658,8 +720,9 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(PlanParams p) {
       }
       const int full_cls = cbase + size_class(per, chunk);
       const int last_cls = cbase + size_class(keys - (ns - 1) * per, chunk);
-      const int full0 = ns > 1 ? atomicAdd(&s_cur[full_cls], ns - 1) : 0;
-      const int last0 = atomicAdd(&s_cur[last_cls], 1);
+      const int full0 =
+          ns > 1 ? s_cur[full_cls] + s_wcnt[warp][full_cls] + atomicAdd(&s_wcur[warp][full_cls], ns - 1) : 0;
+      const int last0 = s_cur[last_cls] + s_wcnt[warp][last_cls] + atomicAdd(&s_wcur[warp][last_cls], 1);
       for (int sp = 0; sp < ns; ++sp) {
         WorkItem it;
         it.seq = s;
@@ -744,7 +807,7 @@ cudaError_t launch_prefix_search(const PlanParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_planner(const PlanParams& p, cudaStream_t s) {
-  const size_t smem = (size_t)(p.B + 1) * sizeof(int);
+  const size_t smem = (size_t)((p.B + 2) & ~1) * sizeof(int) + (p.B <= kPlanSmemSeqs ? (size_t)p.B * sizeof(int2) : 0);
   if (p.B > kMaxPlanSeqs) return cudaErrorInvalidValue;
   static unsigned long long done_mask = 0;
   int dev = 0;
@@ -752,8 +815,11 @@ cudaError_t launch_planner(const PlanParams& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-    e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)((kMaxPlanSeqs + 1) * sizeof(int)));
+    const size_t most = ((kMaxPlanSeqs + 2) & ~1) * sizeof(int);  // seq_off alone, above kPlanSmemSeqs
+    static_assert(((kPlanSmemSeqs + 2) & ~1) * sizeof(int) + kPlanSmemSeqs * sizeof(int2) <=
+                      ((kMaxPlanSeqs + 2) & ~1) * sizeof(int),
+                  "planner shared memory");
+    e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, 1ull << dev, __ATOMIC_RELEASE);
   }
