@@ -574,12 +574,12 @@ def run_reference(args):
 # workload runs); reported as null once those sources change.  The captures
 # and their commands are summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": ("1df0dd060c35cc39", 613120000 + 4368640),  # dectc_kernel<4>, decode batch
-    "prefill": ("cecd99cff8111ed8", 81004800 + 8169728),  # mma_attn_kernel, prefill chunks
-    "specverify": ("cecd99cff8111ed8", 1076760576 + 13708288),  # mma_attn_kernel, spec-verify
-    "prefix": ("ffe453f953418479", 10567680 + 0 + 648741632 + 1411328),  # mma_attn_kernel + dectc_kernel<4>
-    "prefix-long": ("1df0dd060c35cc39", 2116710912 + 4214784),  # dectc_kernel<4>, long-context prefix-shared
-    "decode-fp8": ("1df0dd060c35cc39", 309542656 + 4083712),  # dectc_kernel<4, FP8>, decode batch with FP8 pools
+    "decode": ("1440905514f1b5cf", 613059328 + 4434176),  # dectc_kernel<4>, decode batch
+    "prefill": ("c302e2cc6bdbae4a", 81584896 + 9232384),  # mma_attn_kernel<128>, prefill chunks
+    "specverify": ("c302e2cc6bdbae4a", 1078105344 + 13638400),  # mma_attn_kernel<128>, spec-verify
+    "prefix": ("85a69a9eeb3d3422", 10571264 + 0 + 648634624 + 1286400),  # mma_attn_kernel + dectc_kernel<4>
+    "prefix-long": ("1440905514f1b5cf", 2116405760 + 4168704),  # dectc_kernel<4>, long-context prefix-shared
+    "decode-fp8": ("1440905514f1b5cf", 306806272 + 4166144),  # dectc_kernel<4, FP8>, decode batch with FP8 pools
 }
 
 
