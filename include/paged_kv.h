@@ -334,6 +334,17 @@ pkv_status pkv_device_errors(int32_t* flags, int32_t clear);
 void pkv_set_profile_events(void* start, void* stop);
 
 /*
+ * pkv_set_profile_mid_event - with profile events set, later forward calls on
+ * this thread also record `mid` (a cudaEvent_t) right after the multi-token
+ * tensor-core kernel's launch, before the decode-shaped kernel's, so that the
+ * former can be timed alone (start .. mid; start .. mid is empty when it does
+ * not launch).  The event sits between the two launches, so a call that runs
+ * both side by side runs them one after the other while it is set.  NULL
+ * turns it off.  The event stays the caller's.
+ */
+void pkv_set_profile_mid_event(void* mid);
+
+/*
  * pkv_event_elapsed_ms - milliseconds between two recorded events
  * (cudaEventElapsedTime), for events recorded by this library.  Returns
  * PKV_ERR_CUDA if either has not completed.

@@ -30,7 +30,7 @@ import torch
 
 __all__ = [
     "paged_kv_write", "paged_attention_forward", "workspace_size", "workspace_min",
-    "device_errors", "debug_fault", "set_profile_events", "profile_elapsed_ms", "lib", "LibraryError", "DEVERR",
+    "device_errors", "debug_fault", "set_profile_events", "set_profile_mid_event", "profile_elapsed_ms", "lib", "LibraryError", "DEVERR",
     "BlockManager", "OutOfBlocks", "copy_blocks", "paged_kv_write_fp8", "paged_attention_forward_fp8kv",
     "paged_kv_write_attention_forward", "paged_kv_write_attention_forward_fp8kv",
 ]
@@ -99,6 +99,8 @@ def lib() -> ctypes.CDLL:
             L.pkv_device_errors.argtypes = [ctypes.POINTER(c_i32), c_i32]
             L.pkv_set_profile_events.restype = None
             L.pkv_set_profile_events.argtypes = [c_vp, c_vp]
+            L.pkv_set_profile_mid_event.restype = None
+            L.pkv_set_profile_mid_event.argtypes = [c_vp]
             L.pkv_event_elapsed_ms.restype = c_i32
             L.pkv_event_elapsed_ms.argtypes = [c_vp, c_vp, ctypes.POINTER(c_f)]
             L.pkv_version.restype = ctypes.c_char_p
@@ -308,6 +310,12 @@ def set_profile_events(start, stop) -> None:
         lib().pkv_set_profile_events(None, None)
     else:
         lib().pkv_set_profile_events(start.cuda_event, stop.cuda_event)
+
+
+def set_profile_mid_event(mid) -> None:
+    """Also record ``mid`` (torch.cuda.Event) right after the multi-token
+    tensor-core kernel of later forward calls on this thread; ``None`` stops."""
+    lib().pkv_set_profile_mid_event(None if mid is None else mid.cuda_event)
 
 
 def profile_elapsed_ms(start, stop) -> float:

@@ -21,7 +21,7 @@
 namespace {
 
 thread_local char g_msg[512] = "";
-thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr, g_prof_mid = nullptr;
 // pkv_debug_fault: armed for the next forward call of this thread only
 thread_local int g_fault_tile = 0;
 thread_local uint64_t g_fault_wait_ns = 0;
@@ -198,6 +198,8 @@ void pkv_set_profile_events(void* start, void* stop) {
   g_prof_stop = static_cast<cudaEvent_t>(stop);
   if (!g_prof_start || !g_prof_stop) g_prof_start = g_prof_stop = nullptr;
 }
+
+void pkv_set_profile_mid_event(void* mid) { g_prof_mid = static_cast<cudaEvent_t>(mid); }
 
 pkv_status pkv_event_elapsed_ms(void* start, void* stop, float* ms) {
   if (!start || !stop || !ms) return fail(PKV_ERR_INVALID_ARG, "null argument");
@@ -566,6 +568,8 @@ static pkv_status forward_impl(const void* q, const void* k_cache, const void* v
     if ((e = launch_mma(ap, qmap, kmap_sw, vmap_sw, omap, dev->sms, s)) != cudaSuccess)
       return cuda_fail(e, "mma launch");
   }
+  if (g_prof_start && g_prof_mid && (e = cudaEventRecord(g_prof_mid, s)) != cudaSuccess)
+    return cuda_fail(e, "profile event");
   ap.counter = &header->dec_counter;
   ap.items = dec_items;
   ap.no_wait = side_by_side ? 1 : 0;
