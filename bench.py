@@ -584,9 +584,9 @@ def run_reference(args):
 # and their commands are summarised under profiles/.
 NCU_TRAFFIC = {
     "decode": ("37bf4e0f41ab35a3", 613078016 + 4111872),  # dectc_kernel<4>, decode batch
-    "prefill": ("d91b99d380b820c7", 81645312 + 9222400),  # mma_attn_kernel<128>, prefill chunks
-    "specverify": ("d91b99d380b820c7", 1078126848 + 13199104),  # mma_attn_kernel<128>, spec-verify
-    "prefix": ("062f7eecaa1f9564", 10571264 + 0 + 648672768 + 1484032),  # mma_attn_kernel + dectc_kernel<4>
+    "prefill": ("5153ddf63cdf8780", 81314048 + 9465088),  # mma_attn_kernel<128>, prefill chunks
+    "specverify": ("5153ddf63cdf8780", 1078176768 + 13722368),  # mma_attn_kernel<128>, spec-verify
+    "prefix": ("27660c8a9957e688", 10576640 + 0 + 648663296 + 1429760),  # mma_attn_kernel + dectc_kernel<4>
     "prefix-long": ("37bf4e0f41ab35a3", 2116601600 + 3866880),  # dectc_kernel<4>, long-context prefix-shared
     "decode-fp8": ("37bf4e0f41ab35a3", 306789632 + 4079104),  # dectc_kernel<4, FP8>, decode batch with FP8 pools
 }

@@ -7,7 +7,9 @@
 // call), for a work item of up to 128 rows (query token, head-in-group) of one
 // sequence and one kv head over keys [kb, ke):
 //   S = Q K^T (128 rows x 128 keys per tile, fp32 in TMEM), online softmax in
-//   registers, P (bf16) written to TMEM, O += P V (fp32 in TMEM; the tensor
+//   registers, P (bf16) written to TMEM in 8-column pieces as the
+//   exponentials produce them (the stores overlap the arithmetic, and a
+//   thread holds 8 packed words instead of 32), O += P V (fp32 in TMEM; the tensor
 //   core reads P from TMEM and V from shared memory), O / l at the end, or a
 //   partial (m, l, O) row for split-KV; the last split of a merge group to
 //   finish merges the group (atomic ticket, no waiting).
@@ -555,6 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bars->s_free[sb]);  // S buffer sb may take S(g+2)
+        // P buffer sb is free once the P.V of tile g-2, which read it, is done;
+        // the exponentials below write P to it in 8-column pieces
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[sb], ((g >> 1) & 1) ^ 1, wc))) {
+          owe = ntiles - j + 2;
+          break;
+        }
         const int nvis = vis - (kt + 64 * h);  // keys c < nvis of this half are visible
         if (nvis < 64) {
 #pragma unroll
@@ -573,18 +581,23 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
         // P of keys 64h .. 64h+63: 2^(S scale_log2 - m) packed to bf16 pairs
         // (TMEM columns 32h .. 32h+31 of P buffer sb), ps2 their sums
         const f32x2 sc2 = pk2(p.scale_log2, p.scale_log2);
-        uint32_t pk[32];
         f32x2 ps2[2];
         auto exps = [&](float m) {
           const float nm = m == -CUDART_INF_F ? 0.f : -m;
           const f32x2 nm2 = pk2(nm, nm);
           ps2[0] = ps2[1] = pk2(0.f, 0.f);
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc) {
-            const float2 x = up2(fma2(pk2(__uint_as_float(sraw[2 * cc]), __uint_as_float(sraw[2 * cc + 1])), sc2, nm2));
-            const float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
-            ps2[cc & 1] = add2(ps2[cc & 1], pk2(e0, e1));
-            pk[cc] = pack_bf16(e0, e1);
+          for (int grp = 0; grp < 4; ++grp) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int cc = grp * 8 + u;
+              const float2 x = up2(fma2(pk2(__uint_as_float(sraw[2 * cc]), __uint_as_float(sraw[2 * cc + 1])), sc2, nm2));
+              const float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
+              ps2[cc & 1] = add2(ps2[cc & 1], pk2(e0, e1));
+              pk[u] = pack_bf16(e0, e1);
+            }
+            tmem_st8(lane_base + kPCol + 64 * sb + 32 * h + 8 * grp, pk);
           }
         };
         float alpha = 1.f;
@@ -610,15 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1) mma_attn_kernel(const AttnParams 
             alpha = fast_exp2(m_ref - mx);  // 0 when m_ref is -inf
             rescale = m_ref != -CUDART_INF_F;
             m_ref = mx;
+            tmem_wait_st();  // the first pass's P pieces land before they are rewritten
             exps(m_ref);
           }
         }
-        // P buffer sb is free once the P.V of tile g-2, which read it, is done
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[sb], ((g >> 1) & 1) ^ 1, wc))) {
-          owe = ntiles - j + 1;
-          break;
-        }
-        tmem_st32(lane_base + kPCol + 64 * sb + 32 * h, pk);
         {
           const float2 a = up2(ps2[0]), b = up2(ps2[1]);
           l = fmaf(l, alpha, (a.x + a.y) + (b.x + b.y));
