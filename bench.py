@@ -583,12 +583,12 @@ def run_reference(args):
 # workload runs); reported as null once those sources change.  The captures
 # and their commands are summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": ("37bf4e0f41ab35a3", 613078016 + 4111872),  # dectc_kernel<4>, decode batch
-    "prefill": ("5153ddf63cdf8780", 81314048 + 9465088),  # mma_attn_kernel<128>, prefill chunks
-    "specverify": ("5153ddf63cdf8780", 1078176768 + 13722368),  # mma_attn_kernel<128>, spec-verify
-    "prefix": ("27660c8a9957e688", 10576640 + 0 + 648663296 + 1429760),  # mma_attn_kernel + dectc_kernel<4>
-    "prefix-long": ("37bf4e0f41ab35a3", 2116601600 + 3866880),  # dectc_kernel<4>, long-context prefix-shared
-    "decode-fp8": ("37bf4e0f41ab35a3", 306789632 + 4079104),  # dectc_kernel<4, FP8>, decode batch with FP8 pools
+    "decode": ("2a08660119772f1a", 613132032 + 4455424),  # dectc_kernel<4>, decode batch
+    "prefill": ("2db9b0567d6cce62", 81409024 + 9590784),  # mma_attn_kernel<128>, prefill chunks
+    "specverify": ("2db9b0567d6cce62", 1078138624 + 13500928),  # mma_attn_kernel<128>, spec-verify
+    "prefix": ("ebbebfeac78de688", 10575872 + 0 + 648673792 + 1372672),  # mma_attn_kernel + dectc_kernel<4>
+    "prefix-long": ("2a08660119772f1a", 2116409088 + 4201728),  # dectc_kernel<4>, long-context prefix-shared
+    "decode-fp8": ("2a08660119772f1a", 306789888 + 4071168),  # dectc_kernel<4, FP8>, decode batch with FP8 pools
 }
 
 

@@ -550,6 +550,9 @@ static pkv_status forward_impl(const void* q, const void* k_cache, const void* v
   g_fault_tile = 0;
   g_fault_wait_ns = 0;
 
+  // side by side: the decode kernel does not wait for the tensor-core grid,
+  // and the tensor-core grid starts once the planner's grid has completed
+  ap.no_wait = side_by_side ? 1 : 0;
   if (g_prof_start && (e = cudaEventRecord(g_prof_start, s)) != cudaSuccess) return cuda_fail(e, "profile event");
   if (mma_launch) {
     CUtensorMap qmap, kmap_sw, vmap_sw;
@@ -572,7 +575,6 @@ static pkv_status forward_impl(const void* q, const void* k_cache, const void* v
     return cuda_fail(e, "profile event");
   ap.counter = &header->dec_counter;
   ap.items = dec_items;
-  ap.no_wait = side_by_side ? 1 : 0;
   if (dectc && kv_fp8) {
     CUtensorMap qmap16;
     if ((st = encode_q_map(&qmap16, q, T, Hq, D, 64, G, kTcDecRows / G)) != PKV_OK) return st;

@@ -808,7 +808,15 @@ cudaError_t launch_mma_t(const AttnParams& p, const CUtensorMap& qmap, const CUt
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, 1ull << dev, __ATOMIC_RELEASE);
   }
-  e = launch_pdl(mma_attn_kernel<D, kFaultHook>, dim3(grid), dim3(kThreads), kSmem, s, p, qmap, kmap, vmap, omap);
+  if (p.no_wait) {
+    // beside the decode kernel (p.no_wait): a plain launch, which starts once
+    // the planner's grid has completed; started early, before the plan, it
+    // delayed the pair on the mixed batch
+    mma_attn_kernel<D, kFaultHook><<<dim3(grid), dim3(kThreads), kSmem, s>>>(p, qmap, kmap, vmap, omap);
+    e = cudaGetLastError();
+  } else {
+    e = launch_pdl(mma_attn_kernel<D, kFaultHook>, dim3(grid), dim3(kThreads), kSmem, s, p, qmap, kmap, vmap, omap);
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
